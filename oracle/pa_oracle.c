@@ -1,0 +1,342 @@
+/*
+ * pa_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, obviously-correct CPU statement of attention over a paged
+ * KV cache, in fp64.  It exists to check the CUDA library, never to serve
+ * it: only the tests, the smoke check and the benchmark's CPU-baseline leg
+ * load it.  It shares no code, header, table or helper with the CUDA path.
+ *
+ * Sources (web pages on paged KV caches; cited by page and section):
+ *   [SKILL] cannbot-skills "model-infer-kvcache" skill page (devpress.csdn.net)
+ *           §3.1 physical layout and logical mapping, §3.3 slot_mapping,
+ *           §3.6 data-flow overview, App. C sparse_mode / masks.
+ *   [VLLM]  "vLLM on CANN" page (lnwmold.com): the PagedKVCache class and its
+ *           read_kv gather.
+ *   [MHPQ]  "Paged KV Cache and Packed Sequence in cann-recipes-infer"
+ *           (mhpq.cn) §3.3: ops.paged_attention parameters, all-zero
+ *           context_lengths give an all-zero output.
+ *
+ * What it computes, in the pages' order:
+ *   write  : for each new token t with slot s >= 0, the row of the pool at
+ *            physical block s / block_size, offset s % block_size receives
+ *            the token's K (and V) row, bit for bit   ([SKILL] §3.1, §3.3).
+ *   gather : for sequence b and logical position j < L_b the key/value row
+ *            is pool[block_table[b][j / block_size]][j % block_size]
+ *            ([SKILL] §3.1; [VLLM] read_kv), copied into contiguous arrays.
+ *   attend : naive two-pass softmax attention over the gathered rows:
+ *            s_j = scale * q.K_j, m = max s_j, p_j = exp(s_j - m),
+ *            o = sum p_j V_j / sum p_j;  an empty key set gives o = 0
+ *            ([MHPQ] §3.3).  Decode attends to all L_b keys (sparse_mode 0);
+ *            prefill row i of a sequence with q_b queries and L_b keys
+ *            attends to keys j <= L_b - q_b + i (causal, sparse_mode 3,
+ *            aligned so the last query sees every key: [SKILL] App. C/E).
+ *
+ * Readings taken where the pages are silent (each is listed in the design
+ * notes): query head h reads KV head h / (Hq / Hkv); a negative slot means
+ * "no write"; the cache layout is [num_blocks, block_size, Hkv, D] with K and
+ * V in separate pools ([SKILL] §3.1).
+ *
+ * Inputs are raw 16-bit patterns (fp16 or bf16), decoded here exactly to
+ * double from the IEEE-754 binary16 / bfloat16 definitions.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { PAO_F16 = 0, PAO_BF16 = 1 };
+enum {
+  PAO_OK = 0,
+  PAO_ERR_ARG = 1,   /* inconsistent sizes / null pointers            */
+  PAO_ERR_SLOT = 2,  /* a slot at or beyond num_blocks * block_size    */
+  PAO_ERR_BLOCK = 3, /* a block id outside [0, num_blocks)             */
+  PAO_ERR_LEN = 4,   /* a length beyond the block table's capacity,
+                        or cu_seqlens not a valid prefix sum           */
+  PAO_ERR_NOMEM = 5
+};
+
+/* ---- exact 16-bit decoders -------------------------------------------- */
+
+/* IEEE-754 binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+double pao_f16_to_double(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 10) & 0x1f;
+  int f = h & 0x3ff;
+  double v;
+  if (e == 0)
+    v = ldexp((double)f, -24); /* subnormal: f * 2^(1-15-10) */
+  else if (e == 0x1f)
+    v = f ? NAN : INFINITY;
+  else
+    v = ldexp((double)(0x400 | f), e - 25); /* (1024+f) * 2^(e-15-10) */
+  return sign ? -v : v;
+}
+
+/* bfloat16: 1 sign, 8 exponent (bias 127), 7 fraction bits. */
+double pao_bf16_to_double(uint16_t b) {
+  int sign = (b >> 15) & 1;
+  int e = (b >> 7) & 0xff;
+  int f = b & 0x7f;
+  double v;
+  if (e == 0)
+    v = ldexp((double)f, -133); /* subnormal: f * 2^(1-127-7) */
+  else if (e == 0xff)
+    v = f ? NAN : INFINITY;
+  else
+    v = ldexp((double)(0x80 | f), e - 134); /* (128+f) * 2^(e-127-7) */
+  return sign ? -v : v;
+}
+
+static double decode16(uint16_t x, int dtype) {
+  return dtype == PAO_BF16 ? pao_bf16_to_double(x) : pao_f16_to_double(x);
+}
+
+/* Decode n patterns to doubles (used by the exhaustive decoder check). */
+void pao_decode_array(double *out, const uint16_t *in, int64_t n, int dtype) {
+  for (int64_t i = 0; i < n; ++i) out[i] = decode16(in[i], dtype);
+}
+
+int pao_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+void pao_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
+/* ---- write: new K/V rows into the pool through slot_mapping ------------ */
+
+/* Pools are [num_blocks, block_size, hkv, d] 16-bit patterns.  New rows are
+ * [n, hkv, d] with `row_stride` elements between consecutive tokens.  A
+ * negative slot is skipped; an out-of-range slot is skipped and reported.
+ * The copy is a bit copy, so no decoding happens here. */
+int pao_write(uint16_t *k_pool, uint16_t *v_pool, const uint16_t *k_new,
+              const uint16_t *v_new, int64_t row_stride,
+              const int64_t *slot_mapping, int64_t n, int hkv, int d,
+              int block_size, int64_t num_blocks) {
+  if (!k_pool || !v_pool || (n > 0 && (!k_new || !v_new || !slot_mapping)))
+    return PAO_ERR_ARG;
+  if (hkv <= 0 || d <= 0 || block_size <= 0 || num_blocks < 0 || n < 0)
+    return PAO_ERR_ARG;
+  int status = PAO_OK;
+  const int64_t row = (int64_t)hkv * d;
+  for (int64_t t = 0; t < n; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= num_blocks * (int64_t)block_size) {
+      status = PAO_ERR_SLOT;
+      continue;
+    }
+    int64_t block = slot / block_size; /* physical block id   */
+    int64_t offset = slot % block_size; /* position in block   */
+    int64_t dst = (block * block_size + offset) * row;
+    for (int64_t x = 0; x < row; ++x) {
+      k_pool[dst + x] = k_new[t * row_stride + x];
+      v_pool[dst + x] = v_new[t * row_stride + x];
+    }
+  }
+  return status;
+}
+
+/* ---- gather: one sequence's keys/values for one KV head ---------------- */
+
+/* Fills kc, vc ([len, d] doubles) with logical positions 0..len-1 of the
+ * sequence whose block-table row is `bt_row`, for KV head g. */
+static int gather(double *kc, double *vc, const uint16_t *k_pool,
+                  const uint16_t *v_pool, const int32_t *bt_row, int len,
+                  int g, int hkv, int d, int block_size, int64_t num_blocks,
+                  int dtype) {
+  for (int j = 0; j < len; ++j) {
+    int logical_block = j / block_size;
+    int offset = j % block_size;
+    int32_t block = bt_row[logical_block];
+    if (block < 0 || block >= num_blocks) return PAO_ERR_BLOCK;
+    int64_t base = (((int64_t)block * block_size + offset) * hkv + g) * d;
+    for (int x = 0; x < d; ++x) {
+      kc[(int64_t)j * d + x] = decode16(k_pool[base + x], dtype);
+      vc[(int64_t)j * d + x] = decode16(v_pool[base + x], dtype);
+    }
+  }
+  return PAO_OK;
+}
+
+/* ---- attend: naive two-pass softmax attention for one query row -------- */
+
+/* o[d] = sum_j softmax(scale * q.K_j) V_j over keys 0..n-1; o = 0 if n <= 0.
+ * `s` is caller scratch of at least n doubles. */
+static void attend(double *o, const double *q, const double *kc,
+                   const double *vc, int n, int d, double scale, double *s) {
+  if (n <= 0) {
+    for (int x = 0; x < d; ++x) o[x] = 0.0;
+    return;
+  }
+  double m = -INFINITY;
+  for (int j = 0; j < n; ++j) {
+    double dot = 0.0;
+    for (int x = 0; x < d; ++x) dot += q[x] * kc[(int64_t)j * d + x];
+    s[j] = scale * dot;
+    if (s[j] > m) m = s[j];
+  }
+  double denom = 0.0;
+  for (int j = 0; j < n; ++j) {
+    s[j] = exp(s[j] - m);
+    denom += s[j];
+  }
+  for (int x = 0; x < d; ++x) {
+    double acc = 0.0;
+    for (int j = 0; j < n; ++j) acc += s[j] * vc[(int64_t)j * d + x];
+    o[x] = acc / denom;
+  }
+}
+
+/* ---- decode: one query token per sequence ------------------------------ */
+
+/* q: [num_seqs, hq, d] patterns with q_row_stride elements between
+ * sequences (heads contiguous).  out: [num_seqs, hq, d] doubles.
+ * block_table: [num_seqs, bt_stride] int32 of which the first
+ * max_blocks_per_seq columns may be used.  context_lens: [num_seqs]. */
+int pao_decode(double *out, const uint16_t *q, int64_t q_row_stride,
+               const uint16_t *k_pool, const uint16_t *v_pool,
+               const int32_t *block_table, int64_t bt_stride,
+               int max_blocks_per_seq, const int32_t *context_lens,
+               int num_seqs, int hq, int hkv, int d, int block_size,
+               int64_t num_blocks, double scale, int dtype) {
+  if (!out || !q || !k_pool || !v_pool || !block_table || !context_lens)
+    return PAO_ERR_ARG;
+  if (hq <= 0 || hkv <= 0 || hq % hkv != 0 || d <= 0 || block_size <= 0)
+    return PAO_ERR_ARG;
+  const int group = hq / hkv;
+  int status = PAO_OK;
+  const int units = num_seqs * hkv;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int u = 0; u < units; ++u) {
+    int b = u / hkv, g = u % hkv;
+    int len = context_lens[b];
+    int err = PAO_OK;
+    if (len < 0 || (int64_t)len > (int64_t)max_blocks_per_seq * block_size)
+      err = PAO_ERR_LEN;
+    double *kc = NULL, *vc = NULL, *s = NULL, *qd = NULL;
+    if (err == PAO_OK) {
+      size_t rows = len > 0 ? (size_t)len : 1;
+      kc = (double *)malloc(rows * d * sizeof(double));
+      vc = (double *)malloc(rows * d * sizeof(double));
+      s = (double *)malloc(rows * sizeof(double));
+      qd = (double *)malloc((size_t)d * sizeof(double));
+      if (!kc || !vc || !s || !qd) err = PAO_ERR_NOMEM;
+    }
+    if (err == PAO_OK)
+      err = gather(kc, vc, k_pool, v_pool, block_table + (int64_t)b * bt_stride,
+                   len, g, hkv, d, block_size, num_blocks, dtype);
+    for (int h = g * group; h < (g + 1) * group; ++h) {
+      double *o = out + ((int64_t)b * hq + h) * d;
+      if (err != PAO_OK) {
+        for (int x = 0; x < d; ++x) o[x] = NAN;
+        continue;
+      }
+      for (int x = 0; x < d; ++x)
+        qd[x] = decode16(q[(int64_t)b * q_row_stride + (int64_t)h * d + x], dtype);
+      attend(o, qd, kc, vc, len, d, scale, s);
+    }
+    free(kc);
+    free(vc);
+    free(s);
+    free(qd);
+    if (err != PAO_OK) {
+#pragma omp critical
+      status = err;
+    }
+  }
+  return status;
+}
+
+/* ---- prefill: packed variable-length queries --------------------------- */
+
+/* q: [total_q, hq, d] patterns, sequence b owning rows cu_seqlens_q[b] ..
+ * cu_seqlens_q[b+1]-1.  context_lens[b] = L_b keys in the cache.  With
+ * `causal`, row i of sequence b attends keys 0 .. L_b - q_b + i; otherwise
+ * all L_b keys.  If `row_mask` is non-null only rows t with row_mask[t] != 0
+ * are computed (the others are left untouched).  out: [total_q, hq, d]. */
+int pao_prefill(double *out, const uint16_t *q, int64_t q_row_stride,
+                const uint16_t *k_pool, const uint16_t *v_pool,
+                const int32_t *block_table, int64_t bt_stride,
+                int max_blocks_per_seq, const int32_t *cu_seqlens_q,
+                const int32_t *context_lens, int num_seqs, int64_t total_q,
+                int hq, int hkv, int d, int block_size, int64_t num_blocks,
+                double scale, int causal, const uint8_t *row_mask, int dtype) {
+  if (!out || !q || !k_pool || !v_pool || !block_table || !cu_seqlens_q ||
+      !context_lens)
+    return PAO_ERR_ARG;
+  if (hq <= 0 || hkv <= 0 || hq % hkv != 0 || d <= 0 || block_size <= 0)
+    return PAO_ERR_ARG;
+  /* cu_seqlens must be a prefix sum: starts at 0, never decreases, ends at
+   * the packed total. */
+  if (cu_seqlens_q[0] != 0 || cu_seqlens_q[num_seqs] != total_q)
+    return PAO_ERR_LEN;
+  for (int b = 0; b < num_seqs; ++b)
+    if (cu_seqlens_q[b + 1] < cu_seqlens_q[b]) return PAO_ERR_LEN;
+  const int group = hq / hkv;
+  int status = PAO_OK;
+  const int units = num_seqs * hkv;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int u = 0; u < units; ++u) {
+    int b = u / hkv, g = u % hkv;
+    int len = context_lens[b];
+    int first = cu_seqlens_q[b];
+    int qlen = cu_seqlens_q[b + 1] - first;
+    int err = PAO_OK;
+    if (len < 0 || (int64_t)len > (int64_t)max_blocks_per_seq * block_size)
+      err = PAO_ERR_LEN;
+    int needed = 0; /* any row of this sequence requested? */
+    for (int i = 0; i < qlen; ++i)
+      if (!row_mask || row_mask[first + i]) needed = 1;
+    if (!needed) continue;
+    double *kc = NULL, *vc = NULL, *s = NULL, *qd = NULL;
+    if (err == PAO_OK) {
+      size_t rows = len > 0 ? (size_t)len : 1;
+      kc = (double *)malloc(rows * d * sizeof(double));
+      vc = (double *)malloc(rows * d * sizeof(double));
+      s = (double *)malloc(rows * sizeof(double));
+      qd = (double *)malloc((size_t)d * sizeof(double));
+      if (!kc || !vc || !s || !qd) err = PAO_ERR_NOMEM;
+    }
+    if (err == PAO_OK)
+      err = gather(kc, vc, k_pool, v_pool, block_table + (int64_t)b * bt_stride,
+                   len, g, hkv, d, block_size, num_blocks, dtype);
+    for (int i = 0; i < qlen; ++i) {
+      int64_t t = first + i;
+      if (row_mask && !row_mask[t]) continue;
+      int n = causal ? len - qlen + i + 1 : len;
+      if (n > len) n = len;
+      for (int h = g * group; h < (g + 1) * group; ++h) {
+        double *o = out + (t * hq + h) * d;
+        if (err != PAO_OK) {
+          for (int x = 0; x < d; ++x) o[x] = NAN;
+          continue;
+        }
+        for (int x = 0; x < d; ++x)
+          qd[x] = decode16(q[t * q_row_stride + (int64_t)h * d + x], dtype);
+        attend(o, qd, kc, vc, n, d, scale, s);
+      }
+    }
+    free(kc);
+    free(vc);
+    free(s);
+    free(qd);
+    if (err != PAO_OK) {
+#pragma omp critical
+      status = err;
+    }
+  }
+  return status;
+}

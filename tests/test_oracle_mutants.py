@@ -1,0 +1,191 @@
+"""The pins must be strong enough to catch plausible mistakes in the oracle.
+
+Each case below plants one mistake in a copy of the oracle's C source (on the
+CPU, in a temporary directory), builds it, and checks that at least one pin
+fails for it while the unmodified oracle passes them all."""
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from paged_kv_cache_34_gb300 import workloads as W
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "pa_oracle.c")
+
+MUTANTS = {
+    "logical_block_uses_modulo": ("int logical_block = j / block_size;",
+                                  "int logical_block = j % block_size;"),
+    "offset_uses_division": ("int offset = j % block_size;",
+                             "int offset = j / block_size;"),
+    "kv_head_ignored": ("+ offset) * hkv + g) * d;", "+ offset) * hkv + 0) * d;"),
+    "value_read_from_key_pool": ("vc[(int64_t)j * d + x] = decode16(v_pool",
+                                 "vc[(int64_t)j * d + x] = decode16(k_pool"),
+    "scale_dropped": ("s[j] = scale * dot;", "s[j] = dot;"),
+    "no_normalisation": ("o[x] = acc / denom;", "o[x] = acc;"),
+    "max_not_subtracted": ("s[j] = exp(s[j] - m);", "s[j] = exp(s[j]);"),
+    "causal_top_left": ("int n = causal ? len - qlen + i + 1 : len;",
+                        "int n = causal ? i + 1 : len;"),
+    "causal_off_by_one": ("int n = causal ? len - qlen + i + 1 : len;",
+                          "int n = causal ? len - qlen + i : len;"),
+    "f16_exponent_bias": ("v = ldexp((double)(0x400 | f), e - 25);",
+                          "v = ldexp((double)(0x400 | f), e - 24);"),
+    "bf16_subnormal_scale": ("v = ldexp((double)f, -133);",
+                             "v = ldexp((double)f, -126);"),
+    "write_offset_swapped": ("int64_t offset = slot % block_size; /* position in block   */",
+                             "int64_t offset = slot / block_size;"),
+    "decode_heads_strided": (
+        "for (int h = g * group; h < (g + 1) * group; ++h) {\n      double *o = out + ((int64_t)b * hq + h) * d;",
+        "for (int h = g; h < hq; h += hkv) {\n      double *o = out + ((int64_t)b * hq + h) * d;"),
+}
+
+
+def _build(tmp, name, replace):
+    src = open(SRC).read()
+    if replace is not None:
+        old, new = replace
+        assert src.count(old) >= 1, f"mutation site for {name} not found"
+        src = src.replace(old, new)
+    path = os.path.join(tmp, f"{name}.c")
+    open(path, "w").write(src)
+    so = os.path.join(tmp, f"lib{name}.so")
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+                    "-ffp-contract=off", path, "-o", so, "-lm"], check=True)
+    return oracle.load(so)
+
+
+def _cfg(kind, hq, hkv, d, bs, nb, lengths, placement, dtype="f16"):
+    return dict(kind=kind, num_seqs=len(lengths), lengths=("list", lengths, None),
+                num_q_heads=hq, num_kv_heads=hkv, head_dim=d, block_size=bs,
+                num_blocks=nb, placement=placement, dtype=dtype, name="m")
+
+
+def _contig(pool, x, b):
+    L = int(x.context_lens[b])
+    start = int(x.block_table[b, 0]) * x.block_size
+    flat = pool.reshape(-1, x.num_kv_heads, x.head_dim)
+    return flat[start:start + L].double().permute(1, 0, 2)
+
+
+def _pin_decode_sdpa(lib):
+    x = W.make_inputs(_cfg("decode", 8, 2, 64, 16, 40, [1, 40, 99],
+                           "identity"), seed=31)
+    out = oracle.decode(x.q, x.k_pool, x.v_pool, x.block_table,
+                        x.context_lens, 2, 16, x.scale, lib=lib)
+    for b in range(3):
+        k, v = _contig(x.k_pool, x, b), _contig(x.v_pool, x, b)
+        want = F.scaled_dot_product_attention(
+            x.q[b].double()[None, :, None], k[None], v[None], scale=x.scale,
+            enable_gqa=True)[0, :, 0]
+        if not np.allclose(out[b], want.numpy(), rtol=1e-10, atol=1e-12):
+            return False
+    return True
+
+
+def _pin_prefill_sdpa(lib):
+    x = W.make_inputs(_cfg("prefill", 4, 2, 64, 16, 40, [33, 70], "identity"),
+                      seed=37)
+    kp = oracle._u16(x.k_pool).copy()
+    vp = oracle._u16(x.v_pool).copy()
+    oracle.write(kp, vp, x.k_new, x.v_new, x.slot_mapping, 16, lib=lib)
+    out = oracle.prefill(x.q, kp, vp, x.block_table, x.cu_seqlens_q,
+                         x.context_lens, 2, 16, x.scale, dtype=oracle.F16,
+                         lib=lib)
+    kt = torch.from_numpy(kp.view(np.int16)).view(torch.float16)
+    vt = torch.from_numpy(vp.view(np.int16)).view(torch.float16)
+    cu = x.cu_seqlens_q.tolist()
+    for b in range(2):
+        k, v = _contig(kt, x, b), _contig(vt, x, b)
+        q = x.q[cu[b]:cu[b + 1]].double().permute(1, 0, 2)
+        want = F.scaled_dot_product_attention(q[None], k[None], v[None],
+                                              is_causal=True, scale=x.scale,
+                                              enable_gqa=True)[0]
+        if not np.allclose(out[cu[b]:cu[b + 1]], want.permute(1, 0, 2).numpy(),
+                           rtol=1e-10, atol=1e-12):
+            return False
+    return True
+
+
+def _pin_chunked_tail(lib):
+    # q < L rows must equal the tail rows of SDPA's full causal attention
+    x = W.make_inputs(_cfg("prefill", 4, 4, 64, 16, 40, [50], "identity"),
+                      seed=41)
+    kp = oracle._u16(x.k_pool).copy()
+    vp = oracle._u16(x.v_pool).copy()
+    oracle.write(kp, vp, x.k_new, x.v_new, x.slot_mapping, 16, lib=lib)
+    qn = 9
+    out = oracle.prefill(x.q[-qn:], kp, vp, x.block_table, [0, qn],
+                         x.context_lens, 4, 16, x.scale, dtype=oracle.F16,
+                         lib=lib)
+    kt = torch.from_numpy(kp.view(np.int16)).view(torch.float16)
+    vt = torch.from_numpy(vp.view(np.int16)).view(torch.float16)
+    k, v = _contig(kt, x, 0), _contig(vt, x, 0)
+    want = F.scaled_dot_product_attention(
+        x.q.double().permute(1, 0, 2)[None], k[None], v[None], is_causal=True,
+        scale=x.scale)[0].permute(1, 0, 2)[-qn:]
+    return np.allclose(out, want.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def _pin_decoders(lib):
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    f16 = oracle.decode16(pats, oracle.F16, lib=lib)
+    bf = oracle.decode16(pats, oracle.BF16, lib=lib)
+    want16 = pats.view(np.float16).astype(np.float64)
+    wantbf = torch.from_numpy(pats.view(np.int16)).view(torch.bfloat16).double().numpy()
+    return (np.array_equal(f16, want16, equal_nan=True)
+            and np.array_equal(bf, wantbf, equal_nan=True))
+
+
+def _pin_write(lib):
+    nb, bs, hkv, d = 4, 8, 1, 2
+    kp = np.zeros((nb, bs, hkv, d), np.uint16)
+    vp = np.zeros((nb, bs, hkv, d), np.uint16)
+    kn = np.array([[[5, 6]]], np.uint16)
+    oracle.write(kp, vp, kn, kn, np.array([2 * bs + 3]), bs, lib=lib)
+    return kp[2, 3, 0].tolist() == [5, 6] and int(kp.sum()) == 11
+
+
+def _pin_saturated_softmax(lib):
+    # With a huge scale the softmax is one-hot at the best key, so the output
+    # is that key's value row (the limit of the closed form).
+    x = W.make_inputs(_cfg("decode", 2, 2, 64, 16, 20, [60, 90], "identity"),
+                      seed=43)
+    big = 1.0e4
+    out = oracle.decode(x.q, x.k_pool, x.v_pool, x.block_table,
+                        x.context_lens, 2, 16, big, lib=lib)
+    for b in range(2):
+        k, v = _contig(x.k_pool, x, b), _contig(x.v_pool, x, b)
+        for h in range(2):
+            sc = k[h] @ x.q[b, h].double()
+            top2 = torch.topk(sc, 2).values
+            assert (top2[0] - top2[1]) * big > 60  # limit reached in fp64
+            want = v[h, int(torch.argmax(sc))].numpy()
+            if not np.allclose(out[b, h], want, rtol=0, atol=1e-12):
+                return False
+    return True
+
+
+PINS = [_pin_decode_sdpa, _pin_prefill_sdpa, _pin_chunked_tail,
+        _pin_decoders, _pin_write, _pin_saturated_softmax]
+
+
+@pytest.fixture(scope="module")
+def tmpdir_mod():
+    with tempfile.TemporaryDirectory() as d:
+        yield d
+
+
+def test_unmodified_oracle_passes_every_pin(tmpdir_mod):
+    lib = _build(tmpdir_mod, "clean", None)
+    assert all(p(lib) for p in PINS)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(tmpdir_mod, name):
+    lib = _build(tmpdir_mod, name, MUTANTS[name])
+    failed = [p.__name__ for p in PINS if not p(lib)]
+    assert failed, f"mutant {name} passed every pin"
