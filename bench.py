@@ -1,0 +1,540 @@
+"""Benchmark of the paged-KV attention hot path on GB300.
+
+One step = one pass of the path over one batch of the llama7b-decode workload
+(8 sequences, context ~ U[512, 2048], 32 heads, head_dim 128, block_size 16,
+8192-block pool, bf16): write each sequence's new token into the pool through
+slot_mapping, then paged decode over the whole context (split-KV partitions
+plus the log-sum-exp combine).  The headline value is the K/V bytes the step
+must read from HBM divided by the step's device time, with L2 flushed between
+timed steps.  The same line carries two secondary measurements (the
+packed-prefill workload in TFLOP/s and the long-context decode workload in
+GB/s), the roofline of the dominant kernel, the oracle's CPU time, and an
+end-to-end figure through host buffers.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With --gpus N > 1 (launched by torchrun) every rank runs its own batch on its
+own GPU (the decode batch shards by sequence: weak scaling, no data-path
+collective); the value is all ranks' bytes over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+HEADLINE = "llama7b-decode"
+METRIC = "paged-decode KV-read GB/s (% of HBM peak); varlen prefill TFLOP/s"
+L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work
+# ---------------------------------------------------------------------------
+def kv_read_bytes(x) -> int:
+    """K and V bytes decode must read: every context position, every KV head."""
+    return int(x.context_lens.sum().item()) * x.num_kv_heads * x.head_dim * 2 * 2
+
+
+def decode_bytes(x) -> int:
+    """All HBM bytes the decode launch needs: K/V, q in, out, the block-table
+    entries it walks, context_lens."""
+    s, hq, d, bs = x.num_seqs, x.num_q_heads, x.head_dim, x.block_size
+    blocks = int(((x.context_lens + bs - 1) // bs).sum().item())
+    return kv_read_bytes(x) + 2 * s * hq * d * 2 + blocks * 4 + s * 4
+
+
+def write_bytes(x) -> int:
+    n = int(x.slot_mapping.numel())
+    return 2 * n * x.num_kv_heads * x.head_dim * 2 * 2 + n * 8
+
+
+def prefill_flops(x) -> int:
+    """4 * Hq * D per visible (query, key) pair (QK^T and PV), causal
+    bottom-right: row i of a sequence with q queries, L keys sees L-q+i+1."""
+    q = x.q_lens.long()
+    L = x.context_lens.long()
+    if x.causal:
+        pairs = (q * (L - q) + q * (q + 1) // 2).sum().item()
+    else:
+        pairs = (q * L).sum().item()
+    return int(4 * x.num_q_heads * x.head_dim * pairs)
+
+
+# ---------------------------------------------------------------------------
+# device-side helpers
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        mhz, maxmhz, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [c.strip() for c in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                maxmhz = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": maxmhz,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+def flush_l2(buf):
+    """Write a buffer larger than L2, then read a second one: the write
+    evicts every useful line, the read evicts the write's dirty lines, so their
+    write-back happens here (untimed) and not inside the next timed step."""
+    buf[0].add_(1)
+    buf[1].sum()
+
+
+def time_steps(step, k, flush_buf, stream):
+    """Per-step device time (ms) with CUDA events on the launching stream, L2
+    flushed (untimed) before each step."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
+    for i in range(k):
+        flush_l2(flush_buf)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def source_hash(*names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "paged_kv_cache_34_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str, src_hash: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of the kernel."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        m = re.match(r"\s*(\S+)\s+(\S+)\s+src=(\w+)\s+dram_bytes_per_launch=(\d+)", line)
+        if m and m.group(1) == kernel and m.group(2) == workload and m.group(3) == src_hash:
+            return int(m.group(4))
+    return None
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# the steps
+# ---------------------------------------------------------------------------
+def decode_step_fn(pa, x, out, ws, stream):
+    def step():
+        if x.slot_mapping.numel():
+            pa.pa_reshape_and_cache(x.k_new, x.v_new, x.k_pool, x.v_pool, x.slot_mapping,
+                                    stream=stream)
+        pa.pa_decode(out, x.q, x.k_pool, x.v_pool, x.block_table, x.context_lens,
+                     scale=x.scale, max_context_len=x.max_context_len,
+                     partition_size=x.partition_size, workspace=ws, stream=stream)
+    return step
+
+
+def decode_workspace(pa, x):
+    part, need = pa.pa_decode_plan(x.num_seqs, x.num_q_heads, x.num_kv_heads, x.head_dim,
+                                   x.max_context_len, x.partition_size)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda") if need else None
+    nparts = math.ceil(x.max_context_len / part) if x.max_context_len else 1
+    return ws, part, nparts
+
+
+def bench_decode(pa, W, name, steps, warmup, flush_buf, stream, seed=None):
+    x = W.make_inputs(name, seed=seed, device="cuda")
+    out = torch.empty_like(x.q)
+    ws, part, nparts = decode_workspace(pa, x)
+    step = decode_step_fn(pa, x, out, ws, stream)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    t_step = time_steps(step, steps, flush_buf, stream)
+    # the decode launch alone (for its roofline), same conditions
+    def dec():
+        pa.pa_decode(out, x.q, x.k_pool, x.v_pool, x.block_table, x.context_lens,
+                     scale=x.scale, max_context_len=x.max_context_len,
+                     partition_size=x.partition_size, workspace=ws, stream=stream)
+    t_dec = time_steps(dec, steps, flush_buf, stream)
+    return x, out, ws, part, nparts, t_step, t_dec
+
+
+def bench_prefill(pa, W, steps, warmup, flush_buf, stream):
+    x = W.make_inputs("packed-prefill", device="cuda")
+    out = torch.empty_like(x.q)
+
+    def pre():
+        pa.pa_prefill_varlen(out, x.q, x.k_pool, x.v_pool, x.block_table, x.cu_seqlens_q,
+                             x.context_lens, scale=x.scale, max_seqlen_q=x.max_seqlen_q,
+                             max_context_len=x.max_context_len, causal=True, stream=stream)
+
+    def step():
+        pa.pa_reshape_and_cache(x.k_new, x.v_new, x.k_pool, x.v_pool, x.slot_mapping,
+                                stream=stream)
+        pre()
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    t_step = time_steps(step, steps, flush_buf, stream)
+    t_pre = time_steps(pre, steps, flush_buf, stream)
+    return x, t_step, t_pre
+
+
+def e2e_decode(pa, W, name, steps, warmup, stream):
+    """Through host buffers: each step copies its inputs from pinned host
+    memory, runs write + decode, and copies the output back."""
+    x = W.make_inputs(name, device="cuda")
+    host = {k: getattr(x, k).cpu().pin_memory() for k in
+            ("q", "k_new", "v_new", "slot_mapping", "context_lens", "block_table")}
+    dev = {k: torch.empty_like(getattr(x, k)) for k in host}
+    out_h = torch.empty(x.q.shape, dtype=x.q.dtype).pin_memory()
+    out_d = torch.empty_like(x.q)
+    ws, _, _ = decode_workspace(pa, x)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def step():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        if dev["slot_mapping"].numel():
+            pa.pa_reshape_and_cache(dev["k_new"], dev["v_new"], x.k_pool, x.v_pool,
+                                    dev["slot_mapping"], stream=stream)
+        pa.pa_decode(out_d, dev["q"], x.k_pool, x.v_pool, dev["block_table"],
+                     dev["context_lens"], scale=x.scale, max_context_len=x.max_context_len,
+                     partition_size=x.partition_size, workspace=ws, stream=stream)
+        out_h.copy_(out_d, non_blocking=True)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    flush = torch.zeros(2, L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    times = []
+    for _ in range(steps):
+        flush_l2(flush)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        step()
+        torch.cuda.synchronize()
+        times.append((time.perf_counter() - t0) * 1e3)
+    return kv_read_bytes(x), times, h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle on the host cores
+# ---------------------------------------------------------------------------
+def oracle_decode_rate(x_dev, budget_s: float, max_calls: int | None = None):
+    """The oracle's write + decode over sequences of the workload, repeated
+    until ~budget_s of CPU time; returns (GB/s of K/V read, sample text,
+    threads, calls, seconds)."""
+    import oracle
+    x = x_dev.to("cpu")
+    kp = oracle._u16(x.k_pool)
+    vp = oracle._u16(x.v_pool)
+    lib = oracle.load()
+    threads = oracle.max_threads(lib)
+    kv_per_seq = (x.context_lens.long() * x.num_kv_heads * x.head_dim * 4).tolist()
+    # one call = one sequence's write + decode (all heads); cycle through them
+    nbytes, calls, t0 = 0, 0, time.perf_counter()
+    cu = 0
+    slots = x.slot_mapping
+    while True:
+        b = calls % x.num_seqs
+        n_new = int(x.new_lens[b])
+        if n_new:
+            oracle.write(kp, vp, x.k_new[cu:cu + n_new], x.v_new[cu:cu + n_new],
+                         slots[cu:cu + n_new], x.block_size, lib=lib)
+        cu = (cu + n_new) % max(1, slots.numel())
+        oracle.decode(x.q[b:b + 1], kp, vp, x.block_table[b:b + 1], x.context_lens[b:b + 1],
+                      x.num_kv_heads, x.block_size, x.scale, lib=lib)
+        nbytes += kv_per_seq[b]
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_calls and calls >= max_calls):
+            break
+    return nbytes / el / 1e9, calls, threads, el
+
+
+# ---------------------------------------------------------------------------
+def dist_setup(gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        rank = dist.get_rank()
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", rank)))
+        return dist, rank, world
+    torch.cuda.set_device(0)
+    return None, 0, 1
+
+
+def reduce_max(dist, v: float) -> float:
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(dist, v: float) -> float:
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def run_reference(args):
+    """The oracle (the path's plain fp64 CPU statement) timed on the host
+    cores on bounded samples of the same workload and metric."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from paged_kv_cache_34_gb300 import workloads as W
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    x = W.make_inputs(HEADLINE, device=dev)
+    per_step = max(0.02, min(2.0, 60.0 / max(1, args.steps + args.warmup)))
+    oracle_decode_rate(x, per_step * args.warmup, max_calls=max(1, args.warmup))
+    rates, calls_total, secs = [], 0, 0.0
+    threads = 1
+    for _ in range(args.steps):
+        r, calls, threads, el = oracle_decode_rate(x, per_step)
+        rates.append(r)
+        calls_total += calls
+        secs += el
+    value = calls_total and sum(rates) / len(rates)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs * 1e3 / max(1, args.steps), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": HEADLINE, "sequences": 8, "context": "U[512,2048]",
+                   "heads": "32/32", "head_dim": 128, "block_size": 16, "pool_blocks": 8192},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"{calls_total} single-sequence write+decode oracle calls "
+                                   f"(~{per_step:.2f} s per step) cycling the 8 sequences"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def run_only(pa, W, args, flush_buf, stream):
+    """One kernel's workload alone, without the e2e, secondary and CPU legs."""
+    if args.only == "decode":
+        x, _, _, part, nparts, _, t = bench_decode(pa, W, HEADLINE, args.steps, args.warmup,
+                                                   flush_buf, stream)
+        ms = statistics.fmean(t)
+        print(json.dumps({"only": "decode", "workload": HEADLINE, "ms": round(ms, 5),
+                          "GBps": round(decode_bytes(x) / (ms * 1e-3) / 1e9, 1),
+                          "partition_size": part, "partitions": nparts}))
+    else:
+        x, _, t = bench_prefill(pa, W, args.steps, args.warmup, flush_buf, stream)
+        ms = statistics.fmean(t)
+        print(json.dumps({"only": "prefill", "workload": "packed-prefill", "ms": round(ms, 5),
+                          "TFLOPs": round(prefill_flops(x) / (ms * 1e-3) / 1e12, 1)}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the packed-prefill and long-context measurements")
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle time for the CPU baseline")
+    ap.add_argument("--only", choices=["decode", "prefill"],
+                    help="time one kernel's workload alone (a small profiling target)")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    import paged_kv_cache_34_gb300 as pa
+    from paged_kv_cache_34_gb300 import build as pabuild
+    from paged_kv_cache_34_gb300 import workloads as W
+    if not pabuild.up_to_date():
+        pabuild.build()
+    dist, rank, world = dist_setup(args.gpus)
+    stream = torch.cuda.current_stream()
+    flush_buf = torch.zeros(2, L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    hbm_peak, tf_peak, tf_sustained, peak_kind = measured_peaks()
+    if args.only:
+        run_only(pa, W, args, flush_buf, stream)
+        return
+
+    # ---- headline: write + decode on the llama7b-decode workload ----------
+    seed = W.default_seed(HEADLINE) + 7919 * rank  # each rank its own batch
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        x, out, ws, part, nparts, t_step, t_dec = bench_decode(
+            pa, W, HEADLINE, args.steps, args.warmup, flush_buf, stream, seed=seed)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if dist is not None:
+        dist.barrier()
+    ms_step = statistics.fmean(t_step)
+    ms_step_max = reduce_max(dist, ms_step)
+    kv = kv_read_bytes(x)
+    total_kv = reduce_sum(dist, kv)  # every rank's own batch
+    value = total_kv / (ms_step_max * 1e-3) / 1e9
+    launches_per_step = (1 if x.slot_mapping.numel() else 0) + 1 + (1 if nparts > 1 else 0)
+
+    ms_dec = statistics.fmean(t_dec)
+    dec_achieved = decode_bytes(x) / (ms_dec * 1e-3) / 1e9
+    dec_hash = source_hash("decode.cu", "pa_device.cuh")
+    traffic = recorded_traffic("pa_decode", HEADLINE, dec_hash)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step_max, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": HEADLINE, "sequences_per_gpu": x.num_seqs,
+                   "context": "U[512,2048]", "heads": "32/32", "head_dim": 128,
+                   "block_size": 16, "pool_blocks": 8192, "partition_size": part,
+                   "partitions": nparts, "kv_bytes_per_step": kv,
+                   "l2": "flushed before every timed step (512 MB write, then 512 MB read)",
+                   "parallelism": f"replica x{world}" if world > 1 else "single GPU",
+                   "wall_s_timed_region": round(wall, 3),
+                   "pct_of_hbm_peak": round(100 * value / world / hbm_peak, 2)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+        "roofline": {"kernel": "pa_decode (partition + combine launches)", "bound": "hbm",
+                     "achieved": round(dec_achieved, 1), "peak": hbm_peak,
+                     "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(dec_achieved / hbm_peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": decode_bytes(x),
+                     "ms_per_launch": round(ms_dec, 5)},
+    }
+
+    if rank == 0:
+        # ---- e2e through host buffers ----------------------------------
+        kv_e2e, t_e2e, h2d, d2h = e2e_decode(pa, W, HEADLINE, max(20, args.steps // 4),
+                                             args.warmup, stream)
+        line["e2e"] = {"value": round(kv_e2e / (statistics.fmean(t_e2e) * 1e-3) / 1e9, 2),
+                       "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": round(statistics.fmean(t_e2e), 5)}
+
+        if not args.no_secondary:
+            sec = {}
+            xp, t_pstep, t_pre = bench_prefill(pa, W, max(10, args.steps // 10), args.warmup,
+                                               flush_buf, stream)
+            fl = prefill_flops(xp)
+            ms_pre = statistics.fmean(t_pre)
+            tf = fl / (ms_pre * 1e-3) / 1e12
+            sec["packed-prefill"] = {
+                "value": round(tf, 2), "unit": "TFLOP/s", "flops": fl,
+                "ms_prefill": round(ms_pre, 5),
+                "ms_write_plus_prefill": round(statistics.fmean(t_pstep), 5),
+                "write_GBps": round(write_bytes(xp) / ((statistics.fmean(t_pstep) - ms_pre)
+                                                      * 1e-3) / 1e9, 1),
+                "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": tf_peak,
+                             "peak_kind": f"{peak_kind} bf16 burst", "unit": "TFLOP/s",
+                             "frac": round(tf / tf_peak, 4),
+                             "traffic": recorded_traffic(
+                                 "pa_prefill_varlen", "packed-prefill",
+                                 source_hash("prefill.cu", "pa_tcgen05.cuh"))}}
+            del xp
+            xl, _, _, partl, npl, t_lstep, t_ldec = bench_decode(
+                pa, W, "long-context-decode", max(10, args.steps // 10), args.warmup,
+                flush_buf, stream)
+            ms_l = statistics.fmean(t_ldec)
+            gb = decode_bytes(xl) / (ms_l * 1e-3) / 1e9
+            sec["long-context-decode"] = {
+                "value": round(kv_read_bytes(xl) / (ms_l * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_decode": round(ms_l, 5), "partition_size": partl, "partitions": npl,
+                "roofline": {"bound": "hbm", "achieved": round(gb, 1), "peak": hbm_peak,
+                             "unit": "GB/s", "frac": round(gb / hbm_peak, 4),
+                             "traffic": recorded_traffic("pa_decode", "long-context-decode",
+                                                         dec_hash)}}
+            del xl
+            line["secondary"] = sec
+
+        # ---- the oracle on the host cores -------------------------------
+        r, calls, threads, el = oracle_decode_rate(x, args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(r, 4), "unit": "GB/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"{calls} single-sequence write+decode oracle calls "
+                                          f"({el:.1f} s) cycling the workload's 8 sequences"}
+        print(json.dumps(line))
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,234 @@
+/*
+ * pa.h -- C ABI of the paged-KV attention library (libpa.so), sm_103a.
+ *
+ * Three operations make up the hot path of attention over a paged KV cache:
+ *
+ *   pa_reshape_and_cache  write new K/V rows into the physical block pool
+ *                         through slot_mapping;
+ *   pa_decode             one query token per sequence against its blocks,
+ *                         online softmax, split-KV log-sum-exp combine;
+ *   pa_prefill_varlen     causal attention for cu_seqlens-packed queries
+ *                         against the paged cache.
+ *
+ * Sources (web pages on paged KV caches, cited by page and section):
+ *   [SKILL] cannbot-skills "model-infer-kvcache" skill page: §3.1 physical
+ *           layout and logical mapping, §3.3 slot_mapping, §3.4
+ *           actual_seq_lengths, §3.6 data flow, App. C sparse_mode, App. E
+ *           prefill vs decode parameters.
+ *   [MHPQ]  "Paged KV Cache and Packed Sequence in cann-recipes-infer":
+ *           §3.3 the paged_attention operator's parameters.
+ *   [LQNN]  "Paged KV Cache is infrastructure, not a renamed cache": §3.1
+ *           cu_seqlens, §4.4 packed attention, §4.5 cache update, §5.1 pitch.
+ *   [VLLM]  "vLLM on CANN": PagedKVCache.read_kv and the block-wise online
+ *           softmax of its attention kernel.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is caller-owned DEVICE memory on the current
+ *    CUDA device unless stated otherwise.  The library never allocates,
+ *    frees, synchronises, or reads device memory on the host; every kernel is
+ *    enqueued on `stream` (a cudaStream_t passed as void*; NULL = the legacy
+ *    default stream) and the call returns before it runs.
+ *  - Strides are in ELEMENTS.  Element type is fp16 or bf16 (`dtype`); every
+ *    K/V/Q/out pointer must be 16-byte aligned and every row stride a
+ *    multiple of 8 elements.
+ *  - Cache layout ([SKILL] §3.1): key_cache and value_cache are separate,
+ *    contiguous [num_blocks, block_size, num_kv_heads, head_dim] pools.  A
+ *    physical slot s addresses row s of the pool viewed as
+ *    [num_blocks * block_size, num_kv_heads, head_dim], i.e. block
+ *    s / block_size, offset s % block_size.
+ *  - block_table is int32 [num_seqs, block_table_stride]; entry [b, i] is the
+ *    physical block of logical block i of sequence b ([SKILL] §3.1-3.2).
+ *    Only the first ceil(context_len / block_size) entries of a row are
+ *    read; max_blocks_per_seq (<= block_table_stride) bounds the capacity.
+ *  - Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *  - `scale` multiplies q.k and has NO default: the pages warn that a
+ *    silently defaulted 1.0 corrupts results ([SKILL] App. A).
+ *  - Host-detectable argument errors return a pa_status and enqueue nothing.
+ *    Data-dependent errors found on the device (a bad slot, block id,
+ *    cu_seqlens entry or context length) skip the affected unit of work and
+ *    OR a PA_DEVERR_* bit into *d_error when d_error is non-NULL (an int32 in
+ *    device memory the caller zeroes and reads).  No kernel traps, asserts or
+ *    waits without a bound: a pipeline wait that exceeds its iteration limit
+ *    sets PA_DEVERR_TIMEOUT and the block returns.
+ *  - Outputs of sequences with context_len == 0, and of causal rows that see
+ *    no key, are written as zeros ([MHPQ] §3.3: all-zero context lengths
+ *    give an all-zero output).
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_ABI_VERSION 1
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_NULL = 1,        /* a required pointer is NULL                      */
+  PA_ERR_SHAPE = 2,       /* inconsistent or negative sizes / strides        */
+  PA_ERR_UNSUPPORTED = 3, /* valid but not built (head_dim, block_size, ...)  */
+  PA_ERR_ALIGN = 4,       /* pointer not 16-byte aligned or stride not x8    */
+  PA_ERR_WORKSPACE = 5,   /* workspace missing or smaller than required      */
+  PA_ERR_CUDA = 6         /* a CUDA runtime call failed (pa_last_cuda_error) */
+} pa_status;
+
+typedef enum pa_dtype { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Bits OR-ed into *d_error by the kernels. */
+#define PA_DEVERR_SLOT 1       /* slot_mapping entry >= num_blocks*block_size */
+#define PA_DEVERR_BLOCK_ID 2   /* block_table entry outside [0, num_blocks)   */
+#define PA_DEVERR_CU_SEQLENS 4 /* cu_seqlens not a prefix sum of the batch    */
+#define PA_DEVERR_CONTEXT 8    /* context_len < 0, > capacity or > host hint  */
+#define PA_DEVERR_TIMEOUT 16   /* a bounded pipeline wait gave up             */
+
+/* ABI version the library was built with (PA_ABI_VERSION). */
+int32_t pa_abi_version(void);
+
+/* Static, human-readable name of a status code. */
+const char *pa_status_string(pa_status status);
+
+/* cudaError_t of the most recent PA_ERR_CUDA on the calling thread (0 if
+ * none). */
+int32_t pa_last_cuda_error(void);
+
+/*
+ * pa_reshape_and_cache -- write this step's K/V rows into the pools.
+ *
+ * Defines ([SKILL] §3.3, App. D; [LQNN] §4.5): for each token t in
+ * [0, num_tokens) with s = slot_mapping[t]:
+ *     s <  0                     -> nothing is written (padding token);
+ *     s >= num_blocks*block_size -> nothing is written, PA_DEVERR_SLOT;
+ *     otherwise key_cache row s   = key[t]   (bit copy, all heads),
+ *               value_cache row s = value[t].
+ *
+ *   key, value      [num_tokens, num_kv_heads, head_dim]; token t starts at
+ *                   element t * kv_row_stride (heads contiguous, so K and V
+ *                   may be views into an interleaved QKV buffer).
+ *   key_cache,
+ *   value_cache     pools as described above; written, never read.
+ *   slot_mapping    int64 [num_tokens].  Duplicate non-negative slots in one
+ *                   call are a caller error (which row wins is unspecified).
+ *   d_error         nullable device int32, see above.
+ * Requirements: num_kv_heads * head_dim * 2 bytes a multiple of 16.
+ * num_tokens == 0 enqueues nothing and returns PA_OK.
+ */
+pa_status pa_reshape_and_cache(const void *key, const void *value,
+                               int64_t kv_row_stride, void *key_cache,
+                               void *value_cache, const int64_t *slot_mapping,
+                               int32_t num_tokens, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t block_size,
+                               int64_t num_blocks, pa_dtype dtype,
+                               int32_t *d_error, void *stream);
+
+/*
+ * pa_decode_plan -- the split-KV plan pa_decode will use.
+ *
+ * Long contexts are split into partitions of *partition_size_out tokens; each
+ * partition's softmax state (max, sum, unnormalised output) is combined by
+ * log-sum-exp.  partition_size == 0 picks a size from max_context_len, the
+ * batch shape and the current device's SM count; a non-zero value must be a
+ * positive multiple of 64 and is used as given.  *workspace_bytes_out is the
+ * device workspace pa_decode needs (0 when no sequence can span two
+ * partitions).  Host-only; enqueues nothing.
+ */
+pa_status pa_decode_plan(int32_t num_seqs, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim,
+                         int32_t max_context_len, int32_t partition_size,
+                         int32_t *partition_size_out,
+                         size_t *workspace_bytes_out);
+
+/*
+ * pa_decode -- paged attention for one query token per sequence.
+ *
+ * Defines ([SKILL] §3.1, §3.6, App. C sparse_mode 0; [MHPQ] §3.3; [VLLM]):
+ * for sequence b, query head h, KV head g = h / (Hq/Hkv), L = context_lens[b]
+ *     K_j = key_cache[block_table[b, j / block_size], j % block_size, g, :]
+ *     V_j likewise from value_cache,   j = 0 .. L-1 (no mask)
+ *     out[b, h, :] = sum_j softmax_j(scale * q[b, h, :] . K_j) V_j,
+ * accumulated in fp32 and rounded to dtype (nearest-even); 0 when L == 0.
+ * context_lens counts the token written this step ([SKILL] §3.6:
+ * actual_seq_lengths_kv = kv_len + 1), so write first, then decode.
+ *
+ *   out             [num_seqs, num_q_heads, head_dim], row stride
+ *                   out_row_stride (elements between sequences).
+ *   query           [num_seqs, num_q_heads, head_dim], row stride
+ *                   q_row_stride.
+ *   block_table     int32 [num_seqs, block_table_stride].
+ *   context_lens    int32 [num_seqs].
+ *   max_context_len host upper bound of context_lens (the pages'
+ *                   max_context_len); sizes the grid.  A larger device value
+ *                   is clamped to it and flagged PA_DEVERR_CONTEXT.
+ *   partition_size  as for pa_decode_plan (0 = auto).
+ *   workspace       device scratch of at least the planned bytes, 256-byte
+ *                   aligned; may be NULL when the plan needs 0 bytes.
+ * Supported: head_dim 64 or 128; num_q_heads / num_kv_heads in 1..8;
+ * block_size 8, 16, 32, 64 or 128.
+ */
+pa_status pa_decode(void *out, int64_t out_row_stride, const void *query,
+                    int64_t q_row_stride, const void *key_cache,
+                    const void *value_cache, const int32_t *block_table,
+                    int64_t block_table_stride, int32_t max_blocks_per_seq,
+                    const int32_t *context_lens, int32_t num_seqs,
+                    int32_t num_q_heads, int32_t num_kv_heads,
+                    int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                    float scale, int32_t max_context_len,
+                    int32_t partition_size, void *workspace,
+                    size_t workspace_bytes, pa_dtype dtype, int32_t *d_error,
+                    void *stream);
+
+/*
+ * pa_prefill_varlen -- causal attention for packed variable-length queries.
+ *
+ * Defines ([LQNN] §3.1, §4.4; [SKILL] App. C sparse_mode 3, App. E): the
+ * queries of sequence b are rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of
+ * `query` (q_b rows), and its keys are the first L_b = context_lens[b]
+ * positions of its paged cache (write them first with pa_reshape_and_cache).
+ * Row i of sequence b (query head h, KV head g) attends keys
+ *     j <= L_b - q_b + i   when causal (the last query sees every key;
+ *                          with L_b == q_b this is the plain lower
+ *                          triangle of each sequence, never across
+ *                          sequences),
+ *     j <  L_b             when not causal,
+ * with the same softmax and rounding as pa_decode.  Rows with no visible key
+ * are written as zeros.
+ *
+ *   out, query      [total_q, num_q_heads, head_dim] with row strides
+ *                   out_row_stride / q_row_stride.
+ *   cu_seqlens_q    int32 [num_seqs + 1]: 0, then the running sum of q_b,
+ *                   ending at total_q ([LQNN] §3.1 / §3.3 assert).
+ *   context_lens    int32 [num_seqs].
+ *   total_q         host copy of cu_seqlens_q[num_seqs].
+ *   max_seqlen_q    host upper bound of q_b (the pages'
+ *                   max_seqlen_in_batch); with total_q it sizes the grid.
+ *   max_context_len host upper bound of context_lens.
+ * Device checks: a cu_seqlens_q that is not a non-decreasing prefix sum
+ * ending at total_q, or a q_b above max_seqlen_q, sets
+ * PA_DEVERR_CU_SEQLENS and the offending sequences are skipped.
+ * Supported: head_dim 128; num_q_heads % num_kv_heads == 0; block_size 16,
+ * 32, 64 or 128.
+ */
+pa_status pa_prefill_varlen(void *out, int64_t out_row_stride,
+                            const void *query, int64_t q_row_stride,
+                            const void *key_cache, const void *value_cache,
+                            const int32_t *block_table,
+                            int64_t block_table_stride,
+                            int32_t max_blocks_per_seq,
+                            const int32_t *cu_seqlens_q,
+                            const int32_t *context_lens, int32_t num_seqs,
+                            int32_t total_q, int32_t max_seqlen_q,
+                            int32_t max_context_len, int32_t num_q_heads,
+                            int32_t num_kv_heads, int32_t head_dim,
+                            int32_t block_size, int64_t num_blocks,
+                            float scale, int32_t causal, pa_dtype dtype,
+                            int32_t *d_error, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

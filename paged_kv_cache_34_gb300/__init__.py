@@ -1,0 +1,188 @@
+"""Attention over a paged KV cache on NVIDIA GB300 (sm_103a).
+
+Python binding of ``libpa.so``, the C-ABI CUDA library declared in
+``include/pa.h``.  Each function here only marshals torch tensors into the
+C call (device pointers, sizes, strides, the current CUDA stream) and turns a
+non-OK status into an exception; every step of the computation runs in the
+library's kernels.  There is no CPU fallback: without the built library the
+first call raises.
+
+    pa_reshape_and_cache  new K/V rows -> pool rows given by slot_mapping
+    pa_decode             one query per sequence, split-KV + LSE combine
+    pa_prefill_varlen     causal attention for cu_seqlens-packed queries
+
+Build the library with ``python -m paged_kv_cache_34_gb300.build``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["pa_reshape_and_cache", "pa_decode", "pa_decode_plan",
+           "pa_prefill_varlen", "PaError", "library", "DEVERR_SLOT",
+           "DEVERR_BLOCK_ID", "DEVERR_CU_SEQLENS", "DEVERR_CONTEXT",
+           "DEVERR_TIMEOUT", "LIB_PATH"]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpa.so")
+
+# Device error bits (include/pa.h PA_DEVERR_*).
+DEVERR_SLOT, DEVERR_BLOCK_ID, DEVERR_CU_SEQLENS, DEVERR_CONTEXT, DEVERR_TIMEOUT = 1, 2, 4, 8, 16
+
+_STATUS = {0: "PA_OK", 1: "PA_ERR_NULL", 2: "PA_ERR_SHAPE", 3: "PA_ERR_UNSUPPORTED",
+           4: "PA_ERR_ALIGN", 5: "PA_ERR_WORKSPACE", 6: "PA_ERR_CUDA"}
+_DTYPE = {torch.float16: 0, torch.bfloat16: 1}
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library(path: str | None = None):
+    """The loaded libpa.so (ctypes), with argument types declared."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"{p} is not built; run `python -m paged_kv_cache_34_gb300.build` "
+                "(there is no fallback implementation)")
+        lib = ctypes.CDLL(p)
+        c = ctypes
+        V, I32, I64, F, SZ = c.c_void_p, c.c_int32, c.c_int64, c.c_float, c.c_size_t
+        lib.pa_abi_version.argtypes, lib.pa_abi_version.restype = [], I32
+        lib.pa_status_string.argtypes, lib.pa_status_string.restype = [c.c_int], c.c_char_p
+        lib.pa_last_cuda_error.argtypes, lib.pa_last_cuda_error.restype = [], I32
+        lib.pa_reshape_and_cache.argtypes = [V, V, I64, V, V, V, I32, I32, I32, I32, I64,
+                                             c.c_int, V, V]
+        lib.pa_reshape_and_cache.restype = c.c_int
+        lib.pa_decode_plan.argtypes = [I32, I32, I32, I32, I32, I32,
+                                       c.POINTER(I32), c.POINTER(SZ)]
+        lib.pa_decode_plan.restype = c.c_int
+        lib.pa_decode.argtypes = [V, I64, V, I64, V, V, V, I64, I32, V, I32, I32, I32, I32,
+                                  I32, I64, F, I32, I32, V, SZ, c.c_int, V, V]
+        lib.pa_decode.restype = c.c_int
+        lib.pa_prefill_varlen.argtypes = [V, I64, V, I64, V, V, V, I64, I32, V, V, I32, I32,
+                                          I32, I32, I32, I32, I32, I32, I64, F, I32, c.c_int,
+                                          V, V]
+        lib.pa_prefill_varlen.restype = c.c_int
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(lib, status: int, what: str):
+    if status != 0:
+        msg = lib.pa_status_string(status).decode()
+        if status == 6:
+            msg += f" (cudaError {lib.pa_last_cuda_error()})"
+        raise PaError(status, f"{what}: {msg}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _rows(t, name):
+    """(row stride in elements) of a [rows, heads, head_dim] view with
+    contiguous heads."""
+    if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+        raise ValueError(f"{name} must be [rows, heads, head_dim] with contiguous heads")
+    return t.stride(0)
+
+
+def pa_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, *,
+                         d_error=None, stream=None, lib=None):
+    """key/value [N, Hkv, D] (equal row strides); caches [NB, bs, Hkv, D]
+    contiguous; slot_mapping int64 [N]."""
+    lib = lib or library()
+    ks = _rows(key, "key")
+    if _rows(value, "value") != ks:
+        raise ValueError("key and value must share a row stride")
+    if not key_cache.is_contiguous() or not value_cache.is_contiguous():
+        raise ValueError("caches must be contiguous [num_blocks, block_size, Hkv, D]")
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    nb, bs, hkv, d = key_cache.shape
+    st = lib.pa_reshape_and_cache(_ptr(key), _ptr(value), ks, _ptr(key_cache),
+                                  _ptr(value_cache), _ptr(slot_mapping), key.shape[0], hkv, d,
+                                  bs, nb, _DTYPE[key.dtype], _ptr(d_error), _stream(stream))
+    _check(lib, st, "pa_reshape_and_cache")
+
+
+def pa_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
+                   partition_size=0, lib=None):
+    """(partition_size, workspace_bytes) that pa_decode will use."""
+    lib = lib or library()
+    p = ctypes.c_int32(0)
+    ws = ctypes.c_size_t(0)
+    st = lib.pa_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
+                            partition_size, ctypes.byref(p), ctypes.byref(ws))
+    _check(lib, st, "pa_decode_plan")
+    return p.value, ws.value
+
+
+def pa_decode(out, query, key_cache, value_cache, block_table, context_lens, *, scale,
+              max_context_len, partition_size=0, workspace=None, d_error=None, stream=None,
+              lib=None):
+    """out/query [S, Hq, D]; caches [NB, bs, Hkv, D]; block_table int32
+    [S, max_blocks]; context_lens int32 [S].  ``max_context_len`` is the
+    host-side upper bound of context_lens.  A workspace is allocated with
+    torch when the plan needs one and none is given."""
+    lib = lib or library()
+    s, hq, d = query.shape
+    nb, bs, hkv, _ = key_cache.shape
+    P, need = pa_decode_plan(s, hq, hkv, d, max_context_len, partition_size, lib=lib)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if block_table.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_table and context_lens must be int32")
+    st = lib.pa_decode(_ptr(out), _rows(out, "out"), _ptr(query), _rows(query, "query"),
+                       _ptr(key_cache), _ptr(value_cache), _ptr(block_table),
+                       block_table.stride(0), block_table.shape[1], _ptr(context_lens), s, hq,
+                       hkv, d, bs, nb, float(scale), int(max_context_len), P,
+                       _ptr(workspace), wbytes, _DTYPE[query.dtype], _ptr(d_error),
+                       _stream(stream))
+    _check(lib, st, "pa_decode")
+    return out
+
+
+def pa_prefill_varlen(out, query, key_cache, value_cache, block_table, cu_seqlens_q,
+                      context_lens, *, scale, max_seqlen_q, max_context_len, causal=True,
+                      d_error=None, stream=None, lib=None):
+    """out/query [T, Hq, D] packed by cu_seqlens_q int32 [S+1];
+    context_lens int32 [S].  ``max_seqlen_q`` / ``max_context_len`` are host
+    upper bounds; T (total_q) is taken from query.shape[0]."""
+    lib = lib or library()
+    t, hq, d = query.shape
+    nb, bs, hkv, _ = key_cache.shape
+    s = context_lens.shape[0]
+    if block_table.dtype != torch.int32 or context_lens.dtype != torch.int32 \
+            or cu_seqlens_q.dtype != torch.int32:
+        raise ValueError("block_table, cu_seqlens_q and context_lens must be int32")
+    st = lib.pa_prefill_varlen(_ptr(out), _rows(out, "out"), _ptr(query), _rows(query, "query"),
+                               _ptr(key_cache), _ptr(value_cache), _ptr(block_table),
+                               block_table.stride(0), block_table.shape[1], _ptr(cu_seqlens_q),
+                               _ptr(context_lens), s, t, int(max_seqlen_q),
+                               int(max_context_len), hq, hkv, d, bs, nb, float(scale),
+                               1 if causal else 0, _DTYPE[query.dtype], _ptr(d_error),
+                               _stream(stream))
+    _check(lib, st, "pa_prefill_varlen")
+    return out

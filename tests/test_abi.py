@@ -1,0 +1,121 @@
+"""The C-ABI library loads, exports every entry point include/pa.h declares,
+and rejects bad arguments on the host before touching the GPU.  These calls
+return before any CUDA call, so they run without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch  # noqa: F401  (loads the CUDA runtime libpa.so links against)
+
+import paged_kv_cache_34_gb300 as pa
+from paged_kv_cache_34_gb300 import build as pabuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "pa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pabuild.build()
+    return pa.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"pa_reshape_and_cache", "pa_decode", "pa_prefill_varlen"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in pa.h but not exported"
+
+
+def test_abi_version_matches_header(lib):
+    m = re.search(r"#define PA_ABI_VERSION (\d+)", open(HEADER).read())
+    assert lib.pa_abi_version() == int(m.group(1))
+
+
+def test_status_strings(lib):
+    for code, name in pa._STATUS.items():
+        assert lib.pa_status_string(code).decode().startswith(name)
+
+
+FAKE = ctypes.c_void_p(0x10000)      # never dereferenced: validation fails first
+MISALIGNED = ctypes.c_void_p(0x10008)
+
+
+def decode_call(lib, **kw):
+    a = dict(out=FAKE, out_stride=8 * 128, q=FAKE, q_stride=8 * 128, kc=FAKE, vc=FAKE,
+             bt=FAKE, bt_stride=16, mbps=16, ctx=FAKE, s=4, hq=8, hkv=2, d=128, bs=16,
+             nb=64, scale=0.125, maxctx=100, part=0, ws=None, wsb=0, dtype=0)
+    a.update(kw)
+    return lib.pa_decode(a["out"], a["out_stride"], a["q"], a["q_stride"], a["kc"], a["vc"],
+                         a["bt"], a["bt_stride"], a["mbps"], a["ctx"], a["s"], a["hq"],
+                         a["hkv"], a["d"], a["bs"], a["nb"], a["scale"], a["maxctx"],
+                         a["part"], a["ws"], a["wsb"], a["dtype"], None, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(hkv=3), 2),                       # Hq % Hkv != 0
+    (dict(hq=32, hkv=2), 3),                # group 16 > 8
+    (dict(d=96), 3),                        # head_dim not built
+    (dict(bs=24), 3),                       # block size not built
+    (dict(bt_stride=8), 2),                 # stride < max_blocks_per_seq
+    (dict(part=100), 2),                    # partition not a multiple of 64
+    (dict(scale=float("nan")), 2),          # scale must be finite
+    (dict(dtype=7), 3),
+    (dict(q=None), 1),
+    (dict(q_stride=8 * 128 - 8), 2),        # row stride below Hq*D
+    (dict(q_stride=8 * 128 + 4), 4),        # row stride not a multiple of 8
+    (dict(kc=MISALIGNED), 4),
+    (dict(s=-1), 2),
+])
+def test_decode_host_validation(lib, kw, status):
+    assert decode_call(lib, **kw) == status
+
+
+def test_decode_empty_batch_is_ok(lib):
+    assert decode_call(lib, s=0) == 0
+
+
+def prefill_call(lib, **kw):
+    a = dict(out=FAKE, q=FAKE, stride=32 * 128, kc=FAKE, vc=FAKE, bt=FAKE, bt_stride=16,
+             mbps=16, cu=FAKE, ctx=FAKE, s=2, t=100, maxq=64, maxctx=64, hq=32, hkv=32,
+             d=128, bs=128, nb=64, scale=0.088, causal=1, dtype=1)
+    a.update(kw)
+    return lib.pa_prefill_varlen(a["out"], a["stride"], a["q"], a["stride"], a["kc"], a["vc"],
+                                 a["bt"], a["bt_stride"], a["mbps"], a["cu"], a["ctx"], a["s"],
+                                 a["t"], a["maxq"], a["maxctx"], a["hq"], a["hkv"], a["d"],
+                                 a["bs"], a["nb"], a["scale"], a["causal"], a["dtype"], None,
+                                 None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=64), 3), (dict(bs=8), 3), (dict(hkv=5), 2), (dict(cu=None), 1),
+    (dict(out=MISALIGNED), 4), (dict(t=-1), 2), (dict(nb=0), 2),
+])
+def test_prefill_host_validation(lib, kw, status):
+    assert prefill_call(lib, **kw) == status
+
+
+def test_prefill_empty_is_ok(lib):
+    assert prefill_call(lib, t=0) == 0 and prefill_call(lib, s=0) == 0
+
+
+def test_reshape_host_validation(lib):
+    f = lib.pa_reshape_and_cache
+    # zero tokens: nothing to do
+    assert f(FAKE, FAKE, 256, FAKE, FAKE, FAKE, 0, 2, 64, 16, 8, 0, None, None) == 0
+    assert f(None, FAKE, 256, FAKE, FAKE, FAKE, 3, 2, 64, 16, 8, 0, None, None) == 1
+    assert f(FAKE, FAKE, 100, FAKE, FAKE, FAKE, 3, 2, 64, 16, 8, 0, None, None) == 2
+    assert f(FAKE, FAKE, 260, FAKE, FAKE, FAKE, 3, 2, 64, 16, 8, 0, None, None) == 4
+    assert f(FAKE, MISALIGNED, 256, FAKE, FAKE, FAKE, 3, 2, 64, 16, 8, 0, None, None) == 4
+    assert f(FAKE, FAKE, 256, FAKE, FAKE, FAKE, 3, 2, 64, 16, 8, 5, None, None) == 3
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="not built"):
+        pa.library(str(tmp_path / "libpa.so"))

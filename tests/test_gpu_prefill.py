@@ -1,0 +1,135 @@
+"""pa_prefill_varlen on the GPU against the fp64 oracle, plus the invariants
+the pages fix (packed = alone, decode = last prefill row)."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import (W, assert_close, cfg, gpu, gpu_decode, gpu_prefill, gpu_write, new_err,
+                      oracle_pools_after_write, oracle_prefill, pa, require_gpu, u16)
+
+pytestmark = gpu
+
+
+def _run(x_host, rows=None, what=""):
+    require_gpu()
+    kp, vp = oracle_pools_after_write(x_host)
+    want = oracle_prefill(x_host, kp, vp, rows=rows)
+    x = x_host.to("cuda")
+    err = new_err()
+    gpu_write(x, err)
+    out = gpu_prefill(x, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, f"device error bits {int(err.item())}"
+    assert_close(out, want, x.dtype, rows=rows, what=what)
+    return x, out
+
+
+def sampled_rows(cu, stride=5):
+    """Every stride-th packed row plus each sequence's first/last rows and the
+    rows around every 128-row tile edge."""
+    cu = list(cu)
+    rows = set(range(0, cu[-1], stride))
+    for b in range(len(cu) - 1):
+        lo, hi = cu[b], cu[b + 1]
+        for r in (lo, lo + 1, hi - 2, hi - 1):
+            if lo <= r < hi:
+                rows.add(r)
+        for e in range(lo + 127, hi, 128):
+            rows.update(r for r in (e - 1, e, e + 1) if lo <= r < hi)
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def test_packed_prefill_full_size_sampled_rows():
+    # The full packed-prefill workload in the benchmark's launch
+    # configuration, checked on a sample of rows the oracle computes.
+    x = W.make_inputs("packed-prefill")
+    _run(x, rows=sampled_rows(x.cu_seqlens_q.tolist()), what="packed-prefill")
+
+
+@pytest.mark.parametrize("bs", [16, 32, 64, 128])
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 2)])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_varlen_grid(bs, hq, hkv, dtype):
+    lengths = [1, 5, 127, 128, 129, 300, 64]
+    c = cfg(kind="prefill", hq=hq, hkv=hkv, d=128, bs=bs,
+            nb=sum(-(-n // bs) for n in lengths) + 3, dtype=dtype, lengths=lengths)
+    _run(W.make_inputs(c, seed=200 + bs + hq), what=f"bs{bs} g{hq // hkv} {dtype}")
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_chunked_prefill_queries_shorter_than_context(causal):
+    # q < L: the cache already holds a prefix; the step writes the new chunk
+    # and its queries attend bottom-right aligned.
+    lengths = [300, 129, 517, 64]
+    qlens = [44, 129, 200, 1]
+    c = cfg(kind="prefill", hq=8, hkv=4, d=128, bs=32, nb=60, dtype="bf16",
+            lengths=lengths, causal=causal)
+    x = W.make_inputs(c, seed=51, q_lens=qlens, new_lens=qlens)
+    _run(x, what=f"chunked causal={causal}")
+
+
+def test_packed_equals_each_sequence_alone_bitwise():
+    require_gpu()
+    lengths = [200, 33, 450, 128]
+    x = W.make_inputs(cfg(kind="prefill", hq=4, hkv=4, d=128, bs=64, nb=40,
+                          lengths=lengths), seed=53).to("cuda")
+    gpu_write(x)
+    packed = gpu_prefill(x)
+    cu = x.cu_seqlens_q.tolist()
+    for b in range(len(lengths)):
+        y = x.to("cuda")
+        y.q = x.q[cu[b]:cu[b + 1]]
+        y.cu_seqlens_q = torch.tensor([0, lengths[b]], dtype=torch.int32, device="cuda")
+        y.q_lens = x.q_lens[b:b + 1]
+        y.context_lens = x.context_lens[b:b + 1]
+        y.block_table = x.block_table[b:b + 1]
+        alone = gpu_prefill(y)
+        torch.cuda.synchronize()
+        assert torch.equal(alone.view(torch.int16), packed[cu[b]:cu[b + 1]].view(torch.int16))
+
+
+def test_decode_matches_last_prefill_row():
+    require_gpu()
+    lengths = [90, 640, 257]
+    x = W.make_inputs(cfg(kind="prefill", hq=8, hkv=2, d=128, bs=16, nb=80,
+                          lengths=lengths), seed=57).to("cuda")
+    gpu_write(x)
+    pre = gpu_prefill(x)
+    last = (x.cu_seqlens_q[1:] - 1).long()
+    d = x.to("cuda")
+    d.q = x.q[last].contiguous()
+    dec = gpu_decode(d, partition_size=128)
+    torch.cuda.synchronize()
+    assert (dec.double() - pre[last].double()).abs().max().item() <= 1e-2
+
+
+def test_bad_cu_seqlens_flagged_not_faults():
+    require_gpu()
+    x = W.make_inputs(cfg(kind="prefill", hq=4, hkv=4, d=128, bs=32, nb=30,
+                          lengths=[100, 200]), seed=59).to("cuda")
+    gpu_write(x)
+    x.cu_seqlens_q = torch.tensor([0, 250, 300], dtype=torch.int32, device="cuda")
+    err = new_err()
+    pa.pa_prefill_varlen(torch.empty_like(x.q), x.q, x.k_pool, x.v_pool, x.block_table,
+                         x.cu_seqlens_q, x.context_lens, scale=x.scale, max_seqlen_q=200,
+                         max_context_len=200, d_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa.DEVERR_CU_SEQLENS
+
+
+def test_bad_block_id_flagged_not_faults():
+    require_gpu()
+    x = W.make_inputs(cfg(kind="prefill", hq=4, hkv=4, d=128, bs=32, nb=30,
+                          lengths=[100, 200]), seed=61)
+    bt = x.block_table.clone()
+    bt[1, 3] = -5
+    xd = x.to("cuda")
+    gpu_write(xd)
+    xd.block_table = bt.cuda()
+    err = new_err()
+    out = gpu_prefill(xd, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa.DEVERR_BLOCK_ID
+    kp, vp = u16(xd.k_pool), u16(xd.v_pool)
+    want = oracle_prefill(x, kp, vp, rows=np.arange(100))
+    assert_close(out, want, x.dtype, rows=np.arange(100), what="unaffected sequence")
