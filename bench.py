@@ -507,7 +507,7 @@ def main():
                              "frac": round(tf / tf_peak, 4),
                              "traffic": recorded_traffic(
                                  "pa_prefill_varlen", "packed-prefill",
-                                 source_hash("prefill.cu", "pa_tcgen05.cuh"))}}
+                                 source_hash("prefill.cu", "pa_tcgen05.cuh", "pa_device.cuh"))}}
             del xp
             xl, _, _, partl, npl, t_lstep, t_ldec = bench_decode(
                 pa, W, "long-context-decode", max(10, args.steps // 10), args.warmup,
