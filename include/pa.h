@@ -132,7 +132,7 @@ pa_status pa_reshape_and_cache(const void *key, const void *value,
  * partition's softmax state (max, sum, unnormalised output) is combined by
  * log-sum-exp.  partition_size == 0 picks a size from max_context_len, the
  * batch shape and the current device's SM count; a non-zero value must be a
- * positive multiple of 64 and is used as given.  *workspace_bytes_out is the
+ * positive multiple of 16 and is used as given.  *workspace_bytes_out is the
  * device workspace pa_decode needs (0 when no sequence can span two
  * partitions).  Host-only; enqueues nothing.
  */

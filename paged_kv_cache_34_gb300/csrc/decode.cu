@@ -11,24 +11,31 @@
 // a scalar online softmax; this keeps the block walk and the online softmax
 // but is shaped for HBM bandwidth):
 //
-//  * Grid (partition, KV head, sequence).  A sequence's context is cut into
-//    partitions of P tokens (split-KV); each CTA streams one partition of
-//    one KV head and serves all G query heads of that KV head from the same
-//    bytes (GQA sharing).  When a sequence spans several partitions each CTA
-//    writes its softmax state (max, sum, unnormalised output) to workspace
-//    and a combine kernel merges them by log-sum-exp.
-//  * One producer warp stages the partition's block-table slice in shared
-//    memory once, then issues TMA tile loads (128-byte swizzled, one box per
-//    (block, D/64 half)) into a 3-stage ring of 64-token K/V chunks guarded
-//    by mbarriers.  Two CTAs fit per SM, so six chunks are in flight.
-//  * Four consumer warps each own 16 tokens of a chunk.  Scores are computed
-//    transposed on the tensor cores -- S^T[16 tokens x 8 heads] =
-//    K[16 x D] Q^T[D x 8] with mma.sync m16n8k16, fp32 accumulate -- so the G
-//    heads fill the N=8 side and no rows are padding for G = 8.  The online
-//    softmax runs on the fragments (warp-shuffle max over tokens), P^T is
-//    formed with movmatrix, and O^T[D x 8] += V^T[D x 16] P^T[16 x 8] reads V
-//    through ldmatrix.trans.  The partition's four warp states are merged in
-//    shared memory at the end.
+//  * Work items.  A sequence's context is cut into partitions of P tokens
+//    (split-KV); an item is one (sequence, KV head, partition).  Every item
+//    serves all G query heads of its KV head from the same K/V bytes (GQA
+//    sharing).  A sequence with one partition writes its output directly;
+//    otherwise each item writes its softmax state (max, sum, unnormalised
+//    output) to workspace and a combine kernel merges them by log-sum-exp.
+//  * Persistent CTAs, independent warps.  The grid is at most two CTAs per
+//    SM.  Each of a CTA's four consumer warps is a worker with its own static
+//    list of items (worker w of W takes items w, w+W, ...), so no warp ever
+//    waits for another to merge results.  Items are numbered from a prefix sum
+//    of the sequences' item counts, computed once per CTA from context_lens.
+//  * One producer warp feeds all four workers through a 3-stage ring of
+//    TMA tile loads (128-byte swizzle) guarded by mbarriers: each stage holds
+//    16 tokens of K and V for every worker, read block by block through the
+//    block table.  Producer lane w walks worker w's items with incremental
+//    (block, offset) counters, and the block ids of the worker's next item
+//    are copied into shared memory with cp.async while its current item
+//    streams, so no id lookup or division sits on the load-issue path.  Two CTAs per SM keep six
+//    stages (192 KB) in flight per SM.
+//  * Scores are computed transposed on the tensor cores -- S^T[16 tokens x 8
+//    heads] = K[16 x D] Q^T[D x 8] with mma.sync m16n8k16, fp32 accumulate --
+//    so the G heads fill the N = 8 side.  The online softmax runs on the
+//    fragments (warp-shuffle max over tokens), P^T is formed with movmatrix,
+//    and O^T[D x 8] += V^T[D x 16] P^T[16 x 8] reads V through ldmatrix.trans.
+//    A worker's next query is prefetched into registers one item ahead.
 //  * Exponentials are base 2 with the scale pre-multiplied by log2(e).
 #include <math.h>
 
@@ -39,18 +46,23 @@ namespace pa {
 
 namespace {
 
-constexpr int kThreads = (kDecodeWarps + 1) * 32;  // + producer warp
+constexpr int kWorkers = kDecodeWarps;
+constexpr int kThreads = (kWorkers + 1) * 32;  // + producer warp
 constexpr int kStages = 3;
-constexpr int kHalfBytes = kDecodeChunk * 128;  // 64 tokens x 64 elements x 2 B
+constexpr int kSub = kDecodeSub;               // tokens per worker per stage
+constexpr int kHalfBytes = kWorkers * kSub * 128;  // 64 rows x 64 elements x 2 B
+constexpr uint32_t kTerminate = 0x100u;        // stage header: no more data
 
 template <int D>
 struct DecodeSmem {
   static constexpr int kHalves = D / 64;
   static constexpr int kStageBytes = 2 * kHalves * kHalfBytes;  // K + V
-  static constexpr int kBarOffset = kStages * kStageBytes;
-  static constexpr int kFlagOffset = kBarOffset + 2 * kStages * 8;
-  static constexpr int kBlkOffset = kFlagOffset + 16;
-  static int bytes(int max_blocks) { return 1024 + kBlkOffset + 4 * max_blocks; }
+  static constexpr int kBarOffset = kStages * kStageBytes;      // full[3], empty[3]
+  static constexpr int kHdrOffset = kBarOffset + 2 * kStages * 8;
+  static constexpr int kVarOffset = kHdrOffset + 32;  // pref[S+1], len[S], ids
+  static int bytes(int num_seqs, int max_ids) {
+    return 1024 + kVarOffset + 4 * (2 * num_seqs + 1) + 4 * kWorkers * 2 * max_ids;
+  }
 };
 
 struct DecodeParams {
@@ -62,184 +74,390 @@ struct DecodeParams {
   int64_t bt_stride;
   const int32_t *context_lens;
   int32_t capacity, max_ctx;
-  int32_t hq, hkv, group, block_size;
+  int32_t num_seqs, hq, hkv, group, block_size;
   int64_t num_blocks;
   float scale_log2;
-  int32_t partition_size, num_partitions;
+  int32_t partition_size, num_partitions, max_ids;
   float *ws_o, *ws_ml;
   int32_t *err;
 };
+
+// One work item: partition `part` of sequence b for KV head g, tokens
+// [start, end) of a context of L tokens.
+struct Item {
+  int b, g, part, L, start, end;
+};
+
+// Item i of the numbering given by the prefix sums `pref` (items of sequence
+// b are pref[b] .. pref[b+1]-1, ordered by KV head then partition).
+__device__ __forceinline__ Item decode_item(int i, const int *pref, const int *len, int S,
+                                            int hkv, int P) {
+  int lo = 0, hi = S;  // pref[lo] <= i < pref[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pref[mid] <= i) lo = mid;
+    else hi = mid;
+  }
+  Item m;
+  m.b = lo;
+  m.L = len[lo];
+  const int np = m.L > 0 ? (m.L + P - 1) / P : 1;
+  const int rem = i - pref[lo];
+  m.g = rem / np;
+  m.part = rem - m.g * np;
+  m.start = m.part * P;
+  m.end = min(m.start + P, m.L);
+  if (m.end < m.start) m.end = m.start;
+  (void)hkv;
+  return m;
+}
 
 __device__ __forceinline__ float shfl_xor(float v, int m) {
   return __shfl_xor_sync(0xffffffffu, v, m);
 }
 
 template <class E, int D>
-__device__ void write_empty_result(const DecodeParams &p, int b, int g, int part,
-                                   int nparts_seq, int tid, int nthreads) {
-  // A partition that contributes nothing: zeros in the output when it is the
-  // sequence's only partition, otherwise a neutral softmax state.
+__device__ __forceinline__ void load_q(uint32_t (&qf)[D / 16][2], const DecodeParams &p,
+                                       const Item &m, int lane) {
   const int G = p.group;
-  if (nparts_seq <= 1) {
-    typename E::T *out = static_cast<typename E::T *>(p.out) + b * p.out_row_stride;
-    for (int i = tid; i < G * D; i += nthreads)
-      out[(g * G) * D + i] = E::from_float(0.f);
-  } else {
-    for (int i = tid; i < G * D; i += nthreads) {
-      const int h = g * G + i / D, d = i % D;
-      const int64_t row = (static_cast<int64_t>(b) * p.hq + h) * p.num_partitions + part;
-      p.ws_o[row * D + d] = 0.f;
-      if (d == 0) {
-        p.ws_ml[row * 2 + 0] = -INFINITY;
-        p.ws_ml[row * 2 + 1] = 0.f;
-      }
-    }
+  const int qh = lane >> 2;  // head column this lane feeds to Q^T
+  const typename E::T *qrow = static_cast<const typename E::T *>(p.q) +
+                              m.b * p.q_row_stride + (m.g * G + qh) * D + 2 * (lane & 3);
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    qf[ks][0] = qh < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16)) : 0u;
+    qf[ks][1] = qh < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8)) : 0u;
   }
 }
 
 template <class E, int D, int BOXR>
 __global__ void __launch_bounds__(kThreads, 2)
-    decode_partition_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
-                            const __grid_constant__ CUtensorMap tmv) {
+    decode_persistent_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
+                             const __grid_constant__ CUtensorMap tmv) {
   using S = DecodeSmem<D>;
   constexpr int NH = S::kHalves;
   constexpr int KSTEPS = D / 16;
-  constexpr int BOXES = kDecodeChunk / BOXR;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kBarOffset);
   uint64_t *empty = full + kStages;
-  volatile int *s_flag = reinterpret_cast<volatile int *>(smem + S::kFlagOffset);
-  int *s_blk = reinterpret_cast<int *>(smem + S::kBlkOffset);
+  volatile uint32_t *s_hdr = reinterpret_cast<volatile uint32_t *>(smem + S::kHdrOffset);
+  volatile int *s_abort = reinterpret_cast<volatile int *>(smem + S::kHdrOffset + 16);
+  int *s_pref = reinterpret_cast<int *>(smem + S::kVarOffset);
+  int *s_len = s_pref + p.num_seqs + 1;
+  int *s_ids = s_len + p.num_seqs;  // [kWorkers][2][max_ids]
 
-  const int part = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int P = p.partition_size;
-  const int L = checked_context_len(__ldg(p.context_lens + b), p.capacity, p.max_ctx, p.err,
-                                    tid == 0 && part == 0 && g == 0);
-  const int start = part * P;
-  const int nparts_seq = (L + P - 1) / P;
-  if (L == 0) {
-    if (part == 0) write_empty_result<E, D>(p, b, g, part, 1, tid, kThreads);
-    return;
-  }
-  if (start >= L) return;
-  const int end = min(start + P, L);
-  const int bs = p.block_size;
-  const int first_lblk = start / bs;
-  const int nblk = (end - 1) / bs - first_lblk + 1;
+  const int nseq = p.num_seqs;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(full + s), 1);
-      mbar_init(smem_u32(empty + s), kDecodeWarps);
+      mbar_init(smem_u32(empty + s), kWorkers);
     }
-    s_flag[0] = 0;  // a bad block id in this partition
-    s_flag[1] = 0;  // a wait gave up
+    *s_abort = 0;
     fence_barrier_init();
   }
-  if (warp == kDecodeWarps) {
-    if (lane == 0) {
-      tma_prefetch_desc(&tmk);
-      tma_prefetch_desc(&tmv);
-    }
-    const int32_t *bt = p.block_table + static_cast<int64_t>(b) * p.bt_stride + first_lblk;
-    for (int i = lane; i < nblk; i += 32) {
-      const int id = __ldg(bt + i);
-      if (id < 0 || id >= p.num_blocks) {
-        raise_error(p.err, PA_DEVERR_BLOCK_ID);
-        s_flag[0] = 1;
+  if (warp == 0) {
+    // Items per sequence (checked context lengths) and their prefix sums.
+    int carry = 0;
+    for (int base = 0; base < nseq; base += 32) {
+      const int b = base + lane;
+      int items = 0;
+      if (b < nseq) {
+        const int L = checked_context_len(__ldg(p.context_lens + b), p.capacity, p.max_ctx,
+                                          p.err, blockIdx.x == 0);
+        s_len[b] = L;
+        items = (L > 0 ? (L + P - 1) / P : 1) * p.hkv;
       }
-      s_blk[i] = id;
+      int incl = items;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (b < nseq) s_pref[b + 1] = carry + incl;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
     }
+    if (lane == 0) s_pref[0] = 0;
+  }
+  if (warp == kWorkers && lane == 0) {
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
   }
   __syncthreads();
-  if (s_flag[0]) {
-    write_empty_result<E, D>(p, b, g, part, nparts_seq, tid, kThreads);
-    return;
-  }
 
-  const int ntok = end - start;
-  const int nchunks = (ntok + kDecodeChunk - 1) / kDecodeChunk;
+  const int total = s_pref[nseq];
+  const int NW = gridDim.x * kWorkers;
+  const int bs = p.block_size;
 
   // ------------------------------------------------------------ producer --
-  if (warp == kDecodeWarps) {
-    if (lane != 0) return;
-    int issued = 0;
-    for (int c = 0; c < nchunks; ++c) {
-      const int s = c % kStages;
-      if (c >= kStages && !mbar_wait_bounded(smem_u32(empty + s), ((c / kStages) - 1) & 1)) {
-        raise_error(p.err, PA_DEVERR_TIMEOUT);
-        s_flag[1] = 1;
+  if (warp == kWorkers) {
+    // Lane w (< 4) feeds worker w: it walks that worker's items block by
+    // block, keeping the current item's position as (logical block, offset)
+    // counters, and copies the block ids of the worker's next item into
+    // shared memory with cp.async while the current item streams.  Lane 0
+    // owns the stage barriers.
+    const bool feeder = lane < kWorkers;
+    int cur = 0, endt = 0, gq = 0, sel = 0, lblk = 0, off = 0;
+    int nx = total, nstart = 0, nend = 0, ng = 0, nbuf = 0;
+    bool act = false;
+    // Finds this worker's first item with tokens at index >= i (items of
+    // empty sequences carry no tokens: the worker writes their zeros itself)
+    // and starts copying its block ids into buffer `buf`.
+    auto prefetch = [&](int i, int buf) {
+      for (; i < total; i += NW) {
+        const Item m = decode_item(i, s_pref, s_len, nseq, p.hkv, P);
+        if (m.end <= m.start) continue;
+        const int l0 = m.start / bs;
+        const int nblk = (m.end - 1) / bs - l0 + 1;
+        const int32_t *src = p.block_table + static_cast<int64_t>(m.b) * p.bt_stride + l0;
+        const uint32_t dst = smem_u32(s_ids + (lane * 2 + buf) * p.max_ids);
+        for (int k = 0; k < nblk; ++k) cp_async_4(dst + 4 * k, src + k);
+        cp_async_commit();
+        nstart = m.start;
+        nend = m.end;
+        ng = m.g;
         break;
       }
-      if (s_flag[1]) break;
-      const int c0 = start + c * kDecodeChunk;
-      int nbox = 0;
+      nx = i < total ? i : total;
+      nbuf = buf;
+    };
+    // Makes the prefetched item current and prefetches the one after it.
+    auto promote = [&]() {
+      act = nx < total;
+      if (!act) return;
+      cp_async_wait_all();  // this item's ids (issued at least one item ago)
+      cur = nstart;
+      endt = nend;
+      gq = ng;
+      sel = nbuf;
+      lblk = 0;
+      off = nstart % bs;
+      prefetch(nx + NW, nbuf ^ 1);
+    };
+    if (feeder) {
+      prefetch(blockIdx.x * kWorkers + lane, 0);
+      promote();
+    }
+    const int *ids = s_ids;
+    for (int c = 0;; ++c) {
+      const int s = c % kStages;
+      int rows[kSub / BOXR];
+      int nb = 0;
+      bool bad = false;
+      if (feeder) {
+        if (act && cur >= endt) promote();
+        ids = s_ids + (lane * 2 + sel) * p.max_ids;
 #pragma unroll
-      for (int k = 0; k < BOXES; ++k) nbox += (c0 + k * BOXR < end) ? 1 : 0;
-      const uint32_t bar = smem_u32(full + s);
-      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nbox * BOXR * 128 * NH * 2));
-      const uint32_t kdst = smem_u32(smem + s * S::kStageBytes);
-      const uint32_t vdst = kdst + NH * kHalfBytes;
-      for (int k = 0; k < nbox; ++k) {
-        const int j = c0 + k * BOXR;
-        const int row = s_blk[j / bs - first_lblk] * bs + (j % bs);
+        for (int k = 0; k < kSub / BOXR; ++k) rows[k] = -1;
+        if (act) {
+          const int ntok = min(kSub, endt - cur);
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          tma_load_3d(kdst + h * kHalfBytes + k * BOXR * 128, &tmk, bar, h * 64, g, row);
-          tma_load_3d(vdst + h * kHalfBytes + k * BOXR * 128, &tmv, bar, h * 64, g, row);
+          for (int k = 0; k < kSub / BOXR; ++k) {
+            if (k * BOXR >= ntok) break;
+            const int id = ids[lblk];
+            if (id >= 0 && id < p.num_blocks) {
+              rows[k] = id * bs + off;
+              ++nb;
+            } else {
+              bad = true;
+            }
+            off += BOXR;
+            if (off >= bs) {
+              off = 0;
+              ++lblk;
+            }
+          }
+          cur += kSub;
         }
       }
-      ++issued;
+      const unsigned live = __ballot_sync(0xffffffffu, feeder && act);
+      const unsigned badmask = __ballot_sync(0xffffffffu, bad);
+      int nbox = nb;
+      nbox += __shfl_xor_sync(0xffffffffu, nbox, 1);
+      nbox += __shfl_xor_sync(0xffffffffu, nbox, 2);  // lanes 0-3 hold all feeders
+      bool ok = true;
+      if (lane == 0 && c >= kStages)
+        ok = mbar_wait_bounded(smem_u32(empty + s), ((c / kStages) - 1) & 1);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok || *s_abort) {
+        if (lane == 0) {
+          if (!ok) raise_error(p.err, PA_DEVERR_TIMEOUT);
+          *s_abort = 1;
+          // Do not leave while copies this CTA issued may still land.
+          for (int k = c - 1; k >= 0 && k >= c - kStages; --k)
+            mbar_wait_bounded(smem_u32(full + (k % kStages)), (k / kStages) & 1);
+        }
+        cp_async_wait_all();
+        return;
+      }
+      if (live == 0) {
+        if (lane == 0) {
+          s_hdr[s] = kTerminate;
+          mbar_arrive(smem_u32(full + s));
+        }
+        cp_async_wait_all();
+        return;
+      }
+      const uint32_t bar = smem_u32(full + s);
+      if (lane == 0) {
+        s_hdr[s] = badmask & ((1u << kWorkers) - 1);
+        if (badmask) raise_error(p.err, PA_DEVERR_BLOCK_ID);
+        // The barrier must expect exactly the bytes that land.
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nbox) * BOXR * 128 * NH * 2);
+      }
+      __syncwarp();
+      if (feeder) {
+        const uint32_t kdst = smem_u32(smem + s * S::kStageBytes);
+        const uint32_t vdst = kdst + NH * kHalfBytes;
+#pragma unroll
+        for (int k = 0; k < kSub / BOXR; ++k) {
+          if (rows[k] < 0) continue;
+          const uint32_t o = (lane * kSub + k * BOXR) * 128;
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            tma_load_3d(kdst + h * kHalfBytes + o, &tmk, bar, h * 64, gq, rows[k]);
+            tma_load_3d(vdst + h * kHalfBytes + o, &tmv, bar, h * 64, gq, rows[k]);
+          }
+        }
+      }
     }
-    // Do not leave while copies this CTA issued may still land.
-    for (int c = issued - 1; c >= 0 && c >= issued - kStages; --c)
-      mbar_wait_bounded(smem_u32(full + (c % kStages)), (c / kStages) & 1);
-    return;
   }
 
-  // ----------------------------------------------------------- consumers --
+  // ----------------------------------------------------- consumer = worker --
   const int G = p.group;
-  const int qh = lane >> 2;  // head column this lane feeds to Q^T
-  uint32_t qf[KSTEPS][2];
-  {
-    const typename E::T *qrow = static_cast<const typename E::T *>(p.q) +
-                                b * p.q_row_stride + (g * G + qh) * D + 2 * (lane & 3);
-#pragma unroll
-    for (int ks = 0; ks < KSTEPS; ++ks) {
-      qf[ks][0] = qh < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16)) : 0u;
-      qf[ks][1] = qh < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8)) : 0u;
-    }
-  }
-  float o[KSTEPS][4];
-#pragma unroll
-  for (int mt = 0; mt < KSTEPS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2(lane&3), +1
   const float sl = p.scale_log2;
-  const int r0 = warp * 16;  // this warp's first row in a chunk
+  const int r0 = warp * kSub;  // this worker's rows in a stage
   const int mj = lane >> 3, mr = lane & 7;
+  const int h0 = 2 * (lane & 3), h1 = h0 + 1;
 
-  for (int c = 0; c < nchunks; ++c) {
+  uint32_t qf[KSTEPS][2], qn[KSTEPS][2];
+  float o[KSTEPS][4];
+  float m0, m1, l0, l1;
+  bool item_bad = false;
+  Item cur_item;
+  int it = blockIdx.x * kWorkers + warp;
+  int qn_item = -1;
+  int cur = 0;
+
+  // Writes a finished item: the normalised output when it is its sequence's
+  // only partition, else its softmax state for the combine.
+  auto finalize = [&](const Item &m, bool bad_item) {
+#pragma unroll
+    for (int s = 4; s < 32; s <<= 1) {
+      l0 += shfl_xor(l0, s);
+      l1 += shfl_xor(l1, s);
+    }
+    const int np = m.L > 0 ? (m.L + P - 1) / P : 1;
+    if (np == 1) {
+      const float i0 = (!bad_item && l0 > 0.f) ? 1.f / l0 : 0.f;
+      const float i1 = (!bad_item && l1 > 0.f) ? 1.f / l1 : 0.f;
+      typename E::T *out =
+          static_cast<typename E::T *>(p.out) + m.b * p.out_row_stride + m.g * G * D;
+#pragma unroll
+      for (int mt = 0; mt < KSTEPS; ++mt) {
+        const int d0 = mt * 16 + (lane >> 2), d1 = d0 + 8;
+        if (h0 < G) {
+          out[h0 * D + d0] = E::from_float(o[mt][0] * i0);
+          out[h0 * D + d1] = E::from_float(o[mt][2] * i0);
+        }
+        if (h1 < G) {
+          out[h1 * D + d0] = E::from_float(o[mt][1] * i1);
+          out[h1 * D + d1] = E::from_float(o[mt][3] * i1);
+        }
+      }
+    } else {
+      const int64_t row0 =
+          (static_cast<int64_t>(m.b) * p.hq + m.g * G) * p.num_partitions + m.part;
+      const int64_t hstride = p.num_partitions;
+#pragma unroll
+      for (int mt = 0; mt < KSTEPS; ++mt) {
+        const int d0 = mt * 16 + (lane >> 2), d1 = d0 + 8;
+        if (h0 < G) {
+          float *w0 = p.ws_o + (row0 + h0 * hstride) * D;
+          w0[d0] = bad_item ? 0.f : o[mt][0];
+          w0[d1] = bad_item ? 0.f : o[mt][2];
+        }
+        if (h1 < G) {
+          float *w1 = p.ws_o + (row0 + h1 * hstride) * D;
+          w1[d0] = bad_item ? 0.f : o[mt][1];
+          w1[d1] = bad_item ? 0.f : o[mt][3];
+        }
+      }
+      if (lane < 4) {
+        if (h0 < G) {
+          p.ws_ml[(row0 + h0 * hstride) * 2 + 0] = bad_item ? -INFINITY : m0;
+          p.ws_ml[(row0 + h0 * hstride) * 2 + 1] = bad_item ? 0.f : l0;
+        }
+        if (h1 < G) {
+          p.ws_ml[(row0 + h1 * hstride) * 2 + 0] = bad_item ? -INFINITY : m1;
+          p.ws_ml[(row0 + h1 * hstride) * 2 + 1] = bad_item ? 0.f : l1;
+        }
+      }
+    }
+  };
+  // Starts this worker's next item with tokens at or after item index `it`;
+  // items of empty sequences are finished on the spot (zero output).
+  auto begin = [&]() -> bool {
+    while (it < total) {
+      const Item m = decode_item(it, s_pref, s_len, nseq, p.hkv, P);
+#pragma unroll
+      for (int mt = 0; mt < KSTEPS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+      m0 = m1 = -INFINITY;
+      l0 = l1 = 0.f;
+      item_bad = false;
+      if (m.end > m.start) {
+        if (qn_item == it) {
+#pragma unroll
+          for (int ks = 0; ks < KSTEPS; ++ks) {
+            qf[ks][0] = qn[ks][0];
+            qf[ks][1] = qn[ks][1];
+          }
+        } else {
+          load_q<E, D>(qf, p, m, lane);
+        }
+        cur_item = m;
+        cur = m.start;
+        // Prefetch the next item's query one item ahead.
+        const int nxt = it + NW;
+        if (nxt < total) {
+          load_q<E, D>(qn, p, decode_item(nxt, s_pref, s_len, nseq, p.hkv, P), lane);
+          qn_item = nxt;
+        }
+        return true;
+      }
+      finalize(m, false);  // empty sequence: zeros
+      it += NW;
+    }
+    return false;
+  };
+  bool active = begin();
+
+  for (int c = 0;; ++c) {
     const int s = c % kStages;
     if (!mbar_wait_bounded(smem_u32(full + s), (c / kStages) & 1)) {
       raise_error(p.err, PA_DEVERR_TIMEOUT);
-      s_flag[1] = 1;
+      *s_abort = 1;
       break;
     }
-    const int j0 = start + c * kDecodeChunk + r0;
-    if (j0 < end) {
+    const uint32_t hdr = s_hdr[s];
+    if (hdr & kTerminate) break;
+    if (active) {
+      const int end = cur_item.end;
+      const int j0 = cur;
       uint8_t *kst = smem + s * S::kStageBytes;
       const uint32_t kb = smem_u32(kst);
       const uint32_t vb = kb + NH * kHalfBytes;
       bool zeroed = false;
-      if (j0 + 16 > end) {
+      if (j0 + kSub > end) {
         // Rows past the context may hold anything (even NaN); their weight is
         // zero, so make their V rows exact zeros before the P.V product.
         uint8_t *vrows = kst + NH * kHalfBytes;
-        for (int i = lane; i < 16 * NH * 8; i += 32) {
+        for (int i = lane; i < kSub * NH * 8; i += 32) {
           const int rr = i / (NH * 8), h = (i / 8) % NH, cc = i % 8;
           if (j0 + rr >= end)
             *reinterpret_cast<uint4 *>(vrows + h * kHalfBytes + (r0 + rr) * 128 + cc * 16) =
@@ -248,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         __syncwarp();
         zeroed = true;
       }
-      // S^T = K Q^T for this warp's 16 tokens.
+      // S^T = K Q^T for this worker's 16 tokens.
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int ks = 0; ks < KSTEPS; ++ks) {
@@ -304,69 +522,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         mma_16816<E::kBF16>(o[mt], a0, a1, a2, a3, pb0, pb1);
       }
       if (zeroed) fence_proxy_async_smem();  // generic writes before the next TMA
+      if (hdr & (1u << warp)) item_bad = true;
+      cur += kSub;
+      if (cur >= end) {
+        finalize(cur_item, item_bad);
+        it += NW;
+        active = begin();
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(empty + s));
-  }
-
-  // Row sums: combine the lanes that share a head.
-#pragma unroll
-  for (int m = 4; m < 32; m <<= 1) {
-    l0 += shfl_xor(l0, m);
-    l1 += shfl_xor(l1, m);
-  }
-
-  // Merge the four warps' states through shared memory (stage 0 is free:
-  // every chunk has been consumed).
-  named_barrier_sync(1, kDecodeWarps * 32);
-  float *sO = reinterpret_cast<float *>(smem);           // [warp][8][D]
-  float *sM = sO + kDecodeWarps * kDecodeMaxGroup * D;  // [warp][8]
-  float *sL = sM + kDecodeWarps * kDecodeMaxGroup;      // [warp][8]
-  {
-    const int h0 = 2 * (lane & 3), h1 = h0 + 1;
-    float *w = sO + warp * kDecodeMaxGroup * D;
-#pragma unroll
-    for (int mt = 0; mt < KSTEPS; ++mt) {
-      const int d0 = mt * 16 + (lane >> 2), d1 = d0 + 8;
-      w[h0 * D + d0] = o[mt][0];
-      w[h1 * D + d0] = o[mt][1];
-      w[h0 * D + d1] = o[mt][2];
-      w[h1 * D + d1] = o[mt][3];
-    }
-    if (lane < 4) {
-      sM[warp * kDecodeMaxGroup + h0] = m0;
-      sM[warp * kDecodeMaxGroup + h1] = m1;
-      sL[warp * kDecodeMaxGroup + h0] = l0;
-      sL[warp * kDecodeMaxGroup + h1] = l1;
-    }
-  }
-  named_barrier_sync(1, kDecodeWarps * 32);
-  for (int i = tid; i < G * D; i += kDecodeWarps * 32) {
-    const int h = i / D, d = i % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kDecodeWarps; ++w) M = fmaxf(M, sM[w * kDecodeMaxGroup + h]);
-    float acc = 0.f, l = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kDecodeWarps; ++w) {
-        const float f = exp2f(sM[w * kDecodeMaxGroup + h] - M);
-        acc += f * sO[(w * kDecodeMaxGroup + h) * D + d];
-        l += f * sL[w * kDecodeMaxGroup + h];
-      }
-    }
-    if (nparts_seq == 1) {
-      typename E::T *out = static_cast<typename E::T *>(p.out) + b * p.out_row_stride;
-      out[(g * G + h) * D + d] = E::from_float(l > 0.f ? acc / l : 0.f);
-    } else {
-      const int64_t row =
-          (static_cast<int64_t>(b) * p.hq + g * G + h) * p.num_partitions + part;
-      p.ws_o[row * D + d] = acc;
-      if (d == 0) {
-        p.ws_ml[row * 2 + 0] = M;
-        p.ws_ml[row * 2 + 1] = l;
-      }
-    }
   }
 }
 
@@ -428,13 +593,16 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeParams p)
 template <class E, int D, int BOXR>
 cudaError_t launch_typed(const DecodeArgs &a, const DecodeParams &p, cudaStream_t stream) {
   using S = DecodeSmem<D>;
-  const int max_blocks = a.partition_size / a.block_size + 2;
-  const int smem = S::bytes(max_blocks);
-  auto kernel = decode_partition_kernel<E, D, BOXR>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int smem = S::bytes(a.num_seqs, p.max_ids);
+  auto kernel = decode_persistent_kernel<E, D, BOXR>;
+  cudaError_t e = allow_dynamic_smem<decode_persistent_kernel<E, D, BOXR>>();
   if (e != cudaSuccess) return e;
-  dim3 grid(a.num_partitions, a.num_kv_heads, a.num_seqs);
-  kernel<<<grid, kThreads, smem, stream>>>(p, a.tm_k, a.tm_v);
+  // Items are at most S * Hkv * partitions; two CTAs per SM, four workers each.
+  const int64_t items = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads * a.num_partitions;
+  int64_t grid = (items + kWorkers - 1) / kWorkers;
+  if (grid > 2LL * a.num_sms) grid = 2LL * a.num_sms;
+  if (grid < 1) grid = 1;
+  kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p, a.tm_k, a.tm_v);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.num_partitions <= 1) return e;
   decode_combine_kernel<E, D><<<a.num_seqs * a.num_q_heads, D,
@@ -447,13 +615,19 @@ cudaError_t launch_box(const DecodeArgs &a, const DecodeParams &p, cudaStream_t 
   switch (a.box_rows) {
     case 8: return launch_typed<E, D, 8>(a, p, stream);
     case 16: return launch_typed<E, D, 16>(a, p, stream);
-    case 32: return launch_typed<E, D, 32>(a, p, stream);
-    case 64: return launch_typed<E, D, 64>(a, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
+
+// Largest dynamic shared memory the decode kernel needs for this shape, so
+// the host can reject shapes that cannot launch.
+size_t decode_smem_bytes(int head_dim, int num_seqs, int partition_size, int block_size) {
+  const int max_ids = partition_size / block_size + 2;
+  return head_dim == 128 ? DecodeSmem<128>::bytes(num_seqs, max_ids)
+                         : DecodeSmem<64>::bytes(num_seqs, max_ids);
+}
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
   DecodeParams p;
@@ -466,6 +640,7 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
   p.context_lens = a.context_lens;
   p.capacity = a.capacity;
   p.max_ctx = a.max_context_len;
+  p.num_seqs = a.num_seqs;
   p.hq = a.num_q_heads;
   p.hkv = a.num_kv_heads;
   p.group = a.num_q_heads / a.num_kv_heads;
@@ -474,6 +649,7 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
   p.scale_log2 = a.scale_log2;
   p.partition_size = a.partition_size;
   p.num_partitions = a.num_partitions;
+  p.max_ids = a.partition_size / a.block_size + 2;
   p.ws_o = a.ws_o;
   p.ws_ml = a.ws_ml;
   p.err = a.d_error;

@@ -91,19 +91,20 @@ bool valid_block_size(int bs) { return bs == 8 || bs == 16 || bs == 32 || bs == 
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Split-KV plan.  Auto: enough partitions that the CTAs of the largest
-// possible batch cover every SM about four times (two CTAs per SM), each
-// partition at least 256 tokens so its pipeline start-up is amortised.
-int plan_partition(int num_seqs, int num_kv_heads, int max_ctx, int partition_size,
-                   int num_sms) {
+// Split-KV plan.  Auto: every worker warp (four per CTA, two CTAs per SM)
+// should get about eight items of the largest possible batch, so the static
+// item schedule balances; a partition is at least 64 tokens (128 when eight
+// query heads share a KV head) so the partial states stay a few percent of the
+// K/V bytes.
+int plan_partition(int num_seqs, int num_q_heads, int num_kv_heads, int max_ctx,
+                   int partition_size, int num_sms) {
   if (partition_size > 0) return partition_size;
   const long units = static_cast<long>(num_seqs > 0 ? num_seqs : 1) * num_kv_heads;
-  const long target = static_cast<long>(num_sms) * 2 * 4;
-  long parts = (target + units - 1) / units;
-  if (parts < 1) parts = 1;
-  long P = (max_ctx + parts - 1) / parts;
-  P = ((P + pa::kDecodeChunk - 1) / pa::kDecodeChunk) * pa::kDecodeChunk;
-  if (P < 256) P = 256;
+  const long target_items = static_cast<long>(num_sms) * 2 * pa::kDecodeWarps * 8;
+  long P = (units * max_ctx + target_items - 1) / target_items;
+  P = ((P + pa::kDecodeSub - 1) / pa::kDecodeSub) * pa::kDecodeSub;
+  const long pmin = (num_q_heads / num_kv_heads) > 4 ? 128 : 64;
+  if (P < pmin) P = pmin;
   if (P > (1 << 20)) P = 1 << 20;
   return static_cast<int>(P);
 }
@@ -169,11 +170,12 @@ pa_status pa_decode_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_h
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       max_context_len < 0 || partition_size < 0)
     return PA_ERR_SHAPE;
-  if (partition_size % pa::kDecodeChunk != 0) return PA_ERR_SHAPE;
+  if (partition_size % pa::kDecodeSub != 0) return PA_ERR_SHAPE;
   int sms = 0;
   cudaError_t e = current_num_sms(&sms);
   if (e != cudaSuccess) return cuda_fail(e);
-  const int P = plan_partition(num_seqs, num_kv_heads, max_context_len, partition_size, sms);
+  const int P = plan_partition(num_seqs, num_q_heads, num_kv_heads, max_context_len,
+                               partition_size, sms);
   const int64_t nparts = max_context_len > 0 ? (max_context_len + P - 1) / P : 1;
   size_t ws = 0;
   if (nparts > 1) {
@@ -205,7 +207,7 @@ pa_status pa_decode(void *out, int64_t out_row_stride, const void *query, int64_
   if (num_q_heads / num_kv_heads > pa::kDecodeMaxGroup) return PA_ERR_UNSUPPORTED;
   if (!valid_block_size(block_size)) return PA_ERR_UNSUPPORTED;
   if (num_blocks * block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
-  if (partition_size % pa::kDecodeChunk != 0) return PA_ERR_SHAPE;
+  if (partition_size % pa::kDecodeSub != 0) return PA_ERR_SHAPE;
   if (num_seqs == 0) return PA_OK;
   if (!out || !query || !key_cache || !value_cache || !block_table || !context_lens)
     return PA_ERR_NULL;
@@ -255,7 +257,12 @@ pa_status pa_decode(void *out, int64_t out_row_stride, const void *query, int64_
   }
   a.d_error = d_error;
   a.dtype = dtype;
-  a.box_rows = block_size < pa::kDecodeChunk ? block_size : pa::kDecodeChunk;
+  a.box_rows = block_size < pa::kDecodeSub ? block_size : pa::kDecodeSub;
+  cudaError_t e = current_num_sms(&a.num_sms);
+  if (e != cudaSuccess) return cuda_fail(e);
+  // The item schedule keeps per-sequence prefix sums in shared memory.
+  if (pa::decode_smem_bytes(head_dim, num_seqs, P, block_size) > 227 * 1024)
+    return PA_ERR_UNSUPPORTED;
   const int64_t rows = num_blocks * block_size;
   const int64_t row_stride = static_cast<int64_t>(num_kv_heads) * head_dim;
   if (!encode_rows_map(&a.tm_k, key_cache, dtype, head_dim, num_kv_heads, rows, row_stride,
@@ -263,7 +270,7 @@ pa_status pa_decode(void *out, int64_t out_row_stride, const void *query, int64_
       !encode_rows_map(&a.tm_v, value_cache, dtype, head_dim, num_kv_heads, rows, row_stride,
                        a.box_rows))
     return cuda_fail(cudaErrorInvalidValue);
-  cudaError_t e = pa::launch_decode(a, static_cast<cudaStream_t>(stream));
+  e = pa::launch_decode(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 

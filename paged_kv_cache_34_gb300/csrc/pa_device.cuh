@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -50,6 +51,26 @@ struct BF16 {
     return __uint_as_float(w & 0xffff0000u);
   }
 };
+
+// ---------------------------------------------------------------------------
+// Host: lift a kernel's dynamic shared-memory limit to the device maximum,
+// once per device.  The attribute call can wait for work in flight, so it
+// must not run on every launch.
+// ---------------------------------------------------------------------------
+template <auto Kernel>
+cudaError_t allow_dynamic_smem() {
+  static int done[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  int max_optin = 0;
+  e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = 1;
+  return e;
+}
 
 // ---------------------------------------------------------------------------
 // Device error flag (caller-owned int32, may be null)
@@ -137,6 +158,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
   }
 }
 
+// 2^x on the special-function unit (PTX ex2.approx, flush-to-zero): the
+// hardware instruction, not a library routine; 2^-inf = 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor) loads into shared memory
 // ---------------------------------------------------------------------------
@@ -152,6 +181,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
+}
+
+// 4-byte asynchronous global -> shared copies (no register staging).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------

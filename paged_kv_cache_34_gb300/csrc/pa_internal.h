@@ -26,9 +26,9 @@ struct ReshapeArgs {
 cudaError_t launch_reshape_and_cache(const ReshapeArgs &a, cudaStream_t stream);
 
 // Decode tiling shared by the planner and the kernels.
-constexpr int kDecodeWarps = 4;                  // consumer warps per CTA
-constexpr int kDecodeChunk = 16 * kDecodeWarps;  // tokens per pipeline stage
-constexpr int kDecodeMaxGroup = 8;               // query heads per KV head
+constexpr int kDecodeWarps = 4;     // consumer warps (independent workers) per CTA
+constexpr int kDecodeSub = 16;      // tokens per worker per pipeline stage
+constexpr int kDecodeMaxGroup = 8;  // query heads per KV head
 
 struct DecodeArgs {
   void *out;
@@ -49,8 +49,10 @@ struct DecodeArgs {
   pa_dtype dtype;
   CUtensorMap tm_k, tm_v;  // pool maps, box (64, 1, box_rows), 128B swizzle
   int box_rows;
+  int num_sms;
 };
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+size_t decode_smem_bytes(int head_dim, int num_seqs, int partition_size, int block_size);
 
 struct PrefillArgs {
   void *out;

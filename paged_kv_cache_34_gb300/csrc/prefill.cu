@@ -307,34 +307,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(kSFree + sb));
 
       const int bound = lim - kt * 128;  // columns 0..bound are visible
-      float mt = -INFINITY;
-      if (bound >= 127) {
+      if (bound < 127) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          s[c] *= sl;
-          mt = fmaxf(mt, s[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          s[c] = c <= bound ? s[c] * sl : -INFINITY;
-          mt = fmaxf(mt, s[c]);
-        }
+        for (int c = 0; c < 128; ++c) s[c] = c <= bound ? s[c] : -INFINITY;
       }
+      // Row max of the raw scores (scale > 0 keeps the order), as a tree.
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl;
       const bool raise_max = mt > m_ref + kRescaleThreshold;
       const float m_new = raise_max ? mt : m_ref;
-      const float corr = raise_max ? exp2f(m_ref - m_new) : 1.f;
+      const float corr = raise_max ? fast_exp2(m_ref - m_new) : 1.f;
       const float mu = m_new == -INFINITY ? 0.f : m_new;
-      // P is rounded to the input type for the tensor core; the row sum uses
-      // the same rounded values, so O / l is an exact weighted mean of V under
-      // the rounded weights.
+      // p = 2^(s * scale*log2(e) - max).  P is rounded to the input type for
+      // the tensor core; the row sum uses the same rounded values, so O / l is
+      // an exact weighted mean of V under the rounded weights.
       uint32_t pw[64];
-      float rs = 0.f;
+      float rsum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        pw[c] = E::pack2(exp2f(s[2 * c] - mu), exp2f(s[2 * c + 1] - mu));
-        rs += E::sum2(pw[c]);
+        pw[c] = E::pack2(fast_exp2(fmaf(s[2 * c], sl, -mu)),
+                         fast_exp2(fmaf(s[2 * c + 1], sl, -mu)));
+        rsum[c & 3] += E::sum2(pw[c]);
       }
+      const float rs = (rsum[0] + rsum[1]) + (rsum[2] + rsum[3]);
       if (kt >= 1) {
         // P(kt-1) has been consumed and O holds the sum through kt-1.
         ok = mbar_wait_bounded(bar(kPVDone), (kt - 1) & 1);
@@ -458,13 +458,11 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
   dim3 grid(static_cast<unsigned>(slots), a.num_q_heads);
   cudaError_t e;
   if (a.dtype == PA_BF16) {
-    e = cudaFuncSetAttribute(prefill_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
+    e = allow_dynamic_smem<prefill_kernel<BF16>>();
     if (e != cudaSuccess) return e;
     prefill_kernel<BF16><<<grid, kThreads, kSmemBytes, stream>>>(p, a.tm_q, a.tm_k, a.tm_v);
   } else {
-    e = cudaFuncSetAttribute(prefill_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
+    e = allow_dynamic_smem<prefill_kernel<F16>>();
     if (e != cudaSuccess) return e;
     prefill_kernel<F16><<<grid, kThreads, kSmemBytes, stream>>>(p, a.tm_q, a.tm_k, a.tm_v);
   }

@@ -124,13 +124,10 @@ class PagedInputs:
     def total_q(self) -> int:
         return int(self.q.shape[0])
 
-    @property
-    def max_context_len(self) -> int:
-        return int(self.context_lens.max().item()) if self.num_seqs else 0
-
-    @property
-    def max_seqlen_q(self) -> int:
-        return int(self.q_lens.max().item()) if self.num_seqs else 0
+    # Host-side upper bounds the caller passes to the library (computed once
+    # from the host copies, so reading them never synchronises a device).
+    max_context_len: int = 0
+    max_seqlen_q: int = 0
 
     def to(self, device) -> "PagedInputs":
         out = copy.copy(self)
@@ -264,5 +261,6 @@ def make_inputs(name_or_cfg, seed: int | None = None, *, lengths=None,
         cu_seqlens_q=torch.from_numpy(cu),
         block_table=torch.from_numpy(block_table),
         slot_mapping=torch.from_numpy(slots.astype(np.int64)),
-        q=q, k_new=k_new, v_new=v_new, k_pool=k_pool, v_pool=v_pool)
+        q=q, k_new=k_new, v_new=v_new, k_pool=k_pool, v_pool=v_pool,
+        max_context_len=int(ctx.max(initial=0)), max_seqlen_q=int(ql.max(initial=0)))
     return inputs.to(device) if str(device) != "cpu" else inputs
