@@ -9,24 +9,30 @@
 // sequence's keys.
 //
 // Design (the pages build a per-sequence mask from cu_seqlens on Ascend;
-// here nothing is masked outside the diagonal tile and nothing padded):
-//  * CTA = (128-row query tile of one sequence, query head).  Tiles are
-//    dealt heaviest-first (by tile index, i.e. by how many KV tiles the
-//    causal row range needs) so long tails start early.
-//  * Warp 4 (TMA): loads the Q tile once and streams 128-token K/V tiles
-//    into a 2-stage ring; each K/V tile is gathered block by block through
-//    block_table (one TMA box per block), with the 128-byte swizzle the MMA
-//    descriptors expect.
-//  * Warp 5 (MMA, one thread): S = Q K^T into a double-buffered TMEM tile
-//    (M=128, N=128, K=16 x 8 instructions), then O += P V with V read
-//    MN-major straight from its TMA tile.  S(kt+1) is issued before P(kt) is
-//    ready, so the tensor core works while the softmax runs.
-//  * Warps 0-3 (softmax, one thread per query row = TMEM lane): read S from
-//    TMEM, mask only tiles that cross the causal edge or the context end,
-//    exponentiate in base 2, and write P (bf16/fp16) to shared memory in the
-//    swizzled K-major layout.  The running max is only raised -- and O in
-//    TMEM rescaled -- when a row's max grows by more than 2^8, which keeps
-//    every P <= 256 and the result exact up to rounding.
+// here nothing is masked outside the diagonal tiles and nothing is padded):
+//  * CTA = (two consecutive 128-row query tiles A and B of one sequence,
+//    query head).  Both tiles share every K/V tile the CTA loads, halving the
+//    K/V traffic per flop.  Pairs are dealt heaviest first.
+//  * Warp 8 (TMA): loads Q_A and Q_B once, then streams K and V tiles (128
+//    tokens each) through separate K (2 buffers) and V (3 buffers) rings,
+//    K running one tile ahead of V; a K/V
+//    tile is gathered block by block through block_table, one TMA box per
+//    block issued by its own lane, with the 128-byte swizzle the MMA
+//    descriptors expect.  The next tile's block ids are loaded while the
+//    current tile is issued.
+//  * Warp 9 (one thread): tcgen05.mma kind::f16, M = 128, N = 128, K = 16 x 8:
+//    S_t = Q_t K^T into TMEM and O_t += P_t V (V read MN-major straight from
+//    its TMA tile, P from TMEM).  The issue order S_A S_B | PV_A S_A' | PV_B
+//    S_B' | ... keeps the tensor core busy with one tile while the other
+//    tile's softmax runs (ping-pong); the tensor core executes one thread's
+//    MMAs in order, so S_t' may overwrite the columns P_t was read from.
+//  * Warps 0-3 / 4-7: the softmax of tile A / B, one thread per query row
+//    (= TMEM lane): S from TMEM, masks only where a tile crosses the causal
+//    edge or the context end, base-2 exponentials on the SFU, P rounded to
+//    the input type and written back into TMEM over S.  The running max
+//    is only raised -- and O in TMEM rescaled -- when a row's max grows by
+//    more than 2^8, which keeps every P <= 256 and the result exact up to
+//    rounding.
 //  * Epilogue: O / l from TMEM to registers to global memory.
 #include <math.h>
 
@@ -38,19 +44,43 @@ namespace pa {
 
 namespace {
 
-constexpr int kThreads = 192;             // warps 0-3 softmax, 4 TMA, 5 MMA
-constexpr int kHalf = 128 * 128;          // 128 rows x 64 elements x 2 B
-constexpr int kTile = 2 * kHalf;          // 128 x 128 tile, two 64-wide halves
-constexpr int kQOff = 0;
-constexpr int kKVOff = kTile;             // stage s: K at +s*2*kTile, V +kTile
-constexpr int kPOff = kKVOff + 4 * kTile;
-constexpr int kBarOff = kPOff + kTile;
-enum { kQFull = 0, kKVFull = 1, kKVEmpty = 3, kSFull = 5, kSFree = 7, kPFull = 9, kPVDone = 10,
-       kFin = 11, kNumBars = 12 };
+constexpr int kThreads = 320;       // warps 0-3 softmax A, 4-7 softmax B, 8 TMA, 9 MMA
+constexpr int kTmaWarp = 8, kMmaWarp = 9;
+constexpr int kHalf = 128 * 128;    // 128 rows x 64 elements x 2 B
+constexpr int kTile = 2 * kHalf;    // 128 x 128 tile, two 64-wide halves
+#ifndef PA_PREFILL_K_BUFS
+#define PA_PREFILL_K_BUFS 2
+#endif
+constexpr int kKBufs = PA_PREFILL_K_BUFS;  // separate K and V rings (5 buffers)
+constexpr int kVBufs = 5 - kKBufs;
+constexpr int kKVBufs = kKBufs + kVBufs;
+constexpr int kQOff = 0;                           // Q_A, Q_B
+constexpr int kKVOff = 2 * kTile;                  // K/V ring
+constexpr int kBarOff = kKVOff + kKVBufs * kTile;
+enum {
+  kQFull = 0,
+  kKVFull = 1,
+  kKVEmpty = kKVFull + kKVBufs,
+  kSFull = kKVEmpty + kKVBufs,
+  kPFull = kSFull + 2,
+  kPVDone = kPFull + 2,
+  kQEmpty = kPVDone + 2,
+  kEpiDone = kQEmpty + 1,
+  kItemGo = kEpiDone + 1,
+  kFin = kItemGo + 1,
+  kNumBars = kFin + 1
+};
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
 constexpr int kSmemBytes = 1024 + kMiscOff + 64;
-constexpr uint32_t kTmemCols = 512;       // S0 | S1 | O | unused
-constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest P allowed
+constexpr uint32_t kTmemCols = 512;         // S_A | S_B | O_A | O_B (P_t overlays S_t)
+constexpr float kRescaleThreshold = 8.0f;   // log2 of the largest P allowed
+// Pairs of exponentials whose index i has (i & kPolyMask) == kPolyMask run on
+// the FMA pipe instead of the SFU (1 = every other pair, 3 = one in four,
+// -1 = none).  Measured on GB300 the SFU is not the limit here, so none.
+#ifndef PA_PREFILL_POLY_MASK
+#define PA_PREFILL_POLY_MASK -1
+#endif
+constexpr int kPolyMask = PA_PREFILL_POLY_MASK;
 
 struct PrefillParams {
   void *out;
@@ -65,35 +95,37 @@ struct PrefillParams {
   int64_t num_blocks;
   float scale_log2;
   int32_t causal;
+  int32_t num_items;
   int32_t *err;
 };
 
-// Which (sequence, query tile) this CTA serves: slot x of the list ordered by
-// tile index descending, sequences in order within one tile index.
-__device__ void find_tile(const PrefillParams &p, int x, int lane, int *seq_out, int *tile_out) {
-  const int max_tiles = (p.max_seqlen_q + 127) / 128;
+// Which (sequence, 256-row pair of query tiles) this CTA serves: slot x of
+// the list ordered by pair index descending (the later pairs of a causal
+// sequence need the most K/V tiles), sequences in order within one index.
+__device__ void find_pair(const PrefillParams &p, int x, int lane, int *seq_out, int *pair_out) {
+  const int max_pairs = (p.max_seqlen_q + 255) / 256;
   int rem = x;
-  for (int i = max_tiles - 1; i >= 0; --i) {
+  for (int i = max_pairs - 1; i >= 0; --i) {
     for (int c0 = 0; c0 < p.num_seqs; c0 += 32) {
       const int s = c0 + lane;
       bool has = false;
       if (s < p.num_seqs) {
         const int q = __ldg(p.cu + s + 1) - __ldg(p.cu + s);
-        has = q >= 0 && q <= p.max_seqlen_q && (q + 127) / 128 > i;
+        has = q >= 0 && q <= p.max_seqlen_q && (q + 255) / 256 > i;
       }
       unsigned bal = __ballot_sync(0xffffffffu, has);
       const int n = __popc(bal);
       if (rem < n) {
         for (int k = 0; k < rem; ++k) bal &= bal - 1;
         *seq_out = c0 + __ffs(bal) - 1;
-        *tile_out = i;
+        *pair_out = i;
         return;
       }
       rem -= n;
     }
   }
   *seq_out = -1;
-  *tile_out = -1;
+  *pair_out = -1;
 }
 
 // cu_seqlens must start at 0, never decrease, end at total_q, and no
@@ -106,6 +138,54 @@ __device__ void check_cu_seqlens(const PrefillParams &p, int lane) {
     bad |= q < 0 || q > p.max_seqlen_q;
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) raise_error(p.err, PA_DEVERR_CU_SEQLENS);
+}
+
+// Ring slots: K of tile kt in slot kt % 2, V of tile kt in slot 2 + kt % 3;
+// the parity is that of the slot's use count.
+__device__ __forceinline__ int k_slot(int kt) { return kt % kKBufs; }
+__device__ __forceinline__ uint32_t k_par(int kt) { return (kt / kKBufs) & 1; }
+__device__ __forceinline__ int v_slot(int kt) { return kKBufs + kt % kVBufs; }
+__device__ __forceinline__ uint32_t v_par(int kt) { return (kt / kVBufs) & 1; }
+
+// One work item: a (sequence, pair of query tiles, query head), with the
+// geometry every role derives from it.
+struct PairItem {
+  int seq, h, q_start, q_len, L, lim_base;
+  int row0[2], nkv_t[2], nkv;
+  bool has_b;
+};
+
+// Item x of the static list (slot x / Hq in find_pair's order, head x % Hq).
+// Warp-collective.
+__device__ PairItem item_at(const PrefillParams &p, int x, int lane, bool report) {
+  PairItem it;
+  int seq, pair;
+  find_pair(p, x / p.hq, lane, &seq, &pair);
+  it.seq = seq;
+  it.h = x % p.hq;
+  it.q_start = it.q_len = it.L = it.lim_base = 0;
+  it.row0[0] = it.row0[1] = 0;
+  it.nkv_t[0] = it.nkv_t[1] = 0;
+  if (seq >= 0) {
+    it.q_start = __ldg(p.cu + seq);
+    it.q_len = __ldg(p.cu + seq + 1) - it.q_start;
+    it.L = checked_context_len(__ldg(p.ctx + seq), p.capacity, p.max_ctx, p.err,
+                               report && lane == 0 && it.h == 0 && pair == 0);
+    it.lim_base = p.causal ? it.L - it.q_len : 0x3fffffff;  // row i sees keys <= lim_base + i
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      it.row0[t] = pair * 256 + t * 128;
+      if (it.row0[t] < it.q_len) {
+        int kv_end = it.L;
+        if (p.causal) kv_end = min(it.L, it.L - it.q_len + it.row0[t] + 128);
+        if (kv_end < 0) kv_end = 0;
+        it.nkv_t[t] = (kv_end + 127) / 128;
+      }
+    }
+  }
+  it.nkv = max(it.nkv_t[0], it.nkv_t[1]);
+  it.has_b = seq >= 0 && it.row0[1] < it.q_len;
+  return it;
 }
 
 template <class E>
@@ -121,155 +201,215 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.y;
+  const int x0 = blockIdx.x, dx = gridDim.x;  // this CTA's items: x0, x0+dx, ...
 
   if (warp == 0) {
-    int seq, tile;
-    find_tile(p, blockIdx.x, lane, &seq, &tile);
-    if (lane == 0) {
-      misc[0] = seq;
-      misc[1] = tile;
-      misc[3] = 0;  // abort: some wait gave up
-    }
-    if (blockIdx.x == 0 && h == 0) check_cu_seqlens(p, lane);
+    if (lane == 0) misc[3] = 0;  // abort: some wait gave up
+    if (blockIdx.x == 0) check_cu_seqlens(p, lane);
   }
   if (warp == 1 && lane == 0) {
-    // S-free and P-full collect one arrival per softmax warp.
-    for (int i = 0; i < kNumBars; ++i)
-      mbar_init(bar(i), (i == kSFree || i == kSFree + 1 || i == kPFull) ? 4 : 1);
+    // P-full collects one arrival per softmax warp of its tile, the
+    // epilogue barrier one per softmax warp of both tiles.
+    for (int i = 0; i < kNumBars; ++i) {
+      uint32_t n = 1;
+      if (i == kPFull || i == kPFull + 1) n = 4;
+      if (i == kEpiDone) n = 8;
+      mbar_init(bar(i), n);
+    }
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(const_cast<int *>(misc + 2)), kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const int seq = misc[0], tile = misc[1];
   const uint32_t tbase = static_cast<uint32_t>(misc[2]);
 
-  int nkv = 0, q_start = 0, rows_valid = 0, L = 0, lim_base = 0, row0 = 0;
-  if (seq >= 0) {
-    q_start = __ldg(p.cu + seq);
-    const int q_len = __ldg(p.cu + seq + 1) - q_start;
-    L = checked_context_len(__ldg(p.ctx + seq), p.capacity, p.max_ctx, p.err,
-                            tid == 0 && h == 0 && tile == 0);
-    row0 = tile * 128;
-    rows_valid = min(128, q_len - row0);
-    lim_base = p.causal ? L - q_len : 0x3fffffff;  // row i sees keys <= lim_base + i
-    int kv_end = L;
-    if (p.causal) kv_end = min(L, L - q_len + row0 + 128);
-    if (kv_end < 0) kv_end = 0;
-    nkv = (kv_end + 127) / 128;
-  }
-  const int g = h / p.group;
-
-  if (warp == 4) {
+  if (warp == kTmaWarp) {
     // ----------------------------------------------------------- TMA --
-    if (lane == 0 && nkv > 0) {
+    if (lane == 0) {
       tma_prefetch_desc(&tmq);
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv);
-      const uint32_t qs = smem_u32(smem + kQOff);
-      mbar_arrive_expect_tx(bar(kQFull), kTile);
-      tma_load_3d(qs, &tmq, bar(kQFull), 0, h, q_start + row0);
-      tma_load_3d(qs + kHalf, &tmq, bar(kQFull), 64, h, q_start + row0);
-      const int bs = p.block_size;  // one TMA box per block (16..128 rows)
-      const int boxr = bs;
-      const int nbox = 128 / boxr;
-      const int32_t *bt = p.block_table + static_cast<int64_t>(seq) * p.bt_stride;
-      int issued = 0;
-      for (int kt = 0; kt < nkv; ++kt) {
-        const int st = kt & 1;
-        if (kt >= 2 && !mbar_wait_bounded(bar(kKVEmpty + st), ((kt >> 1) - 1) & 1)) {
-          raise_error(p.err, PA_DEVERR_TIMEOUT);
-          misc[3] = 1;
-          break;
-        }
-        if (misc[3]) break;
-        const int j0 = kt * 128;
-        int rows[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) rows[k] = -1;
-        int n = 0;
-        for (int k = 0; k < nbox; ++k) {
-          const int j = j0 + k * boxr;
-          if (j >= L) break;
-          const int id = __ldg(bt + j / bs);
-          if (id < 0 || id >= p.num_blocks) {
-            raise_error(p.err, PA_DEVERR_BLOCK_ID);
-            continue;
-          }
-          rows[k] = id * bs + (j % bs);
-          ++n;
-        }
-        const uint32_t kd = smem_u32(smem + kKVOff + st * 2 * kTile);
-        const uint32_t vd = kd + kTile;
-        mbar_arrive_expect_tx(bar(kKVFull + st), static_cast<uint32_t>(n * boxr * 128 * 4));
-        for (int k = 0; k < nbox; ++k) {
-          if (rows[k] < 0) continue;
-          const uint32_t off = k * boxr * 128;
-          tma_load_3d(kd + off, &tmk, bar(kKVFull + st), 0, g, rows[k]);
-          tma_load_3d(kd + kHalf + off, &tmk, bar(kKVFull + st), 64, g, rows[k]);
-          tma_load_3d(vd + off, &tmv, bar(kKVFull + st), 0, g, rows[k]);
-          tma_load_3d(vd + kHalf + off, &tmv, bar(kKVFull + st), 64, g, rows[k]);
-        }
-        ++issued;
+    }
+    const int bs = p.block_size;
+    const int nbox = 128 / bs;  // one box per block, lane k loads block k of a tile
+    int kbase = 0;              // K/V tiles of earlier items (ring positions)
+    bool ok = true;
+    int nk = 0, nv = 0;         // K and V tiles issued in all
+    int j = 0;
+    for (int x = x0; ok && x < p.num_items; x += dx, ++j) {
+      const PairItem it = item_at(p, x, lane, true);
+      if (it.seq < 0) break;
+      const int g = it.h / p.group;
+      // Q of item j once the previous item's last QK has read Q.
+      if (lane == 0 && j > 0) ok = mbar_wait_bounded(bar(kQEmpty), (j - 1) & 1);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok || misc[3]) {
+        ok = false;
+        break;
       }
+      if (lane == 0) {
+        const uint32_t qs = smem_u32(smem + kQOff);
+        const int qtiles = it.nkv > 0 ? (it.has_b ? 2 : 1) : 0;
+        mbar_arrive_expect_tx(bar(kQFull), qtiles * kTile);
+        for (int t = 0; t < qtiles; ++t) {
+          tma_load_3d(qs + t * kTile, &tmq, bar(kQFull), 0, it.h, it.q_start + it.row0[t]);
+          tma_load_3d(qs + t * kTile + kHalf, &tmq, bar(kQFull), 64, it.h,
+                      it.q_start + it.row0[t]);
+        }
+      }
+      const int32_t *bt = p.block_table + static_cast<int64_t>(it.seq) * p.bt_stride;
+      auto load_id = [&](int kt) {
+        return (lane < nbox && kt < it.nkv && kt * 128 + lane * bs < it.L)
+                   ? __ldg(bt + kt * nbox + lane)
+                   : -1;
+      };
+      // Issue order K0 K1 V0 K2 V1 ...: K runs one tile ahead of V, since S
+      // needs K a whole softmax earlier than O needs V.
+      int id_k = load_id(0), id_v = -1;
+      for (int jj = 0; jj <= it.nkv && ok; ++jj) {
+        const int id_nxt = load_id(jj + 1);  // in flight while this step issues
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          const int kt = which == 0 ? jj : jj - 1;  // K of tile jj, then V of tile jj-1
+          if (kt < 0 || kt >= it.nkv) continue;
+          const int id = which == 0 ? id_k : id_v;
+          const bool want = lane < nbox && kt * 128 + lane * bs < it.L;
+          const bool valid = want && id >= 0 && id < p.num_blocks;
+          if (which == 0 && want && !valid) raise_error(p.err, PA_DEVERR_BLOCK_ID);
+          const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+          const int n = kbase + kt;  // ring position
+          const int slot = which == 0 ? k_slot(n) : v_slot(n);
+          const int nuse = which == 0 ? n / kKBufs : n / kVBufs;  // earlier uses of slot
+          if (lane == 0 && nuse > 0)
+            ok = mbar_wait_bounded(bar(kKVEmpty + slot), (nuse - 1) & 1);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok || misc[3]) {
+            ok = false;
+            break;
+          }
+          if (lane == 0)
+            mbar_arrive_expect_tx(bar(kKVFull + slot),
+                                  static_cast<uint32_t>(__popc(vmask)) * bs * 128 * 2);
+          __syncwarp();
+          if (valid) {
+            const uint32_t dst = smem_u32(smem + kKVOff + slot * kTile) + lane * bs * 128;
+            const CUtensorMap *map = which == 0 ? &tmk : &tmv;
+            tma_load_3d(dst, map, bar(kKVFull + slot), 0, g, id * bs);
+            tma_load_3d(dst + kHalf, map, bar(kKVFull + slot), 64, g, id * bs);
+          }
+          if (which == 0) ++nk;
+          else ++nv;
+        }
+        id_v = id_k;
+        id_k = id_nxt;
+      }
+      kbase += it.nkv;
+    }
+    if (!ok && lane == 0) {
+      if (!misc[3]) raise_error(p.err, PA_DEVERR_TIMEOUT);
+      misc[3] = 1;
       // Do not leave while copies this CTA issued may still land.
-      mbar_wait_bounded(bar(kQFull), 0);
-      for (int kt = issued - 1; kt >= 0 && kt >= issued - 2; --kt)
-        mbar_wait_bounded(bar(kKVFull + (kt & 1)), (kt >> 1) & 1);
+      mbar_wait_bounded(bar(kQFull), (j - 1) & 1);
+      for (int n = nk - 1; n >= 0 && n >= nk - kKBufs; --n)
+        mbar_wait_bounded(bar(kKVFull + k_slot(n)), k_par(n));
+      for (int n = nv - 1; n >= 0 && n >= nv - kVBufs; --n)
+        mbar_wait_bounded(bar(kKVFull + v_slot(n)), v_par(n));
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------- MMA --
-    if (lane == 0 && nkv > 0) {
-      constexpr bool kBF = E::kBF16;
-      const uint32_t id_qk = idesc_f16(kBF, 128, 128, false);
-      const uint32_t id_pv = idesc_f16(kBF, 128, 128, true);
-      const uint32_t qs = smem_u32(smem + kQOff);
-      const uint32_t ps = smem_u32(smem + kPOff);
-      const uint32_t t_o = tbase + 256;
-      bool ok = mbar_wait_bounded(bar(kQFull), 0);
-      auto issue_pv = [&](int kt) {
-        const uint32_t vs = smem_u32(smem + kKVOff + (kt & 1) * 2 * kTile + kTile);
+    constexpr bool kBF = E::kBF16;
+    const uint32_t id_qk = idesc_f16(kBF, 128, 128, false);
+    const uint32_t id_pv = idesc_f16(kBF, 128, 128, true);
+    int kbase = 0;            // ring position of this item's first K/V tile
+    int pcnt[2] = {0, 0};     // P tiles consumed per query tile (all items)
+    bool ok = true;
+    int j = 0;
+    for (int x = x0; ok && x < p.num_items; x += dx, ++j) {
+      const PairItem it = item_at(p, x, lane, false);
+      if (it.seq < 0) break;
+      if (lane == 0) {
+        auto qk = [&](int t, int kt) {  // S_t = Q_t K_kt^T
+          const uint32_t qs = smem_u32(smem + kQOff + t * kTile);
+          const uint32_t ks = smem_u32(smem + kKVOff + k_slot(kbase + kt) * kTile);
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          umma_f16_ss(t_o, sdesc_sw128(ps + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024),
-                      sdesc_sw128(vs + k * 2048, kHalf, 1024), id_pv, (kt > 0 || k > 0) ? 1u : 0u);
-        umma_commit(bar(kPVDone));
-        umma_commit(bar(kKVEmpty + (kt & 1)));
-      };
-      for (int kt = 0; ok && kt < nkv; ++kt) {
-        const int st = kt & 1;
-        ok = mbar_wait_bounded(bar(kKVFull + st), (kt >> 1) & 1);
-        if (ok && kt >= 2) ok = mbar_wait_bounded(bar(kSFree + st), ((kt >> 1) - 1) & 1);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t ks = smem_u32(smem + kKVOff + st * 2 * kTile);
+          for (int k = 0; k < 8; ++k)
+            umma_f16_ss(tbase + t * 128,
+                        sdesc_sw128(qs + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024),
+                        sdesc_sw128(ks + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024), id_qk,
+                        k > 0 ? 1u : 0u);
+          umma_commit(bar(kSFull + t));
+        };
+        auto pv = [&](int t, int kt) {  // O_t += P_t V_kt, P_t from TMEM
+          const uint32_t vs = smem_u32(smem + kKVOff + v_slot(kbase + kt) * kTile);
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          umma_f16_ss(tbase + st * 128,
-                      sdesc_sw128(qs + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024),
-                      sdesc_sw128(ks + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024), id_qk,
-                      k > 0 ? 1u : 0u);
-        umma_commit(bar(kSFull + st));
-        if (kt >= 1) {
-          ok = mbar_wait_bounded(bar(kPFull), (kt - 1) & 1);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(kt - 1);
-        }
-      }
-      if (ok) {
-        ok = mbar_wait_bounded(bar(kPFull), (nkv - 1) & 1);
+          for (int k = 0; k < 8; ++k)
+            umma_f16_ts(tbase + 256 + t * 128, tbase + t * 128 + 8 * k,
+                        sdesc_sw128(vs + k * 2048, kHalf, 1024), id_pv,
+                        (kt > 0 || k > 0) ? 1u : 0u);
+          umma_commit(bar(kPVDone + t));
+        };
+        // The previous item's epilogues have read O and S; tell the softmax
+        // warps this item may start.
+        if (j > 0) ok = mbar_wait_bounded(bar(kEpiDone), (j - 1) & 1);
         if (ok) {
           tc_fence_after();
-          issue_pv(nkv - 1);
+          mbar_arrive(bar(kItemGo));
+          ok = mbar_wait_bounded(bar(kQFull), j & 1);
+        }
+        if (ok && it.nkv > 0) {
+          ok = mbar_wait_bounded(bar(kKVFull + k_slot(kbase)), k_par(kbase));
+          if (ok) {
+            tc_fence_after();
+            if (it.nkv_t[0] > 0) qk(0, 0);
+            if (it.nkv_t[1] > 0) qk(1, 0);
+            umma_commit(bar(kKVEmpty + k_slot(kbase)));
+          }
+        }
+        if (ok && it.nkv <= 1) umma_commit(bar(kQEmpty));  // no further QK reads Q
+        for (int kt = 0; ok && kt < it.nkv; ++kt) {
+          const bool more = kt + 1 < it.nkv;
+          // Each group waits only for its own operands: PV for V_kt and P,
+          // the next QK for K_{kt+1}, so a late K never holds back a PV.
+          bool have_v = false, have_k = !more;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (kt < it.nkv_t[t]) {
+              if (!have_v) {
+                ok = mbar_wait_bounded(bar(kKVFull + v_slot(kbase + kt)), v_par(kbase + kt));
+                have_v = true;
+              }
+              if (ok) ok = mbar_wait_bounded(bar(kPFull + t), pcnt[t] & 1);
+              if (!ok) break;
+              tc_fence_after();
+              pv(t, kt);
+              ++pcnt[t];
+            }
+            if (kt + 1 < it.nkv_t[t]) {
+              if (!have_k) {
+                ok = mbar_wait_bounded(bar(kKVFull + k_slot(kbase + kt + 1)),
+                                       k_par(kbase + kt + 1));
+                have_k = true;
+                if (!ok) break;
+                tc_fence_after();
+              }
+              qk(t, kt + 1);
+            }
+          }
+          if (!ok) break;
+          if (kt + 2 == it.nkv) umma_commit(bar(kQEmpty));  // the item's last QK
+          umma_commit(bar(kKVEmpty + v_slot(kbase + kt)));
+          if (more) umma_commit(bar(kKVEmpty + k_slot(kbase + kt + 1)));
         }
       }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      kbase += it.nkv;
+    }
+    if (lane == 0) {
       if (!ok) {
         raise_error(p.err, PA_DEVERR_TIMEOUT);
         misc[3] = 1;
@@ -281,147 +421,178 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------- softmax --
-    const int r = tid;  // query row in the tile == TMEM lane
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
-    const int lim = min(lim_base + row0 + r, L - 1);  // last visible key
+    const int t = warp >> 2;   // tile A or B
+    const int r = tid & 127;   // query row in the tile == TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_tm = tbase + lane_addr + t * 128;
+    const uint32_t o_tm = tbase + lane_addr + 256 + t * 128;
     const float sl = p.scale_log2;
-    float m_ref = -INFINITY, l = 0.f;
+    int kbase = 0;   // ring position of the item's first V tile
+    int n = 0;       // S tiles of this query tile processed in all items
     bool ok = true;
-    uint8_t *prow = smem + kPOff + r * 128;
-    for (int kt = 0; kt < nkv; ++kt) {
-      const int sb = kt & 1;
-      ok = mbar_wait_bounded(bar(kSFull + sb), (kt >> 1) & 1);
+    int j = 0;
+    for (int x = x0; ok && x < p.num_items; x += dx, ++j) {
+      const PairItem it = item_at(p, x, lane, false);
+      if (it.seq < 0) break;
+      ok = mbar_wait_bounded(bar(kItemGo), j & 1);
       if (!ok) break;
-      tc_fence_after();
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tbase + lane_addr + sb * 128 + c * 32, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kSFree + sb));
-
-      const int bound = lim - kt * 128;  // columns 0..bound are visible
-      if (bound < 127) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = c <= bound ? s[c] : -INFINITY;
-      }
-      // Row max of the raw scores (scale > 0 keeps the order), as a tree.
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = s[i];
-#pragma unroll
-      for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl;
-      const bool raise_max = mt > m_ref + kRescaleThreshold;
-      const float m_new = raise_max ? mt : m_ref;
-      const float corr = raise_max ? fast_exp2(m_ref - m_new) : 1.f;
-      const float mu = m_new == -INFINITY ? 0.f : m_new;
-      // p = 2^(s * scale*log2(e) - max).  P is rounded to the input type for
-      // the tensor core; the row sum uses the same rounded values, so O / l is
-      // an exact weighted mean of V under the rounded weights.
-      uint32_t pw[64];
-      float rsum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        pw[c] = E::pack2(fast_exp2(fmaf(s[2 * c], sl, -mu)),
-                         fast_exp2(fmaf(s[2 * c + 1], sl, -mu)));
-        rsum[c & 3] += E::sum2(pw[c]);
-      }
-      const float rs = (rsum[0] + rsum[1]) + (rsum[2] + rsum[3]);
-      if (kt >= 1) {
-        // P(kt-1) has been consumed and O holds the sum through kt-1.
-        ok = mbar_wait_bounded(bar(kPVDone), (kt - 1) & 1);
+      const int my_nkv = it.nkv_t[t];
+      const int lim = min(it.lim_base + it.row0[t] + r, it.L - 1);  // last visible key
+      float m_ref = -INFINITY, l = 0.f;
+      for (int kt = 0; kt < my_nkv; ++kt, ++n) {
+        ok = mbar_wait_bounded(bar(kSFull + t), n & 1);
         if (!ok) break;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, raise_max)) {
+        const int bound = lim - kt * 128;  // columns 0..bound are visible
+        const bool edge = bound < 127;     // the tile crosses the causal edge or L
+        // The whole S row in one TMEM round trip.
+        uint32_t v[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(s_tm + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
+        tmem_wait_ld();
+        if (edge) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c > bound) v[c] = __float_as_uint(-INFINITY);
+        }
+        // Row max of the raw scores (scale > 0 keeps the order), as a tree.
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(v[i]);
+#pragma unroll
+        for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(v[c]));
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl;
+        const bool raise_max = mt > m_ref + kRescaleThreshold;
+        const float m_new = raise_max ? mt : m_ref;
+        const float corr = raise_max ? fast_exp2(m_ref - m_new) : 1.f;
+        const float mu = m_new == -INFINITY ? 0.f : m_new;
+        if (kt >= 1) {
+          // P(kt-1) has been consumed and O holds the sum through kt-1 (PV(kt-1)
+          // was issued before S(kt), so this wait is normally already over).
+          ok = mbar_wait_bounded(bar(kPVDone + t), (n - 1) & 1);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        // The first tile to read V_kt zeroes its rows past the context end
+        // (they may hold anything, even NaN; their weight is zero).
+        const bool first_reader = t == 0 || kt >= it.nkv_t[0];
+        if (first_reader && it.L < (kt + 1) * 128) {
+          const int vn = kbase + kt;
+          ok = mbar_wait_bounded(bar(kKVFull + v_slot(vn)), v_par(vn));
+          if (!ok) break;
+          uint8_t *vt = smem + kKVOff + v_slot(vn) * kTile;
+          const int first = it.L - kt * 128;
+          for (int i = r; i < (128 - first) * 16; i += 128) {
+            const int row = first + i / 16, c16 = i % 16;
+            *reinterpret_cast<uint4 *>(vt + (c16 >> 3) * kHalf + row * 128 + (c16 & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+        }
+        // p = 2^(s * scale*log2(e) - max), rounded to the input type for the
+        // tensor core; the row sum uses the same rounded values, so O / l is
+        // an exact weighted mean of V under the rounded weights.
+        const uint64_t sl2 = f2_pack(sl, sl), nmu2 = f2_pack(-mu, -mu);
+        uint64_t rs2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+        for (int hf = 0; hf < 4; ++hf) {  // 32 columns -> 16 packed words
+          uint32_t pw[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int i = hf * 16 + k;  // column pair
+            float x0f, x1f, e0, e1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                             sl2, nmu2),
+                      x0f, x1f);
+            if ((i & kPolyMask) == kPolyMask) {
+              f2_unpack(f2_exp2_poly(x0f, x1f), e0, e1);
+              if (edge) {
+                e0 = 2 * i <= bound ? e0 : 0.f;
+                e1 = 2 * i + 1 <= bound ? e1 : 0.f;
+              }
+            } else {
+              e0 = fast_exp2(x0f);  // 2^-inf = 0 for masked columns
+              e1 = fast_exp2(x1f);
+            }
+            pw[k] = E::pack2(e0, e1);
+            rs2[k & 1] = f2_add(rs2[k & 1], f2_pack(E::lo(pw[k]), E::hi(pw[k])));
+          }
+          // P overlays the first 64 columns of this tile's S in TMEM, two
+          // 16-bit values per column (the A operand of O += P V).
+          tmem_st16(s_tm + hf * 16, pw);
+        }
+        tmem_wait_st();
+        if (kt >= 1 && __any_sync(0xffffffffu, raise_max)) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            uint32_t v[32];
-            const uint32_t ta = tbase + lane_addr + 256 + c * 32;
-            tmem_ld32(ta, v);
+            uint32_t o[32];
+            tmem_ld32(o_tm + c * 32, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
-            tmem_st32(ta, v);
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+            tmem_st32(o_tm + c * 32, o);
           }
           tmem_wait_st();
         }
+        float rsum[4];
+        f2_unpack(rs2[0], rsum[0], rsum[1]);
+        f2_unpack(rs2[1], rsum[2], rsum[3]);
+        l = l * corr + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
+        m_ref = m_new;
+        fence_proxy_async_smem();  // V-tail zeroing (generic writes) before the MMA
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kPFull + t));
       }
-      l = l * corr + rs;
-      m_ref = m_new;
-
-      if (kt == nkv - 1 && L < (kt + 1) * 128) {
-        // Rows past the context end may hold anything (even NaN); their
-        // weight is zero, so make their V rows exact zeros for the MMA.
-        ok = mbar_wait_bounded(bar(kKVFull + (kt & 1)), (kt >> 1) & 1);
-        if (!ok) break;
-        uint8_t *vt = smem + kKVOff + (kt & 1) * 2 * kTile + kTile;
-        const int first = L - kt * 128;
-        for (int i = tid; i < (128 - first) * 16; i += 128) {
-          const int row = first + i / 16, c16 = i % 16;
-          *reinterpret_cast<uint4 *>(vt + (c16 >> 3) * kHalf + row * 128 + (c16 & 7) * 16) =
-              make_uint4(0, 0, 0, 0);
+      // ---------------------------------------------------- epilogue --
+      if (ok && it.row0[t] < it.q_len) {
+        const bool have_o = my_nkv > 0 && mbar_wait_bounded(bar(kPVDone + t), (n - 1) & 1);
+        ok = my_nkv == 0 || have_o;
+        if (my_nkv > 0) tc_fence_after();
+        const float inv_l = (have_o && l > 0.f) ? 1.f / l : 0.f;
+        const int64_t grow = static_cast<int64_t>(it.q_start) + it.row0[t] + r;
+        const bool store = it.row0[t] + r < it.q_len && grow >= 0 && grow < p.total_q;
+        typename E::T *orow =
+            static_cast<typename E::T *>(p.out) + grow * p.out_row_stride + it.h * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          if (have_o) {
+            tmem_ld32(o_tm + c * 32, o);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+          }
+          if (store) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint4 w;
+              const float *f = reinterpret_cast<const float *>(o) + q4 * 8;
+              w.x = E::pack2(f[0] * inv_l, f[1] * inv_l);
+              w.y = E::pack2(f[2] * inv_l, f[3] * inv_l);
+              w.z = E::pack2(f[4] * inv_l, f[5] * inv_l);
+              w.w = E::pack2(f[6] * inv_l, f[7] * inv_l);
+              *reinterpret_cast<uint4 *>(orow + c * 32 + q4 * 8) = w;
+            }
+          }
         }
       }
-      // P row -> shared memory, K-major with the 128-byte swizzle.
-#pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
-        const uint4 w = make_uint4(pw[c8 * 4 + 0], pw[c8 * 4 + 1], pw[c8 * 4 + 2], pw[c8 * 4 + 3]);
-        *reinterpret_cast<uint4 *>(prow + (c8 >> 3) * kHalf + (((c8 & 7) ^ (r & 7)) << 4)) = w;
-      }
-      fence_proxy_async_smem();
+      kbase += it.nkv;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kPFull));
+      if (lane == 0) mbar_arrive(bar(kEpiDone));  // O and S of this item are free
     }
     if (!ok) {
       raise_error(p.err, PA_DEVERR_TIMEOUT);
       misc[3] = 1;
     }
-    // ------------------------------------------------------ epilogue --
-    if (seq >= 0) {
-      const bool have_o = ok && nkv > 0 && mbar_wait_bounded(bar(kPVDone), (nkv - 1) & 1);
-      if (nkv > 0) tc_fence_after();
-      const float inv_l = (have_o && l > 0.f) ? 1.f / l : 0.f;
-      const int64_t grow = static_cast<int64_t>(q_start) + row0 + r;
-      const bool store = r < rows_valid && grow >= 0 && grow < p.total_q;
-      typename E::T *orow = static_cast<typename E::T *>(p.out) + grow * p.out_row_stride + h * 128;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        if (have_o) {
-          tmem_ld32(tbase + lane_addr + 256 + c * 32, v);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0u;
-        }
-        if (store) {
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 w;
-            const float *f = reinterpret_cast<const float *>(v) + q4 * 8;
-            w.x = E::pack2(f[0] * inv_l, f[1] * inv_l);
-            w.y = E::pack2(f[2] * inv_l, f[3] * inv_l);
-            w.z = E::pack2(f[4] * inv_l, f[5] * inv_l);
-            w.w = E::pack2(f[6] * inv_l, f[7] * inv_l);
-            *reinterpret_cast<uint4 *>(orow + c * 32 + q4 * 8) = w;
-          }
-        }
-      }
-    }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
@@ -449,22 +620,27 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
   p.scale_log2 = a.scale_log2;
   p.causal = a.causal;
   p.err = a.d_error;
-  // Query tiles: sum_b ceil(q_b / 128) is at most both bounds below.
-  const int64_t max_tiles = (static_cast<int64_t>(a.max_seqlen_q) + 127) / 128;
-  int64_t slots = (static_cast<int64_t>(a.total_q) + 127LL * a.num_seqs) / 128;
-  if (slots > a.num_seqs * max_tiles) slots = a.num_seqs * max_tiles;
+  // Pairs of query tiles: sum_b ceil(q_b / 256) is at most both bounds below;
+  // items are (pair, head).  One persistent CTA per SM walks them.
+  const int64_t max_pairs = (static_cast<int64_t>(a.max_seqlen_q) + 255) / 256;
+  int64_t slots = (static_cast<int64_t>(a.total_q) + 255LL * a.num_seqs) / 256;
+  if (slots > a.num_seqs * max_pairs) slots = a.num_seqs * max_pairs;
   if (slots <= 0) return cudaSuccess;
-  if (slots > 0x7fffffff) return cudaErrorInvalidValue;
-  dim3 grid(static_cast<unsigned>(slots), a.num_q_heads);
+  const int64_t items = slots * a.num_q_heads;
+  if (items > 0x7fffffff) return cudaErrorInvalidValue;
+  p.num_items = static_cast<int32_t>(items);
+  const int64_t grid = items < a.num_sms ? items : a.num_sms;
   cudaError_t e;
   if (a.dtype == PA_BF16) {
     e = allow_dynamic_smem<prefill_kernel<BF16>>();
     if (e != cudaSuccess) return e;
-    prefill_kernel<BF16><<<grid, kThreads, kSmemBytes, stream>>>(p, a.tm_q, a.tm_k, a.tm_v);
+    prefill_kernel<BF16><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(
+        p, a.tm_q, a.tm_k, a.tm_v);
   } else {
     e = allow_dynamic_smem<prefill_kernel<F16>>();
     if (e != cudaSuccess) return e;
-    prefill_kernel<F16><<<grid, kThreads, kSmemBytes, stream>>>(p, a.tm_q, a.tm_k, a.tm_v);
+    prefill_kernel<F16><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(
+        p, a.tm_q, a.tm_k, a.tm_v);
   }
   return cudaGetLastError();
 }
