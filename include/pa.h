@@ -227,6 +227,47 @@ pa_status pa_prefill_varlen(void *out, int64_t out_row_stride,
                             float scale, int32_t causal, pa_dtype dtype,
                             int32_t *d_error, void *stream);
 
+/*
+ * pa_decode_static_ws -- pa_decode for callers that cannot allocate.
+ *
+ * The pages have no counterpart to this entry point; it is a convenience of
+ * this library.  pa_decode needs a caller-supplied device workspace whenever
+ * a sequence spans several split-KV partitions.  Some callers cannot provide
+ * one: code that must not call cudaMalloc (for example while recording work
+ * for later replay, or in a loop with a fixed memory budget), a plug-in
+ * whose host framework owns every device allocation, or a plain C caller
+ * without a device allocator.  This variant computes exactly what pa_decode
+ * computes (same arguments, minus workspace/workspace_bytes) with its
+ * workspace in a fixed array of PA_STATIC_WORKSPACE_BYTES inside the
+ * library's device image, so it allocates nothing.
+ *
+ *  - Every GPU that loads the library holds the array until the process
+ *    exits.
+ *  - The first call on each device (with that device current) looks up the
+ *    array's device address once; make that first call before any stream
+ *    capture.  A failed lookup returns PA_ERR_CUDA.
+ *  - partition_size == 0 uses pa_decode's automatic plan, lengthened (fewer
+ *    partitions) until its workspace fits the array; an explicit
+ *    partition_size whose workspace does not fit returns PA_ERR_WORKSPACE.
+ *  - All calls on a device share the array and leave their partial results
+ *    in it (nothing in it has to start at zero).  Calls that may overlap on
+ *    the GPU race on it: order them on one stream.
+ */
+#define PA_STATIC_WORKSPACE_BYTES (16u << 20) /* 16 MiB */
+
+pa_status pa_decode_static_ws(void *out, int64_t out_row_stride,
+                              const void *query, int64_t q_row_stride,
+                              const void *key_cache, const void *value_cache,
+                              const int32_t *block_table,
+                              int64_t block_table_stride,
+                              int32_t max_blocks_per_seq,
+                              const int32_t *context_lens, int32_t num_seqs,
+                              int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t block_size,
+                              int64_t num_blocks, float scale,
+                              int32_t max_context_len, int32_t partition_size,
+                              pa_dtype dtype, int32_t *d_error, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -65,9 +65,8 @@ enum {
   kPFull = kSFull + 2,
   kPVDone = kPFull + 2,
   kQEmpty = kPVDone + 2,
-  kEpiDone = kQEmpty + 1,
-  kItemGo = kEpiDone + 1,
-  kFin = kItemGo + 1,
+  kOFree = kQEmpty + 1,  // per query tile: the epilogue has read O
+  kFin = kOFree + 2,
   kNumBars = kFin + 1
 };
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -208,12 +207,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (blockIdx.x == 0) check_cu_seqlens(p, lane);
   }
   if (warp == 1 && lane == 0) {
-    // P-full collects one arrival per softmax warp of its tile, the
-    // epilogue barrier one per softmax warp of both tiles.
+    // P-full and O-free collect one arrival per softmax warp of their tile.
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t n = 1;
-      if (i == kPFull || i == kPFull + 1) n = 4;
-      if (i == kEpiDone) n = 8;
+      if (i == kPFull || i == kPFull + 1 || i == kOFree || i == kOFree + 1) n = 4;
       mbar_init(bar(i), n);
     }
     fence_barrier_init();
@@ -327,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t id_pv = idesc_f16(kBF, 128, 128, true);
     int kbase = 0;            // ring position of this item's first K/V tile
     int pcnt[2] = {0, 0};     // P tiles consumed per query tile (all items)
+    int prev_nkv[2] = {1, 1}; // the previous item's K/V tiles per query tile
     bool ok = true;
     int j = 0;
     for (int x = x0; ok && x < p.num_items; x += dx, ++j) {
@@ -353,23 +351,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                         (kt > 0 || k > 0) ? 1u : 0u);
           umma_commit(bar(kPVDone + t));
         };
-        // The previous item's epilogues have read O and S; tell the softmax
-        // warps this item may start.
-        if (j > 0) ok = mbar_wait_bounded(bar(kEpiDone), (j - 1) & 1);
-        if (ok) {
-          tc_fence_after();
-          mbar_arrive(bar(kItemGo));
-          ok = mbar_wait_bounded(bar(kQFull), j & 1);
-        }
-        if (ok && it.nkv > 0) {
-          ok = mbar_wait_bounded(bar(kKVFull + k_slot(kbase)), k_par(kbase));
-          if (ok) {
-            tc_fence_after();
-            if (it.nkv_t[0] > 0) qk(0, 0);
-            if (it.nkv_t[1] > 0) qk(1, 0);
-            umma_commit(bar(kKVEmpty + k_slot(kbase)));
+        // S of both tiles is free (their last P was consumed before the
+        // previous item's last PV), so this item's first QKs go at once; a
+        // tile's first PV waits for that tile's previous epilogue (o_free).
+        // A tile with no work this item gets an empty S commit after its
+        // o_free wait, which keeps its softmax warps in step.
+        bool owait[2] = {j == 0, j == 0};  // o_free of the previous item seen
+        // After an item in which a tile had no work, wait for its (instant)
+        // epilogue before committing that tile's next S, so its softmax
+        // warps have taken the empty commit first (never two phases behind).
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!owait[t] && prev_nkv[t] == 0) {
+            if (ok) ok = mbar_wait_bounded(bar(kOFree + t), (j - 1) & 1);
+            owait[t] = true;
           }
         }
+        if (ok) ok = mbar_wait_bounded(bar(kQFull), j & 1);
+        if (ok && it.nkv > 0) {
+          ok = mbar_wait_bounded(bar(kKVFull + k_slot(kbase)), k_par(kbase));
+          if (ok) tc_fence_after();
+        }
+#pragma unroll
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (it.nkv_t[t] > 0) {
+            qk(t, 0);
+          } else {
+            if (!owait[t]) ok = mbar_wait_bounded(bar(kOFree + t), (j - 1) & 1);
+            owait[t] = true;
+            umma_commit(bar(kSFull + t));
+          }
+        }
+        if (ok && it.nkv > 0) umma_commit(bar(kKVEmpty + k_slot(kbase)));
         if (ok && it.nkv <= 1) umma_commit(bar(kQEmpty));  // no further QK reads Q
         for (int kt = 0; ok && kt < it.nkv; ++kt) {
           const bool more = kt + 1 < it.nkv;
@@ -379,6 +392,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (kt < it.nkv_t[t]) {
+              if (!owait[t]) {
+                ok = mbar_wait_bounded(bar(kOFree + t), (j - 1) & 1);
+                owait[t] = true;
+                if (!ok) break;
+                tc_fence_after();
+              }
               if (!have_v) {
                 ok = mbar_wait_bounded(bar(kKVFull + v_slot(kbase + kt)), v_par(kbase + kt));
                 have_v = true;
@@ -408,6 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       kbase += it.nkv;
+      prev_nkv[0] = it.nkv_t[0];
+      prev_nkv[1] = it.nkv_t[1];
     }
     if (lane == 0) {
       if (!ok) {
@@ -428,18 +449,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_tm = tbase + lane_addr + 256 + t * 128;
     const float sl = p.scale_log2;
     int kbase = 0;   // ring position of the item's first V tile
-    int n = 0;       // S tiles of this query tile processed in all items
+    int n = 0;       // S phases of this query tile (QK results and empty commits)
+    int pn = 0;      // PVs of this query tile
     bool ok = true;
     int j = 0;
     for (int x = x0; ok && x < p.num_items; x += dx, ++j) {
       const PairItem it = item_at(p, x, lane, false);
       if (it.seq < 0) break;
-      ok = mbar_wait_bounded(bar(kItemGo), j & 1);
-      if (!ok) break;
       const int my_nkv = it.nkv_t[t];
+      if (my_nkv == 0) {  // the MMA thread's empty S commit for this tile
+        ok = mbar_wait_bounded(bar(kSFull + t), n & 1);
+        ++n;
+        if (!ok) break;
+      }
       const int lim = min(it.lim_base + it.row0[t] + r, it.L - 1);  // last visible key
       float m_ref = -INFINITY, l = 0.f;
-      for (int kt = 0; kt < my_nkv; ++kt, ++n) {
+      for (int kt = 0; kt < my_nkv; ++kt, ++n, ++pn) {
         ok = mbar_wait_bounded(bar(kSFull + t), n & 1);
         if (!ok) break;
         tc_fence_after();
@@ -471,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kt >= 1) {
           // P(kt-1) has been consumed and O holds the sum through kt-1 (PV(kt-1)
           // was issued before S(kt), so this wait is normally already over).
-          ok = mbar_wait_bounded(bar(kPVDone + t), (n - 1) & 1);
+          ok = mbar_wait_bounded(bar(kPVDone + t), (pn - 1) & 1);
           if (!ok) break;
           tc_fence_after();
         }
@@ -547,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // ---------------------------------------------------- epilogue --
       if (ok && it.row0[t] < it.q_len) {
-        const bool have_o = my_nkv > 0 && mbar_wait_bounded(bar(kPVDone + t), (n - 1) & 1);
+        const bool have_o = my_nkv > 0 && mbar_wait_bounded(bar(kPVDone + t), (pn - 1) & 1);
         ok = my_nkv == 0 || have_o;
         if (my_nkv > 0) tc_fence_after();
         const float inv_l = (have_o && l > 0.f) ? 1.f / l : 0.f;
@@ -582,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       kbase += it.nkv;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kEpiDone));  // O and S of this item are free
+      if (lane == 0) mbar_arrive(bar(kOFree + t));  // O of this tile is free
     }
     if (!ok) {
       raise_error(p.err, PA_DEVERR_TIMEOUT);
