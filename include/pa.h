@@ -211,6 +211,10 @@ pa_status pa_decode(void *out, int64_t out_row_stride, const void *query,
  * PA_DEVERR_CU_SEQLENS and the offending sequences are skipped.
  * Supported: head_dim 128; num_q_heads % num_kv_heads == 0; block_size 16,
  * 32, 64 or 128.
+ * Work is handed out to the CTAs through one of 256 counters kept in the
+ * library's device memory, taken round robin per call; it needs no
+ * workspace.  Calls may overlap on the GPU (different streams) as long as
+ * fewer than 256 of them are in flight at once.
  */
 pa_status pa_prefill_varlen(void *out, int64_t out_row_stride,
                             const void *query, int64_t q_row_stride,

@@ -10,9 +10,14 @@
 //
 // Design (the pages build a per-sequence mask from cu_seqlens on Ascend;
 // here nothing is masked outside the diagonal tiles and nothing is padded):
-//  * CTA = (two consecutive 128-row query tiles A and B of one sequence,
-//    query head).  Both tiles share every K/V tile the CTA loads, halving the
-//    K/V traffic per flop.  Pairs are dealt heaviest first.
+//  * Work item = (two consecutive 128-row query tiles A and B of one
+//    sequence, query head).  Both tiles share every K/V tile loaded, halving
+//    the K/V traffic per flop.  One persistent CTA per SM claims items one
+//    at a time from a global counter, in an order that keeps one or two
+//    sequences in flight across the GPU (so each sequence's K/V comes from
+//    HBM once and is then reused from L2) and runs the heaviest items of a
+//    sequence first (so the last items claimed, which set the finish time,
+//    are light).
 //  * Warp 8 (TMA): loads Q_A and Q_B once, then streams K and V tiles (128
 //    tokens each) through separate K (2 buffers) and V (3 buffers) rings,
 //    K running one tile ahead of V; a K/V
@@ -35,6 +40,8 @@
 //    rounding.
 //  * Epilogue: O / l from TMEM to registers to global memory.
 #include <math.h>
+
+#include <atomic>
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
@@ -67,9 +74,13 @@ enum {
   kQEmpty = kPVDone + 2,
   kOFree = kQEmpty + 1,  // per query tile: the epilogue has read O
   kFin = kOFree + 2,
-  kNumBars = kFin + 1
+  kItemFull = kFin + 1,               // item ring: index published by the TMA warp
+  kItemEmpty = kItemFull + 4,         // ... and taken by the MMA and softmax warps
+  kNumBars = kItemEmpty + 4
 };
-constexpr int kMiscOff = kBarOff + kNumBars * 8;
+constexpr int kItemRing = 4;
+constexpr int kItemTakers = 9;        // 8 softmax warps + the MMA warp
+constexpr int kMiscOff = kBarOff + kNumBars * 8;  // ints: [2] TMEM base, [3] abort, [8..11] items
 constexpr int kSmemBytes = 1024 + kMiscOff + 64;
 constexpr uint32_t kTmemCols = 512;         // S_A | S_B | O_A | O_B (P_t overlays S_t)
 constexpr float kRescaleThreshold = 8.0f;   // log2 of the largest P allowed
@@ -95,36 +106,61 @@ struct PrefillParams {
   float scale_log2;
   int32_t causal;
   int32_t num_items;
+  int32_t sched_slot;
   int32_t *err;
 };
 
-// Which (sequence, 256-row pair of query tiles) this CTA serves: slot x of
-// the list ordered by pair index descending (the later pairs of a causal
-// sequence need the most K/V tiles), sequences in order within one index.
-__device__ void find_pair(const PrefillParams &p, int x, int lane, int *seq_out, int *pair_out) {
-  const int max_pairs = (p.max_seqlen_q + 255) / 256;
-  int rem = x;
-  for (int i = max_pairs - 1; i >= 0; --i) {
-    for (int c0 = 0; c0 < p.num_seqs; c0 += 32) {
-      const int s = c0 + lane;
-      bool has = false;
-      if (s < p.num_seqs) {
-        const int q = __ldg(p.cu + s + 1) - __ldg(p.cu + s);
-        has = q >= 0 && q <= p.max_seqlen_q && (q + 255) / 256 > i;
-      }
-      unsigned bal = __ballot_sync(0xffffffffu, has);
-      const int n = __popc(bal);
-      if (rem < n) {
-        for (int k = 0; k < rem; ++k) bal &= bal - 1;
-        *seq_out = c0 + __ffs(bal) - 1;
-        *pair_out = i;
-        return;
-      }
-      rem -= n;
+// Work counters for the dynamic item schedule.  A launch uses one slot
+// (chosen on the host, round robin): `next` hands out item indices, `done`
+// counts CTAs that have finished, and the last CTA to finish puts both back
+// to zero, so the slot is ready for the next launch that is ordered after
+// this one.  Launches that may run at the same time must use different
+// slots; with round-robin choice that fails only when more than kSchedSlots
+// prefill launches are in flight at once.
+struct __align__(128) SchedSlot {
+  unsigned next, done;
+};
+constexpr int kSchedSlots = 256;
+__device__ SchedSlot g_prefill_sched[kSchedSlots];
+
+// Item x of the work list: items are ordered by sequence, then pair of query
+// tiles (latest, i.e. heaviest, pair first), then query head.  The items of
+// one sequence are neighbours, so they run at about the same time and share
+// that sequence's K/V tiles in L2; heads of one KV group are neighbours too.
+// Warp-collective.
+__device__ void find_item(const PrefillParams &p, int x, int lane, int *seq_out, int *pair_out,
+                          int *head_out) {
+  int base = 0;  // items of the sequences before this chunk
+  for (int c0 = 0; c0 < p.num_seqs; c0 += 32) {
+    const int s = c0 + lane;
+    int cnt = 0;
+    if (s < p.num_seqs) {
+      const int q = __ldg(p.cu + s + 1) - __ldg(p.cu + s);
+      if (q > 0 && q <= p.max_seqlen_q) cnt = ((q + 255) / 256) * p.hq;
     }
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, x < base + incl && x >= base + incl - cnt);
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      const int cs = __shfl_sync(0xffffffffu, cnt, src);
+      const int first = base + __shfl_sync(0xffffffffu, incl, src) - cs;
+      const int npairs = cs / p.hq;
+      const int rem = x - first;
+      *seq_out = c0 + src;
+      *pair_out = npairs - 1 - rem / p.hq;
+      *head_out = rem % p.hq;
+      return;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
   }
   *seq_out = -1;
   *pair_out = -1;
+  *head_out = 0;
 }
 
 // cu_seqlens must start at 0, never decrease, end at total_q, and no
@@ -154,14 +190,13 @@ struct PairItem {
   bool has_b;
 };
 
-// Item x of the static list (slot x / Hq in find_pair's order, head x % Hq).
-// Warp-collective.
+// Item x of the work list (see find_item).  Warp-collective.
 __device__ PairItem item_at(const PrefillParams &p, int x, int lane, bool report) {
   PairItem it;
-  int seq, pair;
-  find_pair(p, x / p.hq, lane, &seq, &pair);
+  int seq, pair, head;
+  find_item(p, x, lane, &seq, &pair, &head);
   it.seq = seq;
-  it.h = x % p.hq;
+  it.h = head;
   it.q_start = it.q_len = it.L = it.lim_base = 0;
   it.row0[0] = it.row0[1] = 0;
   it.nkv_t[0] = it.nkv_t[1] = 0;
@@ -200,7 +235,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int x0 = blockIdx.x, dx = gridDim.x;  // this CTA's items: x0, x0+dx, ...
+  SchedSlot *sched = &g_prefill_sched[p.sched_slot];
+  // Item j of this CTA: index published by the TMA warp in ring entry j % 4;
+  // every other warp takes it from there (lane 0 waits, the warp shares it).
+  // Returns false when a wait gave up; *x < 0 ends the list.
+  auto take_item = [&](int j, int *x) {
+    bool ok = true;
+    int v = -1;
+    if (lane == 0) {
+      ok = mbar_wait_bounded(bar(kItemFull + j % kItemRing), (j / kItemRing) & 1);
+      if (ok) v = misc[8 + j % kItemRing];
+      mbar_arrive(bar(kItemEmpty + j % kItemRing));
+    }
+    *x = __shfl_sync(0xffffffffu, v, 0);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  };
 
   if (warp == 0) {
     if (lane == 0) misc[3] = 0;  // abort: some wait gave up
@@ -211,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t n = 1;
       if (i == kPFull || i == kPFull + 1 || i == kOFree || i == kOFree + 1) n = 4;
+      if (i >= kItemEmpty && i < kItemEmpty + kItemRing) n = kItemTakers;
       mbar_init(bar(i), n);
     }
     fence_barrier_init();
@@ -236,10 +286,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     int kbase = 0;              // K/V tiles of earlier items (ring positions)
     bool ok = true;
     int nk = 0, nv = 0;         // K and V tiles issued in all
+    int nq = 0;                 // items whose Q loads were issued
     int j = 0;
-    for (int x = x0; ok && x < p.num_items; x += dx, ++j) {
-      const PairItem it = item_at(p, x, lane, true);
-      if (it.seq < 0) break;
+    int x = blockIdx.x;         // the first item is fixed, the rest are claimed
+    for (;; ++j) {
+      PairItem it;
+      it.seq = -1;
+      if (x < p.num_items) it = item_at(p, x, lane, true);
+      // Publish the item (or the end of the list) to the other warps.
+      if (lane == 0) {
+        if (j >= kItemRing)
+          ok = mbar_wait_bounded(bar(kItemEmpty + j % kItemRing), ((j / kItemRing) - 1) & 1);
+        misc[8 + j % kItemRing] = it.seq >= 0 && ok ? x : -1;
+        mbar_arrive(bar(kItemFull + j % kItemRing));
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok || it.seq < 0) break;
+      // Claim the next item now; the answer is first needed next iteration.
+      int x_next = 0;
+      if (lane == 0) x_next = static_cast<int>(atomicAdd(&sched->next, 1u)) + gridDim.x;
       const int g = it.h / p.group;
       // Q of item j once the previous item's last QK has read Q.
       if (lane == 0 && j > 0) ok = mbar_wait_bounded(bar(kQEmpty), (j - 1) & 1);
@@ -258,6 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       it.q_start + it.row0[t]);
         }
       }
+      ++nq;
       const int32_t *bt = p.block_table + static_cast<int64_t>(it.seq) * p.bt_stride;
       auto load_id = [&](int kt) {
         return (lane < nbox && kt < it.nkv && kt * 128 + lane * bs < it.L)
@@ -305,12 +371,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         id_k = id_nxt;
       }
       kbase += it.nkv;
+      x = __shfl_sync(0xffffffffu, x_next, 0);
+      if (!ok) break;
     }
     if (!ok && lane == 0) {
       if (!misc[3]) raise_error(p.err, PA_DEVERR_TIMEOUT);
       misc[3] = 1;
       // Do not leave while copies this CTA issued may still land.
-      mbar_wait_bounded(bar(kQFull), (j - 1) & 1);
+      if (nq > 0) mbar_wait_bounded(bar(kQFull), (nq - 1) & 1);
       for (int n = nk - 1; n >= 0 && n >= nk - kKBufs; --n)
         mbar_wait_bounded(bar(kKVFull + k_slot(n)), k_par(n));
       for (int n = nv - 1; n >= 0 && n >= nv - kVBufs; --n)
@@ -326,10 +394,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int pcnt[2] = {0, 0};     // P tiles consumed per query tile (all items)
     int prev_nkv[2] = {1, 1}; // the previous item's K/V tiles per query tile
     bool ok = true;
-    int j = 0;
-    for (int x = x0; ok && x < p.num_items; x += dx, ++j) {
+    for (int j = 0;; ++j) {
+      int x;
+      ok = take_item(j, &x);
+      if (!ok || x < 0) break;
       const PairItem it = item_at(p, x, lane, false);
-      if (it.seq < 0) break;
       if (lane == 0) {
         auto qk = [&](int t, int kt) {  // S_t = Q_t K_kt^T
           const uint32_t qs = smem_u32(smem + kQOff + t * kTile);
@@ -429,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       kbase += it.nkv;
       prev_nkv[0] = it.nkv_t[0];
       prev_nkv[1] = it.nkv_t[1];
+      if (!ok) break;
     }
     if (lane == 0) {
       if (!ok) {
@@ -452,10 +522,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int n = 0;       // S phases of this query tile (QK results and empty commits)
     int pn = 0;      // PVs of this query tile
     bool ok = true;
-    int j = 0;
-    for (int x = x0; ok && x < p.num_items; x += dx, ++j) {
+    for (int j = 0;; ++j) {
+      int x;
+      ok = take_item(j, &x);
+      if (!ok || x < 0) break;
       const PairItem it = item_at(p, x, lane, false);
-      if (it.seq < 0) break;
       const int my_nkv = it.nkv_t[t];
       if (my_nkv == 0) {  // the MMA thread's empty S commit for this tile
         ok = mbar_wait_bounded(bar(kSFull + t), n & 1);
@@ -608,6 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kOFree + t));  // O of this tile is free
+      if (!ok) break;
     }
     if (!ok) {
       raise_error(p.err, PA_DEVERR_TIMEOUT);
@@ -621,9 +693,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
+  // Every claim of this CTA precedes its `done` count; the last CTA to
+  // finish returns the slot to zero for the next launch.
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(&sched->done, 1u) == gridDim.x - 1) {
+      __threadfence();
+      atomicExch(&sched->next, 0u);
+      atomicExch(&sched->done, 0u);
+    }
+  }
 }
 
 }  // namespace
+
+// Launches so far in this process; picks each launch's schedule slot.
+std::atomic<uint32_t> g_prefill_launches{0};
 
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
   PrefillParams p;
@@ -654,6 +739,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
   const int64_t items = slots * a.num_q_heads;
   if (items > 0x7fffffff) return cudaErrorInvalidValue;
   p.num_items = static_cast<int32_t>(items);
+  p.sched_slot = static_cast<int32_t>(g_prefill_launches.fetch_add(1) % kSchedSlots);
   const int64_t grid = items < a.num_sms ? items : a.num_sms;
   cudaError_t e;
   if (a.dtype == PA_BF16) {
