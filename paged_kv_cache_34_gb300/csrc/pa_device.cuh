@@ -28,6 +28,14 @@ struct F16 {
   }
   // Sum of the two values packed in `w` (as the tensor core will see them).
   static __device__ __forceinline__ float sum2(uint32_t w) { return lo(w) + hi(w); }
+  // a += low half of w, b += high half, each widened exactly (mixed-precision
+  // add.f32.f16: no separate unpacking instructions).
+  static __device__ __forceinline__ void add_halves(uint32_t w, float &a, float &b) {
+    asm("{\n\t.reg .b16 l16, h16;\n\tmov.b32 {l16, h16}, %2;\n\t"
+        "add.rn.f32.f16 %0, l16, %0;\n\tadd.rn.f32.f16 %1, h16, %1;\n\t}"
+        : "+f"(a), "+f"(b)
+        : "r"(w));
+  }
   static __device__ __forceinline__ float lo(uint32_t w) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
   }
@@ -46,6 +54,12 @@ struct BF16 {
   }
   // Sum of the two values packed in `w` (as the tensor core will see them).
   static __device__ __forceinline__ float sum2(uint32_t w) { return lo(w) + hi(w); }
+  static __device__ __forceinline__ void add_halves(uint32_t w, float &a, float &b) {
+    asm("{\n\t.reg .b16 l16, h16;\n\tmov.b32 {l16, h16}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l16, %0;\n\tadd.rn.f32.bf16 %1, h16, %1;\n\t}"
+        : "+f"(a), "+f"(b)
+        : "r"(w));
+  }
   static __device__ __forceinline__ float lo(uint32_t w) { return __uint_as_float(w << 16); }
   static __device__ __forceinline__ float hi(uint32_t w) {
     return __uint_as_float(w & 0xffff0000u);
@@ -164,6 +178,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// max(a, b, c) in one instruction (three-input max.f32 of sm_100-family).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 // ---------------------------------------------------------------------------

@@ -22,6 +22,22 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
                : "memory");
 }
 
+// ---- per-warpgroup register budget (warpgroup-collective) ---------------
+// setmaxnreg moves registers between the warpgroups of a CTA: .dec returns
+// registers to the CTA's pool, .inc waits until the pool can supply them.
+// The pool is what the CTA was launched with, so the final budgets must add
+// up to at most (threads x registers per thread at launch).
+template <uint32_t N>
+__device__ __forceinline__ void reg_alloc() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg range");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void reg_dealloc() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg range");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---- ordering of tcgen05 operations around thread synchronisation -------
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -48,6 +64,19 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N, bool b
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
          ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// ---- issuing thread -------------------------------------------------------
+// true in exactly one lane of a converged warp.  MMA-issuing code runs
+// warp-uniformly (descriptors and loop state in uniform registers) and only
+// the issue itself goes to the elected lane: a lone lane's divergent code
+// issues MMAs at about half the tensor core's rate while the SM is busy.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
 }
 
 // ---- MMA issue / commit (single thread) ----------------------------------

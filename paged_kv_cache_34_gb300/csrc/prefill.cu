@@ -51,8 +51,23 @@ namespace pa {
 
 namespace {
 
-constexpr int kThreads = 320;       // warps 0-3 softmax A, 4-7 softmax B, 8 TMA, 9 MMA
-constexpr int kTmaWarp = 8, kMmaWarp = 9;
+// Warpgroups: 0 softmax of tile A, 1 softmax of tile B, 2 epilogue of both
+// tiles, 3 producers: warp 12 TMA, 13 MMA, 14-15 idle (setmaxnreg works on
+// whole warpgroups).
+constexpr int kThreads = 512;
+constexpr int kEpiWarp0 = 8, kTmaWarp = 12, kMmaWarp = 13;
+// Registers per thread after the split (setmaxnreg, per warpgroup): the
+// softmax holds a whole S row per thread, the epilogue a packed O row, the
+// producers little.  The split must fit in what the CTA is launched with
+// (checked on the host before the first launch).
+#ifndef PA_SOFTMAX_REGS
+#define PA_SOFTMAX_REGS 152
+#define PA_EPILOGUE_REGS 104
+#define PA_PRODUCER_REGS 104
+#endif
+constexpr int kSoftmaxRegs = PA_SOFTMAX_REGS, kEpilogueRegs = PA_EPILOGUE_REGS,
+              kProducerRegs = PA_PRODUCER_REGS;
+constexpr int kRegPoolNeeded = 128 * (2 * kSoftmaxRegs + kEpilogueRegs + kProducerRegs);
 constexpr int kHalf = 128 * 128;    // 128 rows x 64 elements x 2 B
 constexpr int kTile = 2 * kHalf;    // 128 x 128 tile, two 64-wide halves
 #ifndef PA_PREFILL_K_BUFS
@@ -72,25 +87,24 @@ enum {
   kPFull = kSFull + 2,
   kPVDone = kPFull + 2,
   kQEmpty = kPVDone + 2,
-  kOFree = kQEmpty + 1,  // per query tile: the epilogue has read O
-  kFin = kOFree + 2,
-  kItemFull = kFin + 1,               // item ring: index published by the TMA warp
-  kItemEmpty = kItemFull + 4,         // ... and taken by the MMA and softmax warps
+  kOFull = kQEmpty + 1,     // per query tile and item: its last PV is done
+  kOFree = kOFull + 2,      // per query tile: the epilogue has read O
+  kLFull = kOFree + 2,      // per query tile: the softmax has left its row sums
+  kVFixed = kLFull + 2,     // the TMA warp has cleared a V tile's tail rows
+  kVFixFree = kVFixed + 1,  // ... and the MMA thread has seen it
+  kFin = kVFixFree + 1,
+  kItemFull = kFin + 1,     // item ring: index published by the TMA warp
+  kItemEmpty = kItemFull + 4,  // ... and taken by every other role
   kNumBars = kItemEmpty + 4
 };
 constexpr int kItemRing = 4;
-constexpr int kItemTakers = 9;        // 8 softmax warps + the MMA warp
-constexpr int kMiscOff = kBarOff + kNumBars * 8;  // ints: [2] TMEM base, [3] abort, [8..11] items
+constexpr int kItemTakers = 13;  // 8 softmax warps, 4 epilogue warps, MMA
+constexpr int kLOff = kBarOff + kNumBars * 8;   // float l[2][128]: row sums per tile
+constexpr int kMiscOff = kLOff + 2 * 128 * 4;   // ints: [2] TMEM base, [3] abort, [8..11] items
 constexpr int kSmemBytes = 1024 + kMiscOff + 64;
 constexpr uint32_t kTmemCols = 512;         // S_A | S_B | O_A | O_B (P_t overlays S_t)
 constexpr float kRescaleThreshold = 8.0f;   // log2 of the largest P allowed
-// Pairs of exponentials whose index i has (i & kPolyMask) == kPolyMask run on
-// the FMA pipe instead of the SFU (1 = every other pair, 3 = one in four,
-// -1 = none).  Measured on GB300 the SFU is not the limit here, so none.
-#ifndef PA_PREFILL_POLY_MASK
-#define PA_PREFILL_POLY_MASK -1
-#endif
-constexpr int kPolyMask = PA_PREFILL_POLY_MASK;
+
 
 struct PrefillParams {
   void *out;
@@ -231,13 +245,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kBarOff);
+  float *l_buf = reinterpret_cast<float *>(smem + kLOff);
   volatile int *misc = reinterpret_cast<volatile int *>(smem + kMiscOff);
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   SchedSlot *sched = &g_prefill_sched[p.sched_slot];
   // Item j of this CTA: index published by the TMA warp in ring entry j % 4;
-  // every other warp takes it from there (lane 0 waits, the warp shares it).
+  // every other role takes it from there (lane 0 waits, the warp shares it).
   // Returns false when a wait gave up; *x < 0 ends the list.
   auto take_item = [&](int j, int *x) {
     bool ok = true;
@@ -250,16 +265,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     *x = __shfl_sync(0xffffffffu, v, 0);
     return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
   };
+  // Lane 0 waits, the warp learns the outcome.
+  auto warp_wait = [&](uint32_t b, uint32_t parity) {
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait_bounded(b, parity);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  };
 
   if (warp == 0) {
     if (lane == 0) misc[3] = 0;  // abort: some wait gave up
     if (blockIdx.x == 0) check_cu_seqlens(p, lane);
   }
   if (warp == 1 && lane == 0) {
-    // P-full and O-free collect one arrival per softmax warp of their tile.
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t n = 1;
+      // one arrival per softmax warp (P) or epilogue warp (O free) of a tile;
+      // the row sums are left by every softmax thread
       if (i == kPFull || i == kPFull + 1 || i == kOFree || i == kOFree + 1) n = 4;
+      if (i == kLFull || i == kLFull + 1) n = 128;
       if (i >= kItemEmpty && i < kItemEmpty + kItemRing) n = kItemTakers;
       mbar_init(bar(i), n);
     }
@@ -274,185 +297,234 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = static_cast<uint32_t>(misc[2]);
 
-  if (warp == kTmaWarp) {
-    // ----------------------------------------------------------- TMA --
-    if (lane == 0) {
-      tma_prefetch_desc(&tmq);
-      tma_prefetch_desc(&tmk);
-      tma_prefetch_desc(&tmv);
-    }
-    const int bs = p.block_size;
-    const int nbox = 128 / bs;  // one box per block, lane k loads block k of a tile
-    int kbase = 0;              // K/V tiles of earlier items (ring positions)
-    bool ok = true;
-    int nk = 0, nv = 0;         // K and V tiles issued in all
-    int nq = 0;                 // items whose Q loads were issued
-    int j = 0;
-    int x = blockIdx.x;         // the first item is fixed, the rest are claimed
-    for (;; ++j) {
-      PairItem it;
-      it.seq = -1;
-      if (x < p.num_items) it = item_at(p, x, lane, true);
-      // Publish the item (or the end of the list) to the other warps.
+  if (warp >= kTmaWarp) {
+    reg_dealloc<kProducerRegs>();
+    if (warp == kTmaWarp) {
+      // ----------------------------------------------------------- TMA --
       if (lane == 0) {
-        if (j >= kItemRing)
-          ok = mbar_wait_bounded(bar(kItemEmpty + j % kItemRing), ((j / kItemRing) - 1) & 1);
-        misc[8 + j % kItemRing] = it.seq >= 0 && ok ? x : -1;
-        mbar_arrive(bar(kItemFull + j % kItemRing));
+        tma_prefetch_desc(&tmq);
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
       }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok || it.seq < 0) break;
-      // Claim the next item now; the answer is first needed next iteration.
-      int x_next = 0;
-      if (lane == 0) x_next = static_cast<int>(atomicAdd(&sched->next, 1u)) + gridDim.x;
-      const int g = it.h / p.group;
-      // Q of item j once the previous item's last QK has read Q.
-      if (lane == 0 && j > 0) ok = mbar_wait_bounded(bar(kQEmpty), (j - 1) & 1);
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok || misc[3]) {
-        ok = false;
-        break;
-      }
-      if (lane == 0) {
-        const uint32_t qs = smem_u32(smem + kQOff);
-        const int qtiles = it.nkv > 0 ? (it.has_b ? 2 : 1) : 0;
-        mbar_arrive_expect_tx(bar(kQFull), qtiles * kTile);
-        for (int t = 0; t < qtiles; ++t) {
-          tma_load_3d(qs + t * kTile, &tmq, bar(kQFull), 0, it.h, it.q_start + it.row0[t]);
-          tma_load_3d(qs + t * kTile + kHalf, &tmq, bar(kQFull), 64, it.h,
-                      it.q_start + it.row0[t]);
+      const int bs = p.block_size;
+      const int nbox = 128 / bs;  // one box per block, lane k loads block k of a tile
+      int kbase = 0;              // K/V tiles of earlier items (ring positions)
+      bool ok = true;
+      int nk = 0, nv = 0;         // K and V tiles issued in all
+      int nq = 0;                 // items whose Q loads were issued
+      int nfix = 0;               // V tiles whose tail rows were cleared
+      int j = 0;
+      int x = blockIdx.x;         // the first item is fixed, the rest are claimed
+      for (;; ++j) {
+        PairItem it;
+        it.seq = -1;
+        if (x < p.num_items) it = item_at(p, x, lane, true);
+        // Publish the item (or the end of the list) to the other roles.
+        if (lane == 0) {
+          if (j >= kItemRing)
+            ok = mbar_wait_bounded(bar(kItemEmpty + j % kItemRing), ((j / kItemRing) - 1) & 1);
+          misc[8 + j % kItemRing] = it.seq >= 0 && ok ? x : -1;
+          mbar_arrive(bar(kItemFull + j % kItemRing));
         }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok || it.seq < 0) break;
+        // Claim the next item now; the answer is first needed next iteration.
+        int x_next = 0;
+        if (lane == 0) x_next = static_cast<int>(atomicAdd(&sched->next, 1u)) + gridDim.x;
+        const int g = it.h / p.group;
+        // Q of item j once the previous item's last QK has read Q.
+        if (j > 0) ok = warp_wait(bar(kQEmpty), (j - 1) & 1);
+        if (!ok || misc[3]) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t qs = smem_u32(smem + kQOff);
+          const int qtiles = it.nkv > 0 ? (it.has_b ? 2 : 1) : 0;
+          mbar_arrive_expect_tx(bar(kQFull), qtiles * kTile);
+          for (int t = 0; t < qtiles; ++t) {
+            tma_load_3d(qs + t * kTile, &tmq, bar(kQFull), 0, it.h, it.q_start + it.row0[t]);
+            tma_load_3d(qs + t * kTile + kHalf, &tmq, bar(kQFull), 64, it.h,
+                        it.q_start + it.row0[t]);
+          }
+        }
+        ++nq;
+        const int32_t *bt = p.block_table + static_cast<int64_t>(it.seq) * p.bt_stride;
+        auto load_id = [&](int kt) {
+          return (lane < nbox && kt < it.nkv && kt * 128 + lane * bs < it.L)
+                     ? __ldg(bt + kt * nbox + lane)
+                     : -1;
+        };
+        // Issue order K0 K1 V0 K2 V1 ...: K runs one tile ahead of V, since S
+        // needs K a whole softmax earlier than O needs V.
+        int id_k = load_id(0), id_v = -1;
+        for (int jj = 0; jj <= it.nkv && ok; ++jj) {
+          const int id_nxt = load_id(jj + 1);  // in flight while this step issues
+#pragma unroll
+          for (int which = 0; which < 2; ++which) {
+            const int kt = which == 0 ? jj : jj - 1;  // K of tile jj, then V of tile jj-1
+            if (kt < 0 || kt >= it.nkv) continue;
+            const int id = which == 0 ? id_k : id_v;
+            const bool want = lane < nbox && kt * 128 + lane * bs < it.L;
+            const bool valid = want && id >= 0 && id < p.num_blocks;
+            if (which == 0 && want && !valid) raise_error(p.err, PA_DEVERR_BLOCK_ID);
+            const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+            const int n = kbase + kt;  // ring position
+            const int slot = which == 0 ? k_slot(n) : v_slot(n);
+            const int nuse = which == 0 ? n / kKBufs : n / kVBufs;  // earlier uses of slot
+            if (nuse > 0) ok = warp_wait(bar(kKVEmpty + slot), (nuse - 1) & 1);
+            if (!ok || misc[3]) {
+              ok = false;
+              break;
+            }
+            if (lane == 0)
+              mbar_arrive_expect_tx(bar(kKVFull + slot),
+                                    static_cast<uint32_t>(__popc(vmask)) * bs * 128 * 2);
+            __syncwarp();
+            if (valid) {
+              const uint32_t dst = smem_u32(smem + kKVOff + slot * kTile) + lane * bs * 128;
+              const CUtensorMap *map = which == 0 ? &tmk : &tmv;
+              tma_load_3d(dst, map, bar(kKVFull + slot), 0, g, id * bs);
+              tma_load_3d(dst + kHalf, map, bar(kKVFull + slot), 64, g, id * bs);
+            }
+            if (which == 0) ++nk;
+            else ++nv;
+          }
+          id_v = id_k;
+          id_k = id_nxt;
+        }
+        // Rows of the item's last V tile past the context end may hold
+        // anything (stale or never-written pool rows, even NaN); their
+        // weights are 0, but 0 * NaN is NaN: clear them once the tile has
+        // landed, before the PV that reads it.  The load was issued just
+        // above, so waiting for it here cannot catch an older phase.
+        if (ok && it.nkv > 0 && it.L < it.nkv * 128) {
+          const int vn = kbase + it.nkv - 1;
+          if (nfix > 0) ok = warp_wait(bar(kVFixFree), (nfix - 1) & 1);
+          // every lane waits: each then writes into the landed tile
+          if (ok) ok = mbar_wait_bounded(bar(kKVFull + v_slot(vn)), v_par(vn));
+          ok = __all_sync(0xffffffffu, ok);
+          if (ok) {
+            uint8_t *vt = smem + kKVOff + v_slot(vn) * kTile;
+            const int first = it.L - (it.nkv - 1) * 128;  // 1..127
+            for (int i = lane; i < (128 - first) * 16; i += 32) {
+              const int row = first + i / 16, c16 = i % 16;
+              *reinterpret_cast<uint4 *>(vt + (c16 >> 3) * kHalf + row * 128 + (c16 & 7) * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();  // generic writes before the tensor core reads
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kVFixed));
+            ++nfix;
+          }
+        }
+        kbase += it.nkv;
+        x = __shfl_sync(0xffffffffu, x_next, 0);
+        if (!ok) break;
       }
-      ++nq;
-      const int32_t *bt = p.block_table + static_cast<int64_t>(it.seq) * p.bt_stride;
-      auto load_id = [&](int kt) {
-        return (lane < nbox && kt < it.nkv && kt * 128 + lane * bs < it.L)
-                   ? __ldg(bt + kt * nbox + lane)
-                   : -1;
+      if (!ok && lane == 0) {
+        if (!misc[3]) raise_error(p.err, PA_DEVERR_TIMEOUT);
+        misc[3] = 1;
+        // Do not leave while copies this CTA issued may still land.
+        if (nq > 0) mbar_wait_bounded(bar(kQFull), (nq - 1) & 1);
+        for (int n = nk - 1; n >= 0 && n >= nk - kKBufs; --n)
+          mbar_wait_bounded(bar(kKVFull + k_slot(n)), k_par(n));
+        for (int n = nv - 1; n >= 0 && n >= nv - kVBufs; --n)
+          mbar_wait_bounded(bar(kKVFull + v_slot(n)), v_par(n));
+      }
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      // ----------------------------------------------------------- MMA --
+      // The whole warp runs this loop; only the MMAs and commits are issued
+      // by one elected lane (the same one every time: the warp is converged).
+      constexpr bool kBF = E::kBF16;
+      const uint32_t id_qk = idesc_f16(kBF, 128, 128, false);
+      const uint32_t id_pv = idesc_f16(kBF, 128, 128, true);
+      const uint64_t q_desc[2] = {sdesc_sw128(smem_u32(smem + kQOff), 16, 1024),
+                                  sdesc_sw128(smem_u32(smem + kQOff + kTile), 16, 1024)};
+      int kbase = 0;            // ring position of this item's first K/V tile
+      int pcnt[2] = {0, 0};     // P tiles consumed per query tile (all items)
+      int prev_nkv[2] = {1, 1}; // the previous item's K/V tiles per query tile
+      int nfix = 0;             // V tiles whose tail rows the TMA warp cleared
+      bool ok = true;
+      auto commit = [&](int b) {
+        if (elect_one()) umma_commit(bar(b));
+        __syncwarp();
       };
-      // Issue order K0 K1 V0 K2 V1 ...: K runs one tile ahead of V, since S
-      // needs K a whole softmax earlier than O needs V.
-      int id_k = load_id(0), id_v = -1;
-      for (int jj = 0; jj <= it.nkv && ok; ++jj) {
-        const int id_nxt = load_id(jj + 1);  // in flight while this step issues
+      auto qk = [&](int t, int kt) {  // S_t = Q_t K_kt^T
+        const uint64_t qd = q_desc[t];
+        const uint64_t kd =
+            sdesc_sw128(smem_u32(smem + kKVOff + k_slot(kbase + kt) * kTile), 16, 1024);
+        if (elect_one()) {
+          // K step k: 16 columns = 32 bytes into a 128-byte swizzled row,
+          // the second 64 columns in the tile's second half
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          const int kt = which == 0 ? jj : jj - 1;  // K of tile jj, then V of tile jj-1
-          if (kt < 0 || kt >= it.nkv) continue;
-          const int id = which == 0 ? id_k : id_v;
-          const bool want = lane < nbox && kt * 128 + lane * bs < it.L;
-          const bool valid = want && id >= 0 && id < p.num_blocks;
-          if (which == 0 && want && !valid) raise_error(p.err, PA_DEVERR_BLOCK_ID);
-          const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-          const int n = kbase + kt;  // ring position
-          const int slot = which == 0 ? k_slot(n) : v_slot(n);
-          const int nuse = which == 0 ? n / kKBufs : n / kVBufs;  // earlier uses of slot
-          if (lane == 0 && nuse > 0)
-            ok = mbar_wait_bounded(bar(kKVEmpty + slot), (nuse - 1) & 1);
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-          if (!ok || misc[3]) {
-            ok = false;
-            break;
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t off = ((k >> 2) * kHalf + (k & 3) * 32) >> 4;
+            umma_f16_ss(tbase + t * 128, qd + off, kd + off, id_qk, k > 0 ? 1u : 0u);
           }
-          if (lane == 0)
-            mbar_arrive_expect_tx(bar(kKVFull + slot),
-                                  static_cast<uint32_t>(__popc(vmask)) * bs * 128 * 2);
-          __syncwarp();
-          if (valid) {
-            const uint32_t dst = smem_u32(smem + kKVOff + slot * kTile) + lane * bs * 128;
-            const CUtensorMap *map = which == 0 ? &tmk : &tmv;
-            tma_load_3d(dst, map, bar(kKVFull + slot), 0, g, id * bs);
-            tma_load_3d(dst + kHalf, map, bar(kKVFull + slot), 64, g, id * bs);
-          }
-          if (which == 0) ++nk;
-          else ++nv;
-        }
-        id_v = id_k;
-        id_k = id_nxt;
-      }
-      kbase += it.nkv;
-      x = __shfl_sync(0xffffffffu, x_next, 0);
-      if (!ok) break;
-    }
-    if (!ok && lane == 0) {
-      if (!misc[3]) raise_error(p.err, PA_DEVERR_TIMEOUT);
-      misc[3] = 1;
-      // Do not leave while copies this CTA issued may still land.
-      if (nq > 0) mbar_wait_bounded(bar(kQFull), (nq - 1) & 1);
-      for (int n = nk - 1; n >= 0 && n >= nk - kKBufs; --n)
-        mbar_wait_bounded(bar(kKVFull + k_slot(n)), k_par(n));
-      for (int n = nv - 1; n >= 0 && n >= nv - kVBufs; --n)
-        mbar_wait_bounded(bar(kKVFull + v_slot(n)), v_par(n));
-    }
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ----------------------------------------------------------- MMA --
-    constexpr bool kBF = E::kBF16;
-    const uint32_t id_qk = idesc_f16(kBF, 128, 128, false);
-    const uint32_t id_pv = idesc_f16(kBF, 128, 128, true);
-    int kbase = 0;            // ring position of this item's first K/V tile
-    int pcnt[2] = {0, 0};     // P tiles consumed per query tile (all items)
-    int prev_nkv[2] = {1, 1}; // the previous item's K/V tiles per query tile
-    bool ok = true;
-    for (int j = 0;; ++j) {
-      int x;
-      ok = take_item(j, &x);
-      if (!ok || x < 0) break;
-      const PairItem it = item_at(p, x, lane, false);
-      if (lane == 0) {
-        auto qk = [&](int t, int kt) {  // S_t = Q_t K_kt^T
-          const uint32_t qs = smem_u32(smem + kQOff + t * kTile);
-          const uint32_t ks = smem_u32(smem + kKVOff + k_slot(kbase + kt) * kTile);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            umma_f16_ss(tbase + t * 128,
-                        sdesc_sw128(qs + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024),
-                        sdesc_sw128(ks + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024), id_qk,
-                        k > 0 ? 1u : 0u);
           umma_commit(bar(kSFull + t));
-        };
-        auto pv = [&](int t, int kt) {  // O_t += P_t V_kt, P_t from TMEM
-          const uint32_t vs = smem_u32(smem + kKVOff + v_slot(kbase + kt) * kTile);
+        }
+        __syncwarp();
+      };
+      auto pv = [&](int t, int kt) {  // O_t += P_t V_kt, P_t from TMEM
+        const uint64_t vd =
+            sdesc_sw128(smem_u32(smem + kKVOff + v_slot(kbase + kt) * kTile), kHalf, 1024);
+        const uint32_t acc0 = kt > 0 ? 1u : 0u;
+        if (elect_one()) {
+          // K step k: 16 keys = 16 rows of 128 bytes of the MN-major V tile
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            umma_f16_ts(tbase + 256 + t * 128, tbase + t * 128 + 8 * k,
-                        sdesc_sw128(vs + k * 2048, kHalf, 1024), id_pv,
-                        (kt > 0 || k > 0) ? 1u : 0u);
+            umma_f16_ts(tbase + 256 + t * 128, tbase + t * 128 + 8 * k, vd + ((k * 2048) >> 4),
+                        id_pv, k > 0 ? 1u : acc0);
           umma_commit(bar(kPVDone + t));
-        };
+        }
+        __syncwarp();
+      };
+      for (int j = 0;; ++j) {
+        int x;
+        ok = take_item(j, &x);
+        if (!ok || x < 0) break;
+        const PairItem it = item_at(p, x, lane, false);
+        // the item's last V tile reaches past the context end: its tail rows
+        // are cleared by the TMA warp before any PV reads it
+        const bool v_tail = it.nkv > 0 && it.L < it.nkv * 128;
         // S of both tiles is free (their last P was consumed before the
         // previous item's last PV), so this item's first QKs go at once; a
-        // tile's first PV waits for that tile's previous epilogue (o_free).
-        // A tile with no work this item gets an empty S commit after its
-        // o_free wait, which keeps its softmax warps in step.
+        // tile's first PV waits for the previous item's epilogue to have
+        // read that tile's O (o_free).  A tile with no work this item gets
+        // an empty S commit, which keeps its softmax warps in step.
         bool owait[2] = {j == 0, j == 0};  // o_free of the previous item seen
-        // After an item in which a tile had no work, wait for its (instant)
-        // epilogue before committing that tile's next S, so its softmax
-        // warps have taken the empty commit first (never two phases behind).
+        // After an item in which a tile had no work, wait for that item's
+        // o_free before committing the tile's next S: the epilogue only
+        // frees O after the softmax has handed over its row sums, i.e.
+        // after it took the empty commit (never two S phases behind).
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!owait[t] && prev_nkv[t] == 0) {
-            if (ok) ok = mbar_wait_bounded(bar(kOFree + t), (j - 1) & 1);
+            if (ok) ok = warp_wait(bar(kOFree + t), (j - 1) & 1);
             owait[t] = true;
           }
         }
-        if (ok) ok = mbar_wait_bounded(bar(kQFull), j & 1);
+        if (ok) ok = warp_wait(bar(kQFull), j & 1);
         if (ok && it.nkv > 0) {
-          ok = mbar_wait_bounded(bar(kKVFull + k_slot(kbase)), k_par(kbase));
-          if (ok) tc_fence_after();
+          ok = warp_wait(bar(kKVFull + k_slot(kbase)), k_par(kbase));
+          tc_fence_after();
         }
 #pragma unroll
-        for (int t = 0; t < 2 && ok; ++t) {
+        for (int t = 0; t < 2; ++t) {
+          if (!ok) break;
           if (it.nkv_t[t] > 0) {
             qk(t, 0);
           } else {
-            if (!owait[t]) ok = mbar_wait_bounded(bar(kOFree + t), (j - 1) & 1);
+            if (!owait[t]) ok = warp_wait(bar(kOFree + t), (j - 1) & 1);
             owait[t] = true;
-            umma_commit(bar(kSFull + t));
+            commit(kSFull + t);
+            commit(kOFull + t);  // nothing to add: O is "done" at once
           }
         }
-        if (ok && it.nkv > 0) umma_commit(bar(kKVEmpty + k_slot(kbase)));
-        if (ok && it.nkv <= 1) umma_commit(bar(kQEmpty));  // no further QK reads Q
+        if (ok && it.nkv > 0) commit(kKVEmpty + k_slot(kbase));
+        if (ok && it.nkv <= 1) commit(kQEmpty);  // no further QK reads Q
         for (int kt = 0; ok && kt < it.nkv; ++kt) {
           const bool more = kt + 1 < it.nkv;
           // Each group waits only for its own operands: PV for V_kt and P,
@@ -462,25 +534,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int t = 0; t < 2; ++t) {
             if (kt < it.nkv_t[t]) {
               if (!owait[t]) {
-                ok = mbar_wait_bounded(bar(kOFree + t), (j - 1) & 1);
+                ok = warp_wait(bar(kOFree + t), (j - 1) & 1);
                 owait[t] = true;
                 if (!ok) break;
                 tc_fence_after();
               }
               if (!have_v) {
-                ok = mbar_wait_bounded(bar(kKVFull + v_slot(kbase + kt)), v_par(kbase + kt));
+                ok = warp_wait(bar(kKVFull + v_slot(kbase + kt)), v_par(kbase + kt));
+                if (ok && v_tail && kt + 1 == it.nkv) {  // cleared by the TMA warp
+                  ok = warp_wait(bar(kVFixed), nfix & 1);
+                  if (lane == 0) mbar_arrive(bar(kVFixFree));
+                  ++nfix;
+                }
                 have_v = true;
               }
-              if (ok) ok = mbar_wait_bounded(bar(kPFull + t), pcnt[t] & 1);
+              if (ok) ok = warp_wait(bar(kPFull + t), pcnt[t] & 1);
               if (!ok) break;
               tc_fence_after();
               pv(t, kt);
+              if (kt + 1 == it.nkv_t[t]) commit(kOFull + t);  // tile t's last PV
               ++pcnt[t];
             }
             if (kt + 1 < it.nkv_t[t]) {
               if (!have_k) {
-                ok = mbar_wait_bounded(bar(kKVFull + k_slot(kbase + kt + 1)),
-                                       k_par(kbase + kt + 1));
+                ok = warp_wait(bar(kKVFull + k_slot(kbase + kt + 1)), k_par(kbase + kt + 1));
                 have_k = true;
                 if (!ok) break;
                 tc_fence_after();
@@ -489,36 +566,94 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (!ok) break;
-          if (kt + 2 == it.nkv) umma_commit(bar(kQEmpty));  // the item's last QK
-          umma_commit(bar(kKVEmpty + v_slot(kbase + kt)));
-          if (more) umma_commit(bar(kKVEmpty + k_slot(kbase + kt + 1)));
+          if (kt + 2 == it.nkv) commit(kQEmpty);  // the item's last QK
+          commit(kKVEmpty + v_slot(kbase + kt));
+          if (more) commit(kKVEmpty + k_slot(kbase + kt + 1));
         }
+        kbase += it.nkv;
+        prev_nkv[0] = it.nkv_t[0];
+        prev_nkv[1] = it.nkv_t[1];
+        if (!ok) break;
       }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      kbase += it.nkv;
-      prev_nkv[0] = it.nkv_t[0];
-      prev_nkv[1] = it.nkv_t[1];
-      if (!ok) break;
-    }
-    if (lane == 0) {
-      if (!ok) {
+      if (!ok && lane == 0) {
         raise_error(p.err, PA_DEVERR_TIMEOUT);
         misc[3] = 1;
       }
       // Every MMA issued above has completed once this barrier fires.
-      umma_commit(bar(kFin));
-      mbar_wait_bounded(bar(kFin), 0);
+      commit(kFin);
+      warp_wait(bar(kFin), 0);
     }
-    __syncwarp();
+  } else if (warp >= kEpiWarp0) {
+    // ----------------------------------------------------- epilogue --
+    // Per item and tile: wait for the tile's last PV and its row sums, read
+    // O / l out of TMEM (then O is free for the next item's first PV) and
+    // store the rows.  Runs alongside the next item's softmax.
+    reg_dealloc<kEpilogueRegs>();
+    const int q = warp - kEpiWarp0;  // TMEM lanes 32q .. 32q+31
+    const int r = q * 32 + lane;     // query row in the tile
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    bool ok = true;
+    for (int j = 0;; ++j) {
+      int x;
+      ok = take_item(j, &x);
+      if (!ok || x < 0) break;
+      const PairItem it = item_at(p, x, lane, false);
+#pragma unroll 1
+      for (int t = 0; t < 2; ++t) {
+        const int nkv_t = it.nkv_t[t];
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kOFull + t), j & 1));
+        tc_fence_after();
+        // every thread waits: each reads row sums another warp wrote
+        if (ok) ok = mbar_wait_bounded(bar(kLFull + t), j & 1);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const float l = l_buf[t * 128 + r];
+        const float inv_l = (nkv_t > 0 && l > 0.f) ? 1.f / l : 0.f;
+        const bool rows = it.row0[t] < it.q_len;
+        uint32_t w[64];  // the row of O / l, packed to the output type
+        if (nkv_t > 0 && rows) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tbase + lane_addr + 256 + t * 128 + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              w[c * 16 + i] = E::pack2(__uint_as_float(o[2 * i]) * inv_l,
+                                       __uint_as_float(o[2 * i + 1]) * inv_l);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) w[i] = 0u;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kOFree + t));  // O of this tile is free
+        const int64_t grow = static_cast<int64_t>(it.q_start) + it.row0[t] + r;
+        if (rows && it.row0[t] + r < it.q_len && grow >= 0 && grow < p.total_q) {
+          typename E::T *orow =
+              static_cast<typename E::T *>(p.out) + grow * p.out_row_stride + it.h * 128;
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            *reinterpret_cast<uint4 *>(orow + c * 8) =
+                make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        }
+      }
+      if (!ok) break;
+    }
+    if (!ok && lane == 0) {
+      raise_error(p.err, PA_DEVERR_TIMEOUT);
+      misc[3] = 1;
+    }
   } else {
     // ------------------------------------------------------- softmax --
+    reg_alloc<kSoftmaxRegs>();
     const int t = warp >> 2;   // tile A or B
     const int r = tid & 127;   // query row in the tile == TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_tm = tbase + lane_addr + t * 128;
     const uint32_t o_tm = tbase + lane_addr + 256 + t * 128;
     const float sl = p.scale_log2;
-    int kbase = 0;   // ring position of the item's first V tile
     int n = 0;       // S phases of this query tile (QK results and empty commits)
     int pn = 0;      // PVs of this query tile
     bool ok = true;
@@ -564,55 +699,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_new = raise_max ? mt : m_ref;
         const float corr = raise_max ? fast_exp2(m_ref - m_new) : 1.f;
         const float mu = m_new == -INFINITY ? 0.f : m_new;
-        if (kt >= 1) {
-          // P(kt-1) has been consumed and O holds the sum through kt-1 (PV(kt-1)
-          // was issued before S(kt), so this wait is normally already over).
-          ok = mbar_wait_bounded(bar(kPVDone + t), (pn - 1) & 1);
-          if (!ok) break;
-          tc_fence_after();
-        }
-        // The first tile to read V_kt zeroes its rows past the context end
-        // (they may hold anything, even NaN; their weight is zero).
-        const bool first_reader = t == 0 || kt >= it.nkv_t[0];
-        if (first_reader && it.L < (kt + 1) * 128) {
-          const int vn = kbase + kt;
-          ok = mbar_wait_bounded(bar(kKVFull + v_slot(vn)), v_par(vn));
-          if (!ok) break;
-          uint8_t *vt = smem + kKVOff + v_slot(vn) * kTile;
-          const int first = it.L - kt * 128;
-          for (int i = r; i < (128 - first) * 16; i += 128) {
-            const int row = first + i / 16, c16 = i % 16;
-            *reinterpret_cast<uint4 *>(vt + (c16 >> 3) * kHalf + row * 128 + (c16 & 7) * 16) =
-                make_uint4(0, 0, 0, 0);
-          }
-        }
         // p = 2^(s * scale*log2(e) - max), rounded to the input type for the
-        // tensor core; the row sum uses the same rounded values, so O / l is
-        // an exact weighted mean of V under the rounded weights.
+        // tensor core; the row sum adds the same rounded values (exactly
+        // widened), so O / l is an exact weighted mean of V under the
+        // rounded weights.  S(kt) being complete means PV(kt-1) has read
+        // P(kt-1): the tensor core runs one thread's MMAs in order.
         const uint64_t sl2 = f2_pack(sl, sl), nmu2 = f2_pack(-mu, -mu);
-        uint64_t rs2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+        float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int hf = 0; hf < 4; ++hf) {  // 32 columns -> 16 packed words
           uint32_t pw[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
             const int i = hf * 16 + k;  // column pair
-            float x0f, x1f, e0, e1;
+            float x0f, x1f;
             f2_unpack(f2_fma(f2_pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
                              sl2, nmu2),
                       x0f, x1f);
-            if ((i & kPolyMask) == kPolyMask) {
-              f2_unpack(f2_exp2_poly(x0f, x1f), e0, e1);
-              if (edge) {
-                e0 = 2 * i <= bound ? e0 : 0.f;
-                e1 = 2 * i + 1 <= bound ? e1 : 0.f;
-              }
-            } else {
-              e0 = fast_exp2(x0f);  // 2^-inf = 0 for masked columns
-              e1 = fast_exp2(x1f);
-            }
-            pw[k] = E::pack2(e0, e1);
-            rs2[k & 1] = f2_add(rs2[k & 1], f2_pack(E::lo(pw[k]), E::hi(pw[k])));
+            pw[k] = E::pack2(fast_exp2(x0f), fast_exp2(x1f));  // 2^-inf = 0 when masked
+            E::add_halves(pw[k], rs[(k & 1) * 2], rs[(k & 1) * 2 + 1]);
           }
           // P overlays the first 64 columns of this tile's S in TMEM, two
           // 16-bit values per column (the A operand of O += P V).
@@ -620,6 +725,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
         if (kt >= 1 && __any_sync(0xffffffffu, raise_max)) {
+          // O holds the sum through PV(kt-1): wait for it, then rescale.
+          ok = mbar_wait_bounded(bar(kPVDone + t), (pn - 1) & 1);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t o[32];
@@ -631,55 +740,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
         }
-        float rsum[4];
-        f2_unpack(rs2[0], rsum[0], rsum[1]);
-        f2_unpack(rs2[1], rsum[2], rsum[3]);
-        l = l * corr + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
+        l = l * corr + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
         m_ref = m_new;
-        fence_proxy_async_smem();  // V-tail zeroing (generic writes) before the MMA
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kPFull + t));
       }
-      // ---------------------------------------------------- epilogue --
-      if (ok && it.row0[t] < it.q_len) {
-        const bool have_o = my_nkv > 0 && mbar_wait_bounded(bar(kPVDone + t), (pn - 1) & 1);
-        ok = my_nkv == 0 || have_o;
-        if (my_nkv > 0) tc_fence_after();
-        const float inv_l = (have_o && l > 0.f) ? 1.f / l : 0.f;
-        const int64_t grow = static_cast<int64_t>(it.q_start) + it.row0[t] + r;
-        const bool store = it.row0[t] + r < it.q_len && grow >= 0 && grow < p.total_q;
-        typename E::T *orow =
-            static_cast<typename E::T *>(p.out) + grow * p.out_row_stride + it.h * 128;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          if (have_o) {
-            tmem_ld32(o_tm + c * 32, o);
-            tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = 0u;
-          }
-          if (store) {
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint4 w;
-              const float *f = reinterpret_cast<const float *>(o) + q4 * 8;
-              w.x = E::pack2(f[0] * inv_l, f[1] * inv_l);
-              w.y = E::pack2(f[2] * inv_l, f[3] * inv_l);
-              w.z = E::pack2(f[4] * inv_l, f[5] * inv_l);
-              w.w = E::pack2(f[6] * inv_l, f[7] * inv_l);
-              *reinterpret_cast<uint4 *>(orow + c * 32 + q4 * 8) = w;
-            }
-          }
-        }
-      }
-      kbase += it.nkv;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kOFree + t));  // O of this tile is free
       if (!ok) break;
+      // Hand the row sums to the epilogue once it has taken the previous
+      // item's (its o_free of that item comes after reading them).
+      if (j > 0) ok = warp_wait(bar(kOFree + t), (j - 1) & 1);
+      if (!ok) break;
+      l_buf[t * 128 + r] = l;
+      mbar_arrive(bar(kLFull + t));
     }
     if (!ok) {
       raise_error(p.err, PA_DEVERR_TIMEOUT);
@@ -706,6 +779,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 }  // namespace
+
+// The register split inside the kernel (setmaxnreg) must fit in what the
+// CTA is launched with, or its .inc would wait for registers that never
+// come: refuse to launch a build where it would not.
+template <auto Kernel>
+cudaError_t check_register_pool() {
+  static const cudaError_t status = [] {
+    cudaFuncAttributes attr;
+    const cudaError_t e = cudaFuncGetAttributes(&attr, Kernel);
+    if (e != cudaSuccess) return e;
+    return attr.numRegs * kThreads >= kRegPoolNeeded ? cudaSuccess
+                                                     : cudaErrorInvalidConfiguration;
+  }();
+  return status;
+}
 
 // Launches so far in this process; picks each launch's schedule slot.
 std::atomic<uint32_t> g_prefill_launches{0};
@@ -744,11 +832,13 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
   cudaError_t e;
   if (a.dtype == PA_BF16) {
     e = allow_dynamic_smem<prefill_kernel<BF16>>();
+    if (e == cudaSuccess) e = check_register_pool<prefill_kernel<BF16>>();
     if (e != cudaSuccess) return e;
     prefill_kernel<BF16><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(
         p, a.tm_q, a.tm_k, a.tm_v);
   } else {
     e = allow_dynamic_smem<prefill_kernel<F16>>();
+    if (e == cudaSuccess) e = check_register_pool<prefill_kernel<F16>>();
     if (e != cudaSuccess) return e;
     prefill_kernel<F16><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(
         p, a.tm_q, a.tm_k, a.tm_v);
