@@ -51,6 +51,15 @@ def static_decode(lib, x, out, partition_size, err):
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
+def inputs(name, **kw):
+    """Seeded inputs with the step's new tokens already in the cache (decode
+    reads the cache after the write, so context_lens count them)."""
+    x = W.make_inputs(name, device="cuda", **kw)
+    if x.slot_mapping.numel():
+        pa.pa_reshape_and_cache(x.k_new, x.v_new, x.k_pool, x.v_pool, x.slot_mapping)
+    return x
+
+
 def allocated_decode(x, partition_size):
     out = torch.empty_like(x.q)
     pa.pa_decode(out, x.q, x.k_pool, x.v_pool, x.block_table, x.context_lens, scale=x.scale,
@@ -74,13 +83,13 @@ def check(lib, x, partition_size=0):
 def test_two_calls_in_a_row_match_pa_decode():
     lib = _lib()
     # 1: many partitions per sequence (the array holds partial results)
-    a = W.make_inputs("llama7b-decode", device="cuda")
+    a = inputs("llama7b-decode")
     P, need = pa.pa_decode_plan(a.num_seqs, a.num_q_heads, a.num_kv_heads, a.head_dim,
                                 a.max_context_len, 64)
     assert 0 < need <= STATIC_BYTES
     out_a = check(lib, a, partition_size=64)
     # 2: different shapes and dtype right after, reusing the same array
-    b = W.make_inputs("continuous-batching", device="cuda")
+    b = inputs("continuous-batching")
     check(lib, b, partition_size=128)
     # 1 again: identical to the first call (no state carried over)
     again = torch.empty_like(a.q)
@@ -92,8 +101,7 @@ def test_two_calls_in_a_row_match_pa_decode():
 
 def test_automatic_plan_is_lengthened_to_fit():
     lib = _lib()
-    x = W.make_inputs("long-context-decode", device="cuda",
-                      lengths=[131072, 120000, 90000, 131000])
+    x = inputs("long-context-decode", lengths=[131072, 120000, 90000, 131000])
     _, need = pa.pa_decode_plan(x.num_seqs, x.num_q_heads, x.num_kv_heads, x.head_dim,
                                 x.max_context_len, 0)
     assert need > STATIC_BYTES  # the default plan would not fit
