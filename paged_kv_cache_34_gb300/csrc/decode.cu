@@ -152,6 +152,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int P = p.partition_size;
   const int nseq = p.num_seqs;
+  griddep_wait();  // inputs (e.g. this step's cache write) come from earlier kernels
+  griddep_launch_dependents();
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -537,57 +539,83 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 // Merges the partitions of each (sequence, query head) by log-sum-exp:
 //   M = max_p m_p,  w_p = 2^(m_p - M),  out = sum_p w_p o_p / sum_p w_p l_p.
+// One warp per (sequence, query head): the lanes first read the partitions'
+// (m, l) pairs side by side and leave the weights in shared memory, then
+// each lane sums its D/32 output elements over all partitions with many
+// loads in flight.
+constexpr int kCombineWarps = 4;
+constexpr int kCombineMaxParts = 2048;  // weights kept in shared memory up to this
+
 template <class E, int D>
-__global__ void __launch_bounds__(D) decode_combine_kernel(const DecodeParams p) {
-  extern __shared__ float sw[];  // [num_partitions] weights
-  __shared__ float red[D / 32];
-  const int b = blockIdx.x / p.hq, h = blockIdx.x % p.hq;
-  const int tid = threadIdx.x;
+__global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const DecodeParams p) {
+  extern __shared__ float sw[];  // [kCombineWarps][min(num_partitions, kCombineMaxParts)]
+  griddep_wait();  // the partial states of the decode kernel
+  griddep_launch_dependents();
+  constexpr int V = D / 32;  // output elements per lane
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kCombineWarps + warp;  // (sequence, query head)
+  if (row >= p.num_seqs * p.hq) return;
+  const int b = row / p.hq, h = row - b * p.hq;
   const int L = checked_context_len(__ldg(p.context_lens + b), p.capacity, p.max_ctx, p.err, false);
   const int n = (L + p.partition_size - 1) / p.partition_size;
-  if (n <= 1) return;
+  if (n <= 1) return;  // written by the decode kernel itself
   const int64_t row0 = (static_cast<int64_t>(b) * p.hq + h) * p.num_partitions;
-  const float *ml = p.ws_ml + row0 * 2;
+  const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml) + row0;
+  const bool in_smem = p.num_partitions <= kCombineMaxParts;
+  float *w = sw + warp * (in_smem ? p.num_partitions : 0);
 
-  float mx = -INFINITY;
-  for (int i = tid; i < n; i += D) mx = fmaxf(mx, ml[2 * i]);
+  float M = -INFINITY;
+  for (int i = lane; i < n; i += 32) M = fmaxf(M, ml[i].x);
 #pragma unroll
-  for (int m = 16; m > 0; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-  if ((tid & 31) == 0) red[tid >> 5] = mx;
-  __syncthreads();
-  float M = red[0];
-#pragma unroll
-  for (int w = 1; w < D / 32; ++w) M = fmaxf(M, red[w]);
-  __syncthreads();
-
+  for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
   float ls = 0.f;
-  for (int i = tid; i < n; i += D) {
-    const float m = ml[2 * i];
-    const float w = (M == -INFINITY) ? 0.f : exp2f(m - M);
-    sw[i] = w;
-    ls += w * ml[2 * i + 1];
+  if (M != -INFINITY) {
+    for (int i = lane; i < n; i += 32) {
+      const float2 v = ml[i];
+      const float wi = exp2f(v.x - M);
+      if (in_smem) w[i] = wi;
+      ls += wi * v.y;
+    }
   }
 #pragma unroll
-  for (int m = 16; m > 0; m >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, m);
-  if ((tid & 31) == 0) red[tid >> 5] = ls;
-  __syncthreads();
-  float l = 0.f;
-#pragma unroll
-  for (int w = 0; w < D / 32; ++w) l += red[w];
+  for (int x = 16; x > 0; x >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, x);
+  __syncwarp();
 
-  const float *po = p.ws_o + row0 * D + tid;
-  float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-  int i = 0;
-  for (; i + 4 <= n; i += 4) {
-    acc0 += sw[i] * po[(i + 0) * D];
-    acc1 += sw[i + 1] * po[(i + 1) * D];
-    acc2 += sw[i + 2] * po[(i + 2) * D];
-    acc3 += sw[i + 3] * po[(i + 3) * D];
+  float acc[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) acc[v] = 0.f;
+  if (M != -INFINITY) {
+    const float *po = p.ws_o + row0 * D + lane * V;
+#pragma unroll 8
+    for (int i = 0; i < n; ++i) {
+      const float wi = in_smem ? w[i] : exp2f(ml[i].x - M);
+      if constexpr (V == 4) {
+        const float4 o4 = *reinterpret_cast<const float4 *>(po + static_cast<int64_t>(i) * D);
+        acc[0] += wi * o4.x;
+        acc[1] += wi * o4.y;
+        acc[2] += wi * o4.z;
+        acc[3] += wi * o4.w;
+      } else {
+        const float2 o2 = *reinterpret_cast<const float2 *>(po + static_cast<int64_t>(i) * D);
+        acc[0] += wi * o2.x;
+        acc[1] += wi * o2.y;
+      }
+    }
   }
-  for (; i < n; ++i) acc0 += sw[i] * po[i * D];
-  const float acc = (acc0 + acc1) + (acc2 + acc3);
-  typename E::T *out = static_cast<typename E::T *>(p.out) + b * p.out_row_stride + h * D;
-  out[tid] = E::from_float(l > 0.f ? acc / l : 0.f);
+  // a sum that is not positive (no visible key, or a non-finite state from a
+  // bad block) gives zeros
+  const bool good = ls > 0.f;
+  const float inv = good ? 1.f / ls : 0.f;
+  typename E::T *out =
+      static_cast<typename E::T *>(p.out) + b * p.out_row_stride + h * D + lane * V;
+  if constexpr (V == 4) {
+    *reinterpret_cast<uint2 *>(out) =
+        make_uint2(E::pack2(good ? acc[0] * inv : 0.f, good ? acc[1] * inv : 0.f),
+                   E::pack2(good ? acc[2] * inv : 0.f, good ? acc[3] * inv : 0.f));
+  } else {
+    *reinterpret_cast<uint32_t *>(out) =
+        E::pack2(good ? acc[0] * inv : 0.f, good ? acc[1] * inv : 0.f);
+  }
 }
 
 template <class E, int D, int BOXR>
@@ -602,12 +630,16 @@ cudaError_t launch_typed(const DecodeArgs &a, const DecodeParams &p, cudaStream_
   int64_t grid = (items + kWorkers - 1) / kWorkers;
   if (grid > 2LL * a.num_sms) grid = 2LL * a.num_sms;
   if (grid < 1) grid = 1;
-  kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p, a.tm_k, a.tm_v);
-  e = cudaGetLastError();
+  e = launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, stream, p,
+                 a.tm_k, a.tm_v);
   if (e != cudaSuccess || a.num_partitions <= 1) return e;
-  decode_combine_kernel<E, D><<<a.num_seqs * a.num_q_heads, D,
-                                a.num_partitions * sizeof(float), stream>>>(p);
-  return cudaGetLastError();
+  const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.num_q_heads;
+  const size_t wbytes = a.num_partitions <= kCombineMaxParts
+                            ? kCombineWarps * a.num_partitions * sizeof(float)
+                            : 0;
+  return launch_pdl(decode_combine_kernel<E, D>,
+                    dim3(static_cast<unsigned>((rows + kCombineWarps - 1) / kCombineWarps)),
+                    dim3(kCombineWarps * 32), wbytes, stream, p);
 }
 
 template <class E, int D>

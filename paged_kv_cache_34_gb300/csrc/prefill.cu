@@ -250,6 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  griddep_wait();  // inputs (e.g. this step's cache write) come from earlier kernels
+  griddep_launch_dependents();
   SchedSlot *sched = &g_prefill_sched[p.sched_slot];
   // Item j of this CTA: index published by the TMA warp in ring entry j % 4;
   // every other role takes it from there (lane 0 waits, the warp shares it).
@@ -834,16 +836,16 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     e = allow_dynamic_smem<prefill_kernel<BF16>>();
     if (e == cudaSuccess) e = check_register_pool<prefill_kernel<BF16>>();
     if (e != cudaSuccess) return e;
-    prefill_kernel<BF16><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(
-        p, a.tm_q, a.tm_k, a.tm_v);
+    e = launch_pdl(prefill_kernel<BF16>, dim3(static_cast<unsigned>(grid)), dim3(kThreads),
+                   kSmemBytes, stream, p, a.tm_q, a.tm_k, a.tm_v);
   } else {
     e = allow_dynamic_smem<prefill_kernel<F16>>();
     if (e == cudaSuccess) e = check_register_pool<prefill_kernel<F16>>();
     if (e != cudaSuccess) return e;
-    prefill_kernel<F16><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(
-        p, a.tm_q, a.tm_k, a.tm_v);
+    e = launch_pdl(prefill_kernel<F16>, dim3(static_cast<unsigned>(grid)), dim3(kThreads),
+                   kSmemBytes, stream, p, a.tm_q, a.tm_k, a.tm_v);
   }
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace pa

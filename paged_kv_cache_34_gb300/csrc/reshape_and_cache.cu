@@ -30,6 +30,8 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     uint4 *__restrict__ key_cache, uint4 *__restrict__ value_cache,
     const int64_t *__restrict__ slot_mapping, int32_t num_tokens, int32_t row_vec,
     int64_t num_slots, int32_t *err) {
+  griddep_wait();  // inputs may come from the kernel just before this one
+  griddep_launch_dependents();
   for (int64_t t = blockIdx.x; t < num_tokens; t += gridDim.x) {
     const int64_t slot = __ldg(slot_mapping + t);
     if (slot < 0) continue;
@@ -65,12 +67,11 @@ cudaError_t launch_reshape_and_cache(const ReshapeArgs &a, cudaStream_t stream) 
   // Enough CTAs to cover the GPU several times over; each walks tokens.
   const int64_t max_ctas = static_cast<int64_t>(a.num_sms) * 16;
   const int grid = static_cast<int>(a.num_tokens < max_ctas ? a.num_tokens : max_ctas);
-  reshape_and_cache_kernel<<<grid, threads, 0, stream>>>(
-      static_cast<const uint4 *>(a.key), static_cast<const uint4 *>(a.value),
-      a.row_stride_bytes / 16, static_cast<uint4 *>(a.key_cache),
-      static_cast<uint4 *>(a.value_cache), a.slot_mapping, a.num_tokens, row_vec, a.num_slots,
-      a.d_error);
-  return cudaGetLastError();
+  return launch_pdl(reshape_and_cache_kernel, dim3(grid), dim3(threads), 0, stream,
+                    static_cast<const uint4 *>(a.key), static_cast<const uint4 *>(a.value),
+                    static_cast<int64_t>(a.row_stride_bytes / 16),
+                    static_cast<uint4 *>(a.key_cache), static_cast<uint4 *>(a.value_cache),
+                    a.slot_mapping, a.num_tokens, row_vec, a.num_slots, a.d_error);
 }
 
 }  // namespace pa
