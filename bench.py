@@ -201,10 +201,17 @@ def decode_step_fn(pa, x, out, ws, stream):
 
 
 def decode_workspace(pa, x):
+    """Workspace for the plan pa_decode uses, and the plan: partition size
+    (0 = balanced split across the grid's workers) and partitions of the
+    longest context (None for the balanced split, whose pieces depend on
+    the device-side lengths)."""
     part, need = pa.pa_decode_plan(x.num_seqs, x.num_q_heads, x.num_kv_heads, x.head_dim,
                                    x.max_context_len, x.partition_size)
     ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda") if need else None
-    nparts = math.ceil(x.max_context_len / part) if x.max_context_len else 1
+    if part == 0:
+        nparts = None
+    else:
+        nparts = math.ceil(x.max_context_len / part) if x.max_context_len else 1
     return ws, part, nparts
 
 
@@ -451,7 +458,8 @@ def main():
     kv = kv_read_bytes(x)
     total_kv = reduce_sum(dist, kv)  # every rank's own batch
     value = total_kv / (ms_step_max * 1e-3) / 1e9
-    launches_per_step = (1 if x.slot_mapping.numel() else 0) + 1 + (1 if nparts > 1 else 0)
+    merge = nparts is None or nparts > 1  # the merge kernel runs
+    launches_per_step = (1 if x.slot_mapping.numel() else 0) + 1 + (1 if merge else 0)
 
     ms_dec = statistics.fmean(t_dec)
     dec_achieved = decode_bytes(x) / (ms_dec * 1e-3) / 1e9
@@ -465,15 +473,17 @@ def main():
         "data": "synthetic",
         "config": {"workload": HEADLINE, "sequences_per_gpu": x.num_seqs,
                    "context": "U[512,2048]", "heads": "32/32", "head_dim": 128,
-                   "block_size": 16, "pool_blocks": 8192, "partition_size": part,
-                   "partitions": nparts, "kv_bytes_per_step": kv,
+                   "block_size": 16, "pool_blocks": 8192,
+                   "split_kv": "balanced across workers" if part == 0 else
+                               f"fixed partitions of {part} tokens ({nparts} for the longest)",
+                   "kv_bytes_per_step": kv,
                    "l2": "flushed before every timed step (512 MB write, then 512 MB read)",
                    "parallelism": f"replica x{world}" if world > 1 else "single GPU",
                    "wall_s_timed_region": round(wall, 3),
                    "pct_of_hbm_peak": round(100 * value / world / hbm_peak, 2)},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
-        "roofline": {"kernel": "pa_decode (partition + combine launches)", "bound": "hbm",
+        "roofline": {"kernel": "pa_decode (split-KV decode + merge launches)", "bound": "hbm",
                      "achieved": round(dec_achieved, 1), "peak": hbm_peak,
                      "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(dec_achieved / hbm_peak, 4), "traffic": traffic,

@@ -11,17 +11,24 @@
 // a scalar online softmax; this keeps the block walk and the online softmax
 // but is shaped for HBM bandwidth):
 //
-//  * Work items.  A sequence's context is cut into partitions of P tokens
-//    (split-KV); an item is one (sequence, KV head, partition).  Every item
-//    serves all G query heads of its KV head from the same K/V bytes (GQA
-//    sharing).  A sequence with one partition writes its output directly;
-//    otherwise each item writes its softmax state (max, sum, unnormalised
-//    output) to workspace and a combine kernel merges them by log-sum-exp.
+//  * Work.  A unit is one (sequence, KV head); every piece of work serves
+//    all G query heads of its KV head from the same K/V bytes (GQA sharing).
+//    Two schedules cut the units into pieces (split-KV):
+//      - fixed partitions (a partition size is given): a unit's context is
+//        cut into partitions of P tokens, the pages' scheme; worker w of W
+//        takes items w, w+W, ... of the (sequence, KV head, partition) list;
+//      - balanced (automatic): the units' contexts, each rounded up to 16
+//        tokens, are laid end to end and cut into equal chunks, one (or a
+//        few) per worker, so every worker streams the same number of tokens
+//        whatever the mix of lengths.  A chunk can hold the tail of one unit
+//        and the head of the next.
+//    A piece that is its unit's whole context writes the output directly;
+//    otherwise it writes its softmax state (max, sum, unnormalised output)
+//    to workspace and a merge kernel combines the pieces by log-sum-exp.
 //  * Persistent CTAs, independent warps.  The grid is at most two CTAs per
 //    SM.  Each of a CTA's four consumer warps is a worker with its own static
-//    list of items (worker w of W takes items w, w+W, ...), so no warp ever
-//    waits for another to merge results.  Items are numbered from a prefix sum
-//    of the sequences' item counts, computed once per CTA from context_lens.
+//    list of pieces, so no warp ever waits for another.  The lists come from
+//    per-sequence prefix sums computed once per CTA from context_lens.
 //  * One producer warp feeds all four workers through a 3-stage ring of
 //    TMA tile loads (128-byte swizzle) guarded by mbarriers: each stage holds
 //    16 tokens of K and V for every worker, read block by block through the
@@ -78,15 +85,35 @@ struct DecodeParams {
   int64_t num_blocks;
   float scale_log2;
   int32_t partition_size, num_partitions, max_ids;
+  int32_t balanced, chunk_cap, num_workers;  // balanced schedule (see above)
   float *ws_o, *ws_ml;
+  int32_t *ws_pref;  // balanced: the prefix sums, for the merge kernel
   int32_t *err;
 };
 
-// One work item: partition `part` of sequence b for KV head g, tokens
-// [start, end) of a context of L tokens.
+// One piece of work: tokens [start, end) of KV head g of sequence b (whose
+// context is L tokens).  `direct`: the piece is the unit's whole context and
+// writes the output; else its softmax state goes to workspace rows
+// prow + h * pstride for the unit's query heads h = 0..G-1.
 struct Item {
   int b, g, part, L, start, end;
+  bool direct;
+  int64_t prow;
+  int pstride;
 };
+
+__host__ __device__ __forceinline__ int ceil16(int x) { return (x + 15) & ~15; }
+
+// Balanced schedule: chunk size (in 16-rounded token-heads) for T token-heads
+// over NW workers, each taking at most `cap` tokens per chunk (and then
+// several chunks).  The decode and merge kernels must agree on it.
+__host__ __device__ __forceinline__ int balanced_chunk(int T, int NW, int cap) {
+  const int64_t per = static_cast<int64_t>(NW) * cap;
+  const int k = T > 0 ? static_cast<int>((T + per - 1) / per) : 1;
+  const int64_t kn = static_cast<int64_t>(k) * NW;
+  const int c = ceil16(static_cast<int>((T + kn - 1) / kn));
+  return c > 0 ? c : 16;
+}
 
 // Item i of the numbering given by the prefix sums `pref` (items of sequence
 // b are pref[b] .. pref[b+1]-1, ordered by KV head then partition).
@@ -110,6 +137,75 @@ __device__ __forceinline__ Item decode_item(int i, const int *pref, const int *l
   if (m.end < m.start) m.end = m.start;
   (void)hkv;
   return m;
+}
+
+// What every role of a CTA needs to walk the schedule.
+struct Sched {
+  const int *pref;  // fixed: items before sequence b; balanced: token-heads before b
+  const int *len;   // checked context lengths
+  int S, hkv, hq, G, P, NP, NW;
+  bool balanced;
+  int total;      // fixed: items; balanced: token-heads
+  int C, chunks;  // balanced: chunk size and count
+};
+// A worker's place in its piece list (fixed: next item index; balanced:
+// current chunk and position in it).
+struct Cursor {
+  int i, x;
+};
+__device__ __forceinline__ Cursor first_cursor(const Sched &sc, int gw) {
+  Cursor c;
+  c.i = gw;
+  c.x = sc.balanced ? gw * sc.C : 0;
+  return c;
+}
+
+// The next piece of a worker's list; false at the end.  The fixed schedule
+// also returns the (empty) items of empty sequences, end == start.
+__device__ bool next_piece(const Sched &sc, Cursor &cu, Item &m) {
+  if (!sc.balanced) {
+    if (cu.i >= sc.total) return false;
+    m = decode_item(cu.i, sc.pref, sc.len, sc.S, sc.hkv, sc.P);
+    cu.i += sc.NW;
+    m.direct = (m.L > 0 ? (m.L + sc.P - 1) / sc.P : 1) == 1;
+    m.prow = (static_cast<int64_t>(m.b) * sc.hq + m.g * sc.G) * sc.NP + m.part;
+    m.pstride = sc.NP;
+    return true;
+  }
+  while (cu.i < sc.chunks) {
+    const int cend = min((cu.i + 1) * sc.C, sc.total);
+    if (cu.x >= cend) {  // chunk done: this worker's next one
+      cu.i += sc.NW;
+      cu.x = cu.i * sc.C;
+      continue;
+    }
+    // the unit (sequence b, KV head g) holding position x: pref[b] <= x < pref[b+1]
+    int lo = 0, hi = sc.S;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (sc.pref[mid] <= cu.x) lo = mid;
+      else hi = mid;
+    }
+    const int L = sc.len[lo];
+    const int W = ceil16(L);
+    const int rel = cu.x - sc.pref[lo];
+    const int g = rel / W;
+    const int t0 = rel - g * W;
+    const int t1 = min(W, t0 + (cend - cu.x));
+    cu.x += t1 - t0;
+    if (t0 >= L) continue;  // only the rounding past the context end
+    m.b = lo;
+    m.g = g;
+    m.L = L;
+    m.part = cu.i;
+    m.start = t0;
+    m.end = min(t1, L);
+    m.direct = t0 == 0 && t1 >= L;
+    m.prow = (static_cast<int64_t>(lo) * sc.hkv + g + cu.i) * sc.G;
+    m.pstride = 1;
+    return true;
+  }
+  return false;
 }
 
 __device__ __forceinline__ float shfl_xor(float v, int m) {
@@ -173,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int L = checked_context_len(__ldg(p.context_lens + b), p.capacity, p.max_ctx,
                                           p.err, blockIdx.x == 0);
         s_len[b] = L;
-        items = (L > 0 ? (L + P - 1) / P : 1) * p.hkv;
+        items = (p.balanced ? ceil16(L) : (L > 0 ? (L + P - 1) / P : 1)) * p.hkv;
       }
       int incl = items;
 #pragma unroll
@@ -192,8 +288,22 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncthreads();
 
-  const int total = s_pref[nseq];
-  const int NW = gridDim.x * kWorkers;
+  Sched sc;
+  sc.pref = s_pref;
+  sc.len = s_len;
+  sc.S = nseq;
+  sc.hkv = p.hkv;
+  sc.hq = p.hq;
+  sc.G = p.group;
+  sc.P = P;
+  sc.NP = p.num_partitions;
+  sc.NW = gridDim.x * kWorkers;
+  sc.balanced = p.balanced != 0;
+  sc.total = s_pref[nseq];
+  sc.C = sc.balanced ? balanced_chunk(sc.total, sc.NW, p.chunk_cap) : 0;
+  sc.chunks = sc.balanced ? (sc.total + sc.C - 1) / sc.C : 0;
+  if (sc.balanced && blockIdx.x == 0 && p.ws_pref)
+    for (int i = tid; i <= nseq; i += blockDim.x) p.ws_pref[i] = s_pref[i];
   const int bs = p.block_size;
 
   // ------------------------------------------------------------ producer --
@@ -205,14 +315,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     // owns the stage barriers.
     const bool feeder = lane < kWorkers;
     int cur = 0, endt = 0, gq = 0, sel = 0, lblk = 0, off = 0;
-    int nx = total, nstart = 0, nend = 0, ng = 0, nbuf = 0;
-    bool act = false;
-    // Finds this worker's first item with tokens at index >= i (items of
-    // empty sequences carry no tokens: the worker writes their zeros itself)
-    // and starts copying its block ids into buffer `buf`.
-    auto prefetch = [&](int i, int buf) {
-      for (; i < total; i += NW) {
-        const Item m = decode_item(i, s_pref, s_len, nseq, p.hkv, P);
+    int nstart = 0, nend = 0, ng = 0, nbuf = 0;
+    bool act = false, have_next = false;
+    Cursor pc = first_cursor(sc, blockIdx.x * kWorkers + lane);
+    // Finds this worker's next piece with tokens (items of empty sequences
+    // carry none: the worker writes their zeros itself) and starts copying
+    // its block ids into buffer `buf`.
+    auto prefetch = [&](int buf) {
+      Item m;
+      have_next = false;
+      while (next_piece(sc, pc, m)) {
         if (m.end <= m.start) continue;
         const int l0 = m.start / bs;
         const int nblk = (m.end - 1) / bs - l0 + 1;
@@ -223,14 +335,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         nstart = m.start;
         nend = m.end;
         ng = m.g;
+        have_next = true;
         break;
       }
-      nx = i < total ? i : total;
       nbuf = buf;
     };
-    // Makes the prefetched item current and prefetches the one after it.
+    // Makes the prefetched piece current and prefetches the one after it.
     auto promote = [&]() {
-      act = nx < total;
+      act = have_next;
       if (!act) return;
       cp_async_wait_all();  // this item's ids (issued at least one item ago)
       cur = nstart;
@@ -239,10 +351,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       sel = nbuf;
       lblk = 0;
       off = nstart % bs;
-      prefetch(nx + NW, nbuf ^ 1);
+      prefetch(nbuf ^ 1);
     };
     if (feeder) {
-      prefetch(blockIdx.x * kWorkers + lane, 0);
+      prefetch(0);
       promote();
     }
     const int *ids = s_ids;
@@ -342,9 +454,18 @@ __global__ void __launch_bounds__(kThreads, 2)
   float m0, m1, l0, l1;
   bool item_bad = false;
   Item cur_item;
-  int it = blockIdx.x * kWorkers + warp;
-  int qn_item = -1;
+  Cursor wc = first_cursor(sc, blockIdx.x * kWorkers + warp);
+  int qn_b = -1, qn_g = -1;  // the unit whose query qn holds
   int cur = 0;
+  if (sc.balanced) {
+    // Empty sequences have no pieces: their (zero) outputs are written here.
+    for (int b = blockIdx.x * kWorkers + warp; b < nseq; b += sc.NW) {
+      if (s_len[b] != 0) continue;
+      uint4 *orow = reinterpret_cast<uint4 *>(static_cast<typename E::T *>(p.out) +
+                                              b * p.out_row_stride);
+      for (int e = lane; e < p.hq * D / 8; e += 32) orow[e] = make_uint4(0, 0, 0, 0);
+    }
+  }
 
   // Writes a finished item: the normalised output when it is its sequence's
   // only partition, else its softmax state for the combine.
@@ -354,8 +475,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       l0 += shfl_xor(l0, s);
       l1 += shfl_xor(l1, s);
     }
-    const int np = m.L > 0 ? (m.L + P - 1) / P : 1;
-    if (np == 1) {
+    if (m.direct) {
       const float i0 = (!bad_item && l0 > 0.f) ? 1.f / l0 : 0.f;
       const float i1 = (!bad_item && l1 > 0.f) ? 1.f / l1 : 0.f;
       typename E::T *out =
@@ -373,9 +493,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
     } else {
-      const int64_t row0 =
-          (static_cast<int64_t>(m.b) * p.hq + m.g * G) * p.num_partitions + m.part;
-      const int64_t hstride = p.num_partitions;
+      const int64_t row0 = m.prow;
+      const int64_t hstride = m.pstride;
 #pragma unroll
       for (int mt = 0; mt < KSTEPS; ++mt) {
         const int d0 = mt * 16 + (lane >> 2), d1 = d0 + 8;
@@ -402,18 +521,18 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
   };
-  // Starts this worker's next item with tokens at or after item index `it`;
-  // items of empty sequences are finished on the spot (zero output).
+  // Starts this worker's next piece with tokens; items of empty sequences
+  // (fixed schedule) are finished on the spot (zero output).
   auto begin = [&]() -> bool {
-    while (it < total) {
-      const Item m = decode_item(it, s_pref, s_len, nseq, p.hkv, P);
+    Item m;
+    while (next_piece(sc, wc, m)) {
 #pragma unroll
       for (int mt = 0; mt < KSTEPS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
       m0 = m1 = -INFINITY;
       l0 = l1 = 0.f;
       item_bad = false;
       if (m.end > m.start) {
-        if (qn_item == it) {
+        if (qn_b == m.b && qn_g == m.g) {
 #pragma unroll
           for (int ks = 0; ks < KSTEPS; ++ks) {
             qf[ks][0] = qn[ks][0];
@@ -424,16 +543,20 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         cur_item = m;
         cur = m.start;
-        // Prefetch the next item's query one item ahead.
-        const int nxt = it + NW;
-        if (nxt < total) {
-          load_q<E, D>(qn, p, decode_item(nxt, s_pref, s_len, nseq, p.hkv, P), lane);
-          qn_item = nxt;
+        // Prefetch the next piece's query one piece ahead.
+        Cursor peek = wc;
+        Item nm;
+        qn_b = qn_g = -1;
+        while (next_piece(sc, peek, nm)) {
+          if (nm.end <= nm.start) continue;
+          load_q<E, D>(qn, p, nm, lane);
+          qn_b = nm.b;
+          qn_g = nm.g;
+          break;
         }
         return true;
       }
       finalize(m, false);  // empty sequence: zeros
-      it += NW;
     }
     return false;
   };
@@ -528,7 +651,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       cur += kSub;
       if (cur >= end) {
         finalize(cur_item, item_bad);
-        it += NW;
         active = begin();
       }
     }
@@ -537,84 +659,128 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
-// Merges the partitions of each (sequence, query head) by log-sum-exp:
+// Merges the pieces of each (sequence, query head) by log-sum-exp:
 //   M = max_p m_p,  w_p = 2^(m_p - M),  out = sum_p w_p o_p / sum_p w_p l_p.
-// One warp per (sequence, query head): the lanes first read the partitions'
-// (m, l) pairs side by side and leave the weights in shared memory, then
-// each lane sums its D/32 output elements over all partitions with many
-// loads in flight.
+// One CTA of four warps per (sequence, query head).  Warp w takes pieces
+// w, w+4, ... eight at a time -- all their loads issued together, then
+// folded into a running (max, sum, D/32 output elements per lane) -- and the
+// four warps' states are folded once more through shared memory.  A unit's
+// pieces are workspace rows row0 + i * rstride: partitions 0..n-1 (fixed
+// schedule) or chunks c0..c1 (balanced schedule, piece (unit u, chunk c) in
+// rows (u + c) * G + h).
 constexpr int kCombineWarps = 4;
-constexpr int kCombineMaxParts = 2048;  // weights kept in shared memory up to this
+constexpr int kCombineBatch = 8;
 
 template <class E, int D>
 __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const DecodeParams p) {
-  extern __shared__ float sw[];  // [kCombineWarps][min(num_partitions, kCombineMaxParts)]
+  constexpr int V = D / 32;  // output elements per lane
+  __shared__ float s_m[kCombineWarps], s_l[kCombineWarps];
+  __shared__ float s_o[kCombineWarps][D];
   griddep_wait();  // the partial states of the decode kernel
   griddep_launch_dependents();
-  constexpr int V = D / 32;  // output elements per lane
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kCombineWarps + warp;  // (sequence, query head)
-  if (row >= p.num_seqs * p.hq) return;
-  const int b = row / p.hq, h = row - b * p.hq;
+  const int b = blockIdx.x / p.hq, h = blockIdx.x - b * p.hq;
   const int L = checked_context_len(__ldg(p.context_lens + b), p.capacity, p.max_ctx, p.err, false);
-  const int n = (L + p.partition_size - 1) / p.partition_size;
-  if (n <= 1) return;  // written by the decode kernel itself
-  const int64_t row0 = (static_cast<int64_t>(b) * p.hq + h) * p.num_partitions;
-  const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml) + row0;
-  const bool in_smem = p.num_partitions <= kCombineMaxParts;
-  float *w = sw + warp * (in_smem ? p.num_partitions : 0);
-
-  float M = -INFINITY;
-  for (int i = lane; i < n; i += 32) M = fmaxf(M, ml[i].x);
-#pragma unroll
-  for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
-  float ls = 0.f;
-  if (M != -INFINITY) {
-    for (int i = lane; i < n; i += 32) {
-      const float2 v = ml[i];
-      const float wi = exp2f(v.x - M);
-      if (in_smem) w[i] = wi;
-      ls += wi * v.y;
-    }
+  int n;
+  int64_t row0, rstride;
+  if (p.balanced) {
+    if (L <= 0) return;  // zeros written by the decode kernel
+    const int G = p.group, g = h / G;
+    const int T = p.ws_pref[p.num_seqs];
+    const int C = balanced_chunk(T, p.num_workers, p.chunk_cap);
+    const int U = p.ws_pref[b] + g * ceil16(L);  // the unit's first position
+    const int c0 = U / C, c1 = (U + L - 1) / C;
+    n = c1 - c0 + 1;
+    row0 = (static_cast<int64_t>(b) * p.hkv + g + c0) * G + (h - g * G);
+    rstride = G;
+  } else {
+    n = (L + p.partition_size - 1) / p.partition_size;
+    row0 = (static_cast<int64_t>(b) * p.hq + h) * p.num_partitions;
+    rstride = 1;
   }
-#pragma unroll
-  for (int x = 16; x > 0; x >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, x);
-  __syncwarp();
+  if (n <= 1) return;  // written by the decode kernel itself
+  const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml);
+  const float *po = p.ws_o + lane * V;
 
-  float acc[V];
+  // This warp's pieces, folded with an online max.
+  float M = -INFINITY, Ls = 0.f, acc[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = 0.f;
-  if (M != -INFINITY) {
-    const float *po = p.ws_o + row0 * D + lane * V;
-#pragma unroll 8
-    for (int i = 0; i < n; ++i) {
-      const float wi = in_smem ? w[i] : exp2f(ml[i].x - M);
+  for (int i0 = warp; i0 < n; i0 += kCombineWarps * kCombineBatch) {
+    float2 st[kCombineBatch];
+    float ov[kCombineBatch][V];
+#pragma unroll
+    for (int k = 0; k < kCombineBatch; ++k) {
+      const int i = i0 + k * kCombineWarps;
+      const int64_t r = row0 + static_cast<int64_t>(i < n ? i : 0) * rstride;
+      st[k] = i < n ? ml[r] : make_float2(-INFINITY, 0.f);
       if constexpr (V == 4) {
-        const float4 o4 = *reinterpret_cast<const float4 *>(po + static_cast<int64_t>(i) * D);
-        acc[0] += wi * o4.x;
-        acc[1] += wi * o4.y;
-        acc[2] += wi * o4.z;
-        acc[3] += wi * o4.w;
+        const float4 o4 = i < n ? *reinterpret_cast<const float4 *>(po + r * D)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        ov[k][0] = o4.x;
+        ov[k][1] = o4.y;
+        ov[k][2] = o4.z;
+        ov[k][3] = o4.w;
       } else {
-        const float2 o2 = *reinterpret_cast<const float2 *>(po + static_cast<int64_t>(i) * D);
-        acc[0] += wi * o2.x;
-        acc[1] += wi * o2.y;
+        const float2 o2 =
+            i < n ? *reinterpret_cast<const float2 *>(po + r * D) : make_float2(0.f, 0.f);
+        ov[k][0] = o2.x;
+        ov[k][1] = o2.y;
       }
+    }
+    float Mn = M;
+#pragma unroll
+    for (int k = 0; k < kCombineBatch; ++k) Mn = fmaxf(Mn, st[k].x);
+    if (Mn == -INFINITY) continue;  // nothing visible yet
+    const float cr = exp2f(M - Mn);  // 0 while M is -inf
+    Ls *= cr;
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] *= cr;
+#pragma unroll
+    for (int k = 0; k < kCombineBatch; ++k) {
+      const float w = exp2f(st[k].x - Mn);  // 0 for padding and empty pieces
+      Ls += w * st[k].y;
+#pragma unroll
+      for (int v = 0; v < V; ++v) acc[v] += w * ov[k][v];
+    }
+    M = Mn;
+  }
+  if (lane == 0) {
+    s_m[warp] = M;
+    s_l[warp] = Ls;
+  }
+#pragma unroll
+  for (int v = 0; v < V; ++v) s_o[warp][lane * V + v] = acc[v];
+  __syncthreads();
+  if (warp != 0) return;
+  float Mt = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kCombineWarps; ++w) Mt = fmaxf(Mt, s_m[w]);
+  float lt = 0.f, out_v[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) out_v[v] = 0.f;
+  if (Mt != -INFINITY) {
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) {
+      const float f = exp2f(s_m[w] - Mt);  // 0 for a warp that saw nothing
+      lt += f * s_l[w];
+#pragma unroll
+      for (int v = 0; v < V; ++v) out_v[v] += f * s_o[w][lane * V + v];
     }
   }
   // a sum that is not positive (no visible key, or a non-finite state from a
   // bad block) gives zeros
-  const bool good = ls > 0.f;
-  const float inv = good ? 1.f / ls : 0.f;
+  const bool good = lt > 0.f;
+  const float inv = good ? 1.f / lt : 0.f;
   typename E::T *out =
       static_cast<typename E::T *>(p.out) + b * p.out_row_stride + h * D + lane * V;
   if constexpr (V == 4) {
     *reinterpret_cast<uint2 *>(out) =
-        make_uint2(E::pack2(good ? acc[0] * inv : 0.f, good ? acc[1] * inv : 0.f),
-                   E::pack2(good ? acc[2] * inv : 0.f, good ? acc[3] * inv : 0.f));
+        make_uint2(E::pack2(good ? out_v[0] * inv : 0.f, good ? out_v[1] * inv : 0.f),
+                   E::pack2(good ? out_v[2] * inv : 0.f, good ? out_v[3] * inv : 0.f));
   } else {
     *reinterpret_cast<uint32_t *>(out) =
-        E::pack2(good ? acc[0] * inv : 0.f, good ? acc[1] * inv : 0.f);
+        E::pack2(good ? out_v[0] * inv : 0.f, good ? out_v[1] * inv : 0.f);
   }
 }
 
@@ -625,21 +791,12 @@ cudaError_t launch_typed(const DecodeArgs &a, const DecodeParams &p, cudaStream_
   auto kernel = decode_persistent_kernel<E, D, BOXR>;
   cudaError_t e = allow_dynamic_smem<decode_persistent_kernel<E, D, BOXR>>();
   if (e != cudaSuccess) return e;
-  // Items are at most S * Hkv * partitions; two CTAs per SM, four workers each.
-  const int64_t items = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads * a.num_partitions;
-  int64_t grid = (items + kWorkers - 1) / kWorkers;
-  if (grid > 2LL * a.num_sms) grid = 2LL * a.num_sms;
-  if (grid < 1) grid = 1;
-  e = launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, stream, p,
+  e = launch_pdl(kernel, dim3(static_cast<unsigned>(a.grid)), dim3(kThreads), smem, stream, p,
                  a.tm_k, a.tm_v);
-  if (e != cudaSuccess || a.num_partitions <= 1) return e;
+  if (e != cudaSuccess || !a.merge) return e;
   const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.num_q_heads;
-  const size_t wbytes = a.num_partitions <= kCombineMaxParts
-                            ? kCombineWarps * a.num_partitions * sizeof(float)
-                            : 0;
-  return launch_pdl(decode_combine_kernel<E, D>,
-                    dim3(static_cast<unsigned>((rows + kCombineWarps - 1) / kCombineWarps)),
-                    dim3(kCombineWarps * 32), wbytes, stream, p);
+  return launch_pdl(decode_combine_kernel<E, D>, dim3(static_cast<unsigned>(rows)),
+                    dim3(kCombineWarps * 32), 0, stream, p);
 }
 
 template <class E, int D>
@@ -656,7 +813,7 @@ cudaError_t launch_box(const DecodeArgs &a, const DecodeParams &p, cudaStream_t 
 // Largest dynamic shared memory the decode kernel needs for this shape, so
 // the host can reject shapes that cannot launch.
 size_t decode_smem_bytes(int head_dim, int num_seqs, int partition_size, int block_size) {
-  const int max_ids = partition_size / block_size + 2;
+  const int max_ids = (partition_size > 0 ? partition_size : kDecodeChunkCap) / block_size + 2;
   return head_dim == 128 ? DecodeSmem<128>::bytes(num_seqs, max_ids)
                          : DecodeSmem<64>::bytes(num_seqs, max_ids);
 }
@@ -681,9 +838,13 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
   p.scale_log2 = a.scale_log2;
   p.partition_size = a.partition_size;
   p.num_partitions = a.num_partitions;
-  p.max_ids = a.partition_size / a.block_size + 2;
+  p.balanced = a.partition_size == 0;
+  p.chunk_cap = kDecodeChunkCap;
+  p.num_workers = a.grid * kWorkers;
+  p.max_ids = (p.balanced ? kDecodeChunkCap : a.partition_size) / a.block_size + 2;
   p.ws_o = a.ws_o;
   p.ws_ml = a.ws_ml;
+  p.ws_pref = a.ws_pref;
   p.err = a.d_error;
   const bool bf = a.dtype == PA_BF16;
   if (a.head_dim == 128)

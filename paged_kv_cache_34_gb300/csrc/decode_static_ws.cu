@@ -72,10 +72,11 @@ pa_status pa_decode_static_ws(void *out, int64_t out_row_stride, const void *que
                               int64_t num_blocks, float scale, int32_t max_context_len,
                               int32_t partition_size, pa_dtype dtype, int32_t *d_error,
                               void *stream) {
-  // Pick a partition size whose workspace fits the array.  An explicit size
-  // that does not fit is an error; the automatic choice grows the partition
-  // (fewer partial results) until it fits.  A partition at least as long as
-  // max_context_len needs no workspace at all, so the search always ends.
+  // Pick a plan whose workspace fits the array.  An explicit partition size
+  // that does not fit is an error.  When the automatic plan does not fit,
+  // fixed partitions are used instead, grown (fewer partial results) until
+  // they fit; a partition at least as long as max_context_len needs no
+  // workspace at all, so the search always ends.
   int32_t part = 0;
   size_t need = 0;
   pa_status st = pa_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
@@ -83,6 +84,10 @@ pa_status pa_decode_static_ws(void *out, int64_t out_row_stride, const void *que
   if (st != PA_OK) return st;
   if (need > kStaticWorkspaceBytes) {
     if (partition_size != 0) return PA_ERR_WORKSPACE;
+    part = 64;
+    st = pa_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, part,
+                        &part, &need);
+    if (st != PA_OK) return st;
     while (need > kStaticWorkspaceBytes) {
       if (part >= max_context_len) return PA_ERR_WORKSPACE;  // unreachable: need is 0 there
       part *= 2;

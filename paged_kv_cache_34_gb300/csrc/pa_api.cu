@@ -91,7 +91,15 @@ bool valid_block_size(int bs) { return bs == 8 || bs == 16 || bs == 32 || bs == 
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Split-KV plan.  Auto: every worker warp (four per CTA, two CTAs per SM)
+// The automatic plan is the balanced split, as long as its positions fit in
+// int32 (else fixed partitions sized by plan_partition).
+bool use_balanced(int num_seqs, int num_kv_heads, int max_ctx, int partition_size) {
+  if (partition_size != 0 || max_ctx <= 0) return false;
+  const int64_t t = static_cast<int64_t>(num_seqs) * num_kv_heads * ((max_ctx + 15) / 16) * 16;
+  return t < (1LL << 30);
+}
+
+// Fixed split-KV plan.  Auto: every worker warp (four per CTA, two CTAs per SM)
 // should get about eight items of the largest possible batch, so the static
 // item schedule balances; a partition is at least 64 tokens (128 when eight
 // query heads share a KV head) so the partial states stay a few percent of the
@@ -174,13 +182,23 @@ pa_status pa_decode_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_h
   int sms = 0;
   cudaError_t e = current_num_sms(&sms);
   if (e != cudaSuccess) return cuda_fail(e);
-  const int P = plan_partition(num_seqs, num_q_heads, num_kv_heads, max_context_len,
-                               partition_size, sms);
-  const int64_t nparts = max_context_len > 0 ? (max_context_len + P - 1) / P : 1;
   size_t ws = 0;
-  if (nparts > 1) {
-    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * nparts;
-    ws = align256(rows * head_dim * sizeof(float)) + align256(rows * 2 * sizeof(float));
+  int P = 0;
+  if (use_balanced(num_seqs, num_kv_heads, max_context_len, partition_size)) {
+    // Balanced split (P reported as 0): pieces x G rows of partial state,
+    // plus the per-sequence prefix sums for the merge kernel.
+    const pa::DecodeBalance d = pa::decode_balance(num_seqs, num_kv_heads, max_context_len, sms);
+    const size_t rows = static_cast<size_t>(d.pieces) * (num_q_heads / num_kv_heads);
+    ws = align256(rows * head_dim * sizeof(float)) + align256(rows * 2 * sizeof(float)) +
+         align256((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t));
+  } else {
+    P = plan_partition(num_seqs, num_q_heads, num_kv_heads, max_context_len, partition_size,
+                       sms);
+    const int64_t nparts = max_context_len > 0 ? (max_context_len + P - 1) / P : 1;
+    if (nparts > 1) {
+      const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * nparts;
+      ws = align256(rows * head_dim * sizeof(float)) + align256(rows * 2 * sizeof(float));
+    }
   }
   if (partition_size_out) *partition_size_out = P;
   if (workspace_bytes_out) *workspace_bytes_out = ws;
@@ -222,7 +240,8 @@ pa_status pa_decode(void *out, int64_t out_row_stride, const void *query, int64_
   pa_status st = pa_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
                                 partition_size, &P, &need);
   if (st != PA_OK) return st;
-  const int32_t nparts = max_context_len > 0 ? (max_context_len + P - 1) / P : 1;
+  const bool balanced = P == 0;
+  const int32_t nparts = balanced ? 0 : (max_context_len > 0 ? (max_context_len + P - 1) / P : 1);
   if (need > 0 && (!workspace || workspace_bytes < need ||
                    (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
     return PA_ERR_WORKSPACE;
@@ -249,17 +268,39 @@ pa_status pa_decode(void *out, int64_t out_row_stride, const void *query, int64_
   a.num_partitions = nparts;
   a.ws_o = nullptr;
   a.ws_ml = nullptr;
-  if (need > 0) {
-    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * nparts;
-    a.ws_o = static_cast<float *>(workspace);
-    a.ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                        align256(rows * head_dim * sizeof(float)));
+  a.ws_pref = nullptr;
+  cudaError_t e = current_num_sms(&a.num_sms);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (balanced) {
+    const pa::DecodeBalance d =
+        pa::decode_balance(num_seqs, num_kv_heads, max_context_len, a.num_sms);
+    a.grid = d.grid;
+    a.merge = true;
+    const size_t rows = static_cast<size_t>(d.pieces) * (num_q_heads / num_kv_heads);
+    char *w = static_cast<char *>(workspace);
+    a.ws_o = reinterpret_cast<float *>(w);
+    w += align256(rows * head_dim * sizeof(float));
+    a.ws_ml = reinterpret_cast<float *>(w);
+    w += align256(rows * 2 * sizeof(float));
+    a.ws_pref = reinterpret_cast<int32_t *>(w);
+  } else {
+    // Items are at most S * Hkv * partitions; two CTAs per SM, four workers each.
+    const int64_t items = static_cast<int64_t>(num_seqs) * num_kv_heads * nparts;
+    int64_t grid = (items + pa::kDecodeWarps - 1) / pa::kDecodeWarps;
+    if (grid > 2LL * a.num_sms) grid = 2LL * a.num_sms;
+    if (grid < 1) grid = 1;
+    a.grid = static_cast<int>(grid);
+    a.merge = nparts > 1;
+    if (need > 0) {
+      const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * nparts;
+      a.ws_o = static_cast<float *>(workspace);
+      a.ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                          align256(rows * head_dim * sizeof(float)));
+    }
   }
   a.d_error = d_error;
   a.dtype = dtype;
   a.box_rows = block_size < pa::kDecodeSub ? block_size : pa::kDecodeSub;
-  cudaError_t e = current_num_sms(&a.num_sms);
-  if (e != cudaSuccess) return cuda_fail(e);
   // The item schedule keeps per-sequence prefix sums in shared memory.
   if (pa::decode_smem_bytes(head_dim, num_seqs, P, block_size) > 227 * 1024)
     return PA_ERR_UNSUPPORTED;

@@ -29,6 +29,29 @@ cudaError_t launch_reshape_and_cache(const ReshapeArgs &a, cudaStream_t stream);
 constexpr int kDecodeWarps = 4;     // consumer warps (independent workers) per CTA
 constexpr int kDecodeSub = 16;      // tokens per worker per pipeline stage
 constexpr int kDecodeMaxGroup = 8;  // query heads per KV head
+constexpr int kDecodeChunkCap = 2048;  // balanced schedule: most tokens per chunk
+
+// Balanced decode schedule sizes, shared by the planner and the launcher:
+// the grid (CTAs) and the most pieces (workspace rows per query head) the
+// split can produce for max_context_len.
+struct DecodeBalance {
+  int grid, workers;
+  int64_t pieces;  // units + chunks
+};
+inline DecodeBalance decode_balance(int num_seqs, int num_kv_heads, int max_ctx, int num_sms) {
+  DecodeBalance d;
+  const int64_t t_max = static_cast<int64_t>(num_seqs) * num_kv_heads * ((max_ctx + 15) / 16) * 16;
+  int64_t grid = (t_max / kDecodeSub + kDecodeWarps - 1) / kDecodeWarps;
+  if (grid > 2LL * num_sms) grid = 2LL * num_sms;
+  if (grid < 1) grid = 1;
+  d.grid = static_cast<int>(grid);
+  d.workers = d.grid * kDecodeWarps;
+  const int64_t per = static_cast<int64_t>(d.workers) * kDecodeChunkCap;
+  const int64_t k = t_max > 0 ? (t_max + per - 1) / per : 1;
+  const int64_t chunks = k * d.workers;
+  d.pieces = static_cast<int64_t>(num_seqs) * num_kv_heads + chunks;
+  return d;
+}
 
 struct DecodeArgs {
   void *out;
@@ -42,9 +65,12 @@ struct DecodeArgs {
   int32_t num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
   int64_t num_blocks;
   float scale_log2;  // scale * log2(e)
-  int32_t max_context_len, partition_size, num_partitions;
-  float *ws_o;   // [S, Hq, num_partitions, D]      (num_partitions > 1)
-  float *ws_ml;  // [S, Hq, num_partitions, 2]      (max in log2 units, sum)
+  int32_t max_context_len, partition_size, num_partitions;  // partition_size 0: balanced
+  int grid;        // decode CTAs
+  bool merge;      // launch the merge kernel
+  float *ws_o;     // fixed: [S, Hq, num_partitions, D]; balanced: [pieces, G, D]
+  float *ws_ml;    // same rows, 2 floats: max (log2 units), sum
+  int32_t *ws_pref;  // balanced: [S + 1] prefix sums for the merge kernel
   int32_t *d_error;
   pa_dtype dtype;
   CUtensorMap tm_k, tm_v;  // pool maps, box (64, 1, box_rows), 128B swizzle

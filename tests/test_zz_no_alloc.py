@@ -99,14 +99,23 @@ def test_two_calls_in_a_row_match_pa_decode():
     assert torch.equal(again.view(torch.int16), out_a.view(torch.int16))
 
 
-def test_automatic_plan_is_lengthened_to_fit():
+def test_automatic_plan_falls_back_to_fixed_partitions_that_fit():
     lib = _lib()
-    x = inputs("long-context-decode", lengths=[131072, 120000, 90000, 131000])
+    # 512 short sequences with 8 query heads per KV head: the automatic
+    # (balanced) plan keeps one partial state per query head per piece, more
+    # than the array holds, so the call switches to fixed partitions grown
+    # until they fit.
+    lengths = [64 + (37 * i) % 400 for i in range(512)]
+    x = inputs("long-context-decode", num_seqs=512, lengths=lengths)
     _, need = pa.pa_decode_plan(x.num_seqs, x.num_q_heads, x.num_kv_heads, x.head_dim,
                                 x.max_context_len, 0)
-    assert need > STATIC_BYTES  # the default plan would not fit
+    assert need > STATIC_BYTES  # the automatic plan would not fit
     check(lib, x, partition_size=0)
     # an explicit partition size that does not fit is refused, not run
+    y = inputs("long-context-decode", lengths=[131072, 120000, 90000, 131000])
+    _, need64 = pa.pa_decode_plan(y.num_seqs, y.num_q_heads, y.num_kv_heads, y.head_dim,
+                                  y.max_context_len, 64)
+    assert need64 > STATIC_BYTES
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out = torch.empty_like(x.q)
-    assert static_decode(lib, x, out, 64, err) == 5  # PA_ERR_WORKSPACE
+    out = torch.empty_like(y.q)
+    assert static_decode(lib, y, out, 64, err) == 5  # PA_ERR_WORKSPACE
