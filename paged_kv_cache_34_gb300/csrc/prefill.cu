@@ -85,8 +85,7 @@ enum {
   kKVEmpty = kKVFull + kKVBufs,
   kSFull = kKVEmpty + kKVBufs,
   kPFull = kSFull + 2,
-  kPVDone = kPFull + 2,
-  kQEmpty = kPVDone + 2,
+  kQEmpty = kPFull + 2,
   kOFull = kQEmpty + 1,     // per query tile and item: its last PV is done
   kOFree = kOFull + 2,      // per query tile: the epilogue has read O
   kLFull = kOFree + 2,      // per query tile: the softmax has left its row sums
@@ -479,7 +478,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 8; ++k)
             umma_f16_ts(tbase + 256 + t * 128, tbase + t * 128 + 8 * k, vd + ((k * 2048) >> 4),
                         id_pv, k > 0 ? 1u : acc0);
-          umma_commit(bar(kPVDone + t));
         }
         __syncwarp();
       };
@@ -568,9 +566,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (!ok) break;
-          if (kt + 2 == it.nkv) commit(kQEmpty);  // the item's last QK
-          commit(kKVEmpty + v_slot(kbase + kt));
-          if (more) commit(kKVEmpty + k_slot(kbase + kt + 1));
+          // One elected block for the step's releases: V_kt, K_{kt+1} and,
+          // after the item's last QK, Q.
+          if (elect_one()) {
+            if (kt + 2 == it.nkv) umma_commit(bar(kQEmpty));
+            umma_commit(bar(kKVEmpty + v_slot(kbase + kt)));
+            if (more) umma_commit(bar(kKVEmpty + k_slot(kbase + kt + 1)));
+          }
+          __syncwarp();
         }
         kbase += it.nkv;
         prev_nkv[0] = it.nkv_t[0];
@@ -657,7 +660,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_tm = tbase + lane_addr + 256 + t * 128;
     const float sl = p.scale_log2;
     int n = 0;       // S phases of this query tile (QK results and empty commits)
-    int pn = 0;      // PVs of this query tile
     bool ok = true;
     for (int j = 0;; ++j) {
       int x;
@@ -672,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int lim = min(it.lim_base + it.row0[t] + r, it.L - 1);  // last visible key
       float m_ref = -INFINITY, l = 0.f;
-      for (int kt = 0; kt < my_nkv; ++kt, ++n, ++pn) {
+      for (int kt = 0; kt < my_nkv; ++kt, ++n) {
         ok = mbar_wait_bounded(bar(kSFull + t), n & 1);
         if (!ok) break;
         tc_fence_after();
@@ -727,10 +729,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
         if (kt >= 1 && __any_sync(0xffffffffu, raise_max)) {
-          // O holds the sum through PV(kt-1): wait for it, then rescale.
-          ok = mbar_wait_bounded(bar(kPVDone + t), (pn - 1) & 1);
-          if (!ok) break;
-          tc_fence_after();
+          // O holds exactly the sum through PV(kt-1): S(kt) being complete
+          // means QK(kt) ran, and it was issued after PV(kt-1).  Rescale it.
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t o[32];
