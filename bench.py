@@ -3,8 +3,9 @@
 One step = one pass of the path over one batch of the llama7b-decode workload
 (8 sequences, context ~ U[512, 2048], 32 heads, head_dim 128, block_size 16,
 8192-block pool, bf16): write each sequence's new token into the pool through
-slot_mapping, then paged decode over the whole context (split-KV partitions
-plus the log-sum-exp combine).  The headline value is the K/V bytes the step
+slot_mapping, then paged decode over the whole context (split-KV plus the
+log-sum-exp merge) -- one pa_decode_write call, the public entry point for a
+decode step.  The headline value is the K/V bytes the step
 must read from HBM divided by the step's device time, with L2 flushed between
 timed steps.  The same line carries two secondary measurements (the
 packed-prefill workload in TFLOP/s and the long-context decode workload in
@@ -190,13 +191,13 @@ def measured_peaks():
 # the steps
 # ---------------------------------------------------------------------------
 def decode_step_fn(pa, x, out, ws, stream):
+    """One decode step through the public API: pa_decode_write (this step's
+    cache write, then the decode, as one call)."""
     def step():
-        if x.slot_mapping.numel():
-            pa.pa_reshape_and_cache(x.k_new, x.v_new, x.k_pool, x.v_pool, x.slot_mapping,
-                                    stream=stream)
-        pa.pa_decode(out, x.q, x.k_pool, x.v_pool, x.block_table, x.context_lens,
-                     scale=x.scale, max_context_len=x.max_context_len,
-                     partition_size=x.partition_size, workspace=ws, stream=stream)
+        pa.pa_decode_write(out, x.q, x.k_new, x.v_new, x.k_pool, x.v_pool, x.slot_mapping,
+                           x.block_table, x.context_lens, scale=x.scale,
+                           max_context_len=x.max_context_len, partition_size=x.partition_size,
+                           workspace=ws, stream=stream)
     return step
 
 
@@ -256,7 +257,7 @@ def bench_prefill(pa, W, steps, warmup, flush_buf, stream):
 
 def e2e_decode(pa, W, name, steps, warmup, stream):
     """Through host buffers: each step copies its inputs from pinned host
-    memory, runs write + decode, and copies the output back."""
+    memory, runs write + decode (pa_decode_write), and copies the output back."""
     x = W.make_inputs(name, device="cuda")
     host = {k: getattr(x, k).cpu().pin_memory() for k in
             ("q", "k_new", "v_new", "slot_mapping", "context_lens", "block_table")}
@@ -270,12 +271,10 @@ def e2e_decode(pa, W, name, steps, warmup, stream):
     def step():
         for k in host:
             dev[k].copy_(host[k], non_blocking=True)
-        if dev["slot_mapping"].numel():
-            pa.pa_reshape_and_cache(dev["k_new"], dev["v_new"], x.k_pool, x.v_pool,
-                                    dev["slot_mapping"], stream=stream)
-        pa.pa_decode(out_d, dev["q"], x.k_pool, x.v_pool, dev["block_table"],
-                     dev["context_lens"], scale=x.scale, max_context_len=x.max_context_len,
-                     partition_size=x.partition_size, workspace=ws, stream=stream)
+        pa.pa_decode_write(out_d, dev["q"], dev["k_new"], dev["v_new"], x.k_pool, x.v_pool,
+                           dev["slot_mapping"], dev["block_table"], dev["context_lens"],
+                           scale=x.scale, max_context_len=x.max_context_len,
+                           partition_size=x.partition_size, workspace=ws, stream=stream)
         out_h.copy_(out_d, non_blocking=True)
     for _ in range(warmup):
         step()
@@ -474,6 +473,7 @@ def main():
         "config": {"workload": HEADLINE, "sequences_per_gpu": x.num_seqs,
                    "context": "U[512,2048]", "heads": "32/32", "head_dim": 128,
                    "block_size": 16, "pool_blocks": 8192,
+                   "step": "pa_decode_write: cache write of the 8 new tokens + decode",
                    "split_kv": "balanced across workers" if part == 0 else
                                f"fixed partitions of {part} tokens ({nparts} for the longest)",
                    "kv_bytes_per_step": kv,

@@ -10,6 +10,10 @@
  *   pa_prefill_varlen     causal attention for cu_seqlens-packed queries
  *                         against the paged cache.
  *
+ * pa_decode_write is one decode step as one call (the write, then the
+ * decode, overlapped); pa_decode_plan sizes pa_decode's workspace;
+ * pa_decode_static_ws is pa_decode without a caller-supplied workspace.
+ *
  * Sources (web pages on paged KV caches, cited by page and section):
  *   [SKILL] cannbot-skills "model-infer-kvcache" skill page: §3.1 physical
  *           layout and logical mapping, §3.3 slot_mapping, §3.4
@@ -128,13 +132,19 @@ pa_status pa_reshape_and_cache(const void *key, const void *value,
 /*
  * pa_decode_plan -- the split-KV plan pa_decode will use.
  *
- * Long contexts are split into partitions of *partition_size_out tokens; each
- * partition's softmax state (max, sum, unnormalised output) is combined by
- * log-sum-exp.  partition_size == 0 picks a size from max_context_len, the
- * batch shape and the current device's SM count; a non-zero value must be a
- * positive multiple of 16 and is used as given.  *workspace_bytes_out is the
- * device workspace pa_decode needs (0 when no sequence can span two
- * partitions).  Host-only; enqueues nothing.
+ * Long contexts are split into pieces; each piece's softmax state (max, sum,
+ * unnormalised output) is combined by log-sum-exp ([SKILL] §3.1; the pages'
+ * split-KV partitions).  A non-zero partition_size must be a positive
+ * multiple of 16: every (sequence, KV head) is cut into partitions of that
+ * many tokens and *partition_size_out returns it.  partition_size == 0 is the
+ * automatic plan: the balanced split, which cuts the batch's whole token
+ * stream into equal shares, one per worker of the decode grid (so no worker
+ * waits on a long sequence while others idle); *partition_size_out is then 0.
+ * (The automatic plan falls back to fixed partitions sized from
+ * max_context_len, the batch shape and the SM count when the batch's token
+ * count does not fit in int32.)  *workspace_bytes_out is the device
+ * workspace pa_decode needs (0 when no context can be split).  Host-only;
+ * enqueues nothing.
  */
 pa_status pa_decode_plan(int32_t num_seqs, int32_t num_q_heads,
                          int32_t num_kv_heads, int32_t head_dim,
@@ -230,6 +240,41 @@ pa_status pa_prefill_varlen(void *out, int64_t out_row_stride,
                             int32_t block_size, int64_t num_blocks,
                             float scale, int32_t causal, pa_dtype dtype,
                             int32_t *d_error, void *stream);
+
+/*
+ * pa_decode_write -- one decode step: the new tokens' cache write, then the
+ * decode that reads them.
+ *
+ * Defines ([SKILL] §3.6 decode data flow: write the step's K/V through
+ * slot_mapping, then attend with actual_seq_lengths_kv = kv_len + 1;
+ * [LQNN] §4.1–4.7 the decode loop): exactly
+ *     pa_reshape_and_cache(key, value, kv_row_stride, key_cache, value_cache,
+ *                          slot_mapping, num_new_tokens, ...);
+ *     pa_decode(out, ..., key_cache, value_cache, block_table, ...);
+ * on `stream`, with the same arguments, meanings, layouts and device error
+ * bits as those two calls (key/value: [num_new_tokens, num_kv_heads,
+ * head_dim] rows at kv_row_stride elements apart).  Every argument of both
+ * is checked before either is enqueued.  What the pair does not allow: the
+ * decode kernel reads context_lens, block_table and query, and builds its
+ * schedule, while the write is still running, waiting for the write only
+ * before its first K/V load -- so the write's time is hidden behind the
+ * decode's start-up.  num_new_tokens == 0 is a plain pa_decode.
+ */
+pa_status pa_decode_write(void *out, int64_t out_row_stride,
+                          const void *query, int64_t q_row_stride,
+                          const void *key, const void *value,
+                          int64_t kv_row_stride, void *key_cache,
+                          void *value_cache, const int64_t *slot_mapping,
+                          int32_t num_new_tokens, const int32_t *block_table,
+                          int64_t block_table_stride,
+                          int32_t max_blocks_per_seq,
+                          const int32_t *context_lens, int32_t num_seqs,
+                          int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t head_dim, int32_t block_size,
+                          int64_t num_blocks, float scale,
+                          int32_t max_context_len, int32_t partition_size,
+                          void *workspace, size_t workspace_bytes,
+                          pa_dtype dtype, int32_t *d_error, void *stream);
 
 /*
  * pa_decode_static_ws -- pa_decode for callers that cannot allocate.

@@ -21,7 +21,7 @@ import threading
 
 import torch
 
-__all__ = ["pa_reshape_and_cache", "pa_decode", "pa_decode_plan",
+__all__ = ["pa_reshape_and_cache", "pa_decode", "pa_decode_plan", "pa_decode_write",
            "pa_prefill_varlen", "PaError", "library", "DEVERR_SLOT",
            "DEVERR_BLOCK_ID", "DEVERR_CU_SEQLENS", "DEVERR_CONTEXT",
            "DEVERR_TIMEOUT", "LIB_PATH"]
@@ -72,6 +72,10 @@ def library(path: str | None = None):
         lib.pa_decode.argtypes = [V, I64, V, I64, V, V, V, I64, I32, V, I32, I32, I32, I32,
                                   I32, I64, F, I32, I32, V, SZ, c.c_int, V, V]
         lib.pa_decode.restype = c.c_int
+        lib.pa_decode_write.argtypes = [V, I64, V, I64, V, V, I64, V, V, V, I32, V, I64, I32,
+                                        V, I32, I32, I32, I32, I32, I64, F, I32, I32, V, SZ,
+                                        c.c_int, V, V]
+        lib.pa_decode_write.restype = c.c_int
         lib.pa_prefill_varlen.argtypes = [V, I64, V, I64, V, V, V, I64, I32, V, V, I32, I32,
                                           I32, I32, I32, I32, I32, I32, I64, F, I32, c.c_int,
                                           V, V]
@@ -161,6 +165,39 @@ def pa_decode(out, query, key_cache, value_cache, block_table, context_lens, *, 
                        _ptr(workspace), wbytes, _DTYPE[query.dtype], _ptr(d_error),
                        _stream(stream))
     _check(lib, st, "pa_decode")
+    return out
+
+
+def pa_decode_write(out, query, key, value, key_cache, value_cache, slot_mapping, block_table,
+                    context_lens, *, scale, max_context_len, partition_size=0, workspace=None,
+                    d_error=None, stream=None, lib=None):
+    """One decode step in one call: pa_reshape_and_cache(key, value, ...,
+    slot_mapping) then pa_decode(...), the decode overlapping the write.
+    Arguments as for those two functions."""
+    lib = lib or library()
+    s, hq, d = query.shape
+    nb, bs, hkv, _ = key_cache.shape
+    ks = _rows(key, "key")
+    if _rows(value, "value") != ks:
+        raise ValueError("key and value must share a row stride")
+    if not key_cache.is_contiguous() or not value_cache.is_contiguous():
+        raise ValueError("caches must be contiguous [num_blocks, block_size, Hkv, D]")
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    if block_table.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_table and context_lens must be int32")
+    P, need = pa_decode_plan(s, hq, hkv, d, max_context_len, partition_size, lib=lib)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.pa_decode_write(_ptr(out), _rows(out, "out"), _ptr(query), _rows(query, "query"),
+                             _ptr(key), _ptr(value), ks, _ptr(key_cache), _ptr(value_cache),
+                             _ptr(slot_mapping), key.shape[0], _ptr(block_table),
+                             block_table.stride(0), block_table.shape[1], _ptr(context_lens), s,
+                             hq, hkv, d, bs, nb, float(scale), int(max_context_len), P,
+                             _ptr(workspace), wbytes, _DTYPE[query.dtype], _ptr(d_error),
+                             _stream(stream))
+    _check(lib, st, "pa_decode_write")
     return out
 
 

@@ -88,6 +88,7 @@ struct DecodeParams {
   int32_t balanced, chunk_cap, num_workers;  // balanced schedule (see above)
   float *ws_o, *ws_ml;
   int32_t *ws_pref;  // balanced: the prefix sums, for the merge kernel
+  int32_t after_write;  // launched directly after this step's cache write
   int32_t *err;
 };
 
@@ -130,12 +131,18 @@ __device__ __forceinline__ Item decode_item(int i, const int *pref, const int *l
   m.L = len[lo];
   const int np = m.L > 0 ? (m.L + P - 1) / P : 1;
   const int rem = i - pref[lo];
+#if PA_DECODE_PART_MAJOR
+  m.part = rem / hkv;
+  m.g = rem - m.part * hkv;
+#else
   m.g = rem / np;
   m.part = rem - m.g * np;
+#endif
   m.start = m.part * P;
   m.end = min(m.start + P, m.L);
   if (m.end < m.start) m.end = m.start;
   (void)hkv;
+  (void)np;
   return m;
 }
 
@@ -248,7 +255,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int P = p.partition_size;
   const int nseq = p.num_seqs;
-  griddep_wait();  // inputs (e.g. this step's cache write) come from earlier kernels
+  // Inputs come from earlier kernels.  Launched right after this step's
+  // cache write (`after_write`), only the K/V rows can be the write's
+  // output: the kernel then reads context_lens, block_table and q at once
+  // and waits only before its first K/V load (in the producer below).
+  if (!p.after_write) griddep_wait();
   griddep_launch_dependents();
 
   if (tid == 0) {
@@ -357,6 +368,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       prefetch(0);
       promote();
     }
+    if (p.after_write) griddep_wait();  // the cache write has landed
     const int *ids = s_ids;
     for (int c = 0;; ++c) {
       const int s = c % kStages;
@@ -845,6 +857,7 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
   p.ws_o = a.ws_o;
   p.ws_ml = a.ws_ml;
   p.ws_pref = a.ws_pref;
+  p.after_write = a.after_write ? 1 : 0;
   p.err = a.d_error;
   const bool bf = a.dtype == PA_BF16;
   if (a.head_dim == 128)

@@ -138,12 +138,18 @@ const char *pa_status_string(pa_status s) {
   return "unknown pa_status";
 }
 
-pa_status pa_reshape_and_cache(const void *key, const void *value, int64_t kv_row_stride,
-                               void *key_cache, void *value_cache,
-                               const int64_t *slot_mapping, int32_t num_tokens,
-                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                               int64_t num_blocks, pa_dtype dtype, int32_t *d_error,
-                               void *stream) {
+}  // extern "C"
+
+namespace {
+
+// Validates a cache write and fills its launch arguments; enqueues nothing.
+// *empty is set when there is nothing to write.
+pa_status prepare_write(const void *key, const void *value, int64_t kv_row_stride,
+                        void *key_cache, void *value_cache, const int64_t *slot_mapping,
+                        int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t block_size, int64_t num_blocks, pa_dtype dtype, int32_t *d_error,
+                        pa::ReshapeArgs *out, bool *empty) {
+  *empty = true;
   if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0)
     return PA_ERR_SHAPE;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
@@ -166,9 +172,31 @@ pa_status pa_reshape_and_cache(const void *key, const void *value, int64_t kv_ro
   a.row_bytes = row * 2;
   a.num_slots = num_blocks * block_size;
   a.d_error = d_error;
-  cudaError_t e = current_num_sms(&a.num_sms);
+  a.num_sms = 0;  // filled in at launch
+  *out = a;
+  *empty = false;
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_reshape_and_cache(const void *key, const void *value, int64_t kv_row_stride,
+                               void *key_cache, void *value_cache,
+                               const int64_t *slot_mapping, int32_t num_tokens,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                               int64_t num_blocks, pa_dtype dtype, int32_t *d_error,
+                               void *stream) {
+  pa::ReshapeArgs w;
+  bool empty = true;
+  const pa_status st = prepare_write(key, value, kv_row_stride, key_cache, value_cache,
+                                     slot_mapping, num_tokens, num_kv_heads, head_dim, block_size,
+                                     num_blocks, dtype, d_error, &w, &empty);
+  if (st != PA_OK || empty) return st;
+  cudaError_t e = current_num_sms(&w.num_sms);
   if (e != cudaSuccess) return cuda_fail(e);
-  e = pa::launch_reshape_and_cache(a, static_cast<cudaStream_t>(stream));
+  e = pa::launch_reshape_and_cache(w, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
@@ -205,14 +233,21 @@ pa_status pa_decode_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_h
   return PA_OK;
 }
 
-pa_status pa_decode(void *out, int64_t out_row_stride, const void *query, int64_t q_row_stride,
-                    const void *key_cache, const void *value_cache, const int32_t *block_table,
-                    int64_t block_table_stride, int32_t max_blocks_per_seq,
-                    const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
-                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                    int64_t num_blocks, float scale, int32_t max_context_len,
-                    int32_t partition_size, void *workspace, size_t workspace_bytes,
-                    pa_dtype dtype, int32_t *d_error, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// pa_decode, optionally preceded by the step's cache write `write` (launched
+// first, after every check has passed, so an error enqueues nothing).
+pa_status decode_call(void *out, int64_t out_row_stride, const void *query, int64_t q_row_stride,
+                      const void *key_cache, const void *value_cache, const int32_t *block_table,
+                      int64_t block_table_stride, int32_t max_blocks_per_seq,
+                      const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                      int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                      int64_t num_blocks, float scale, int32_t max_context_len,
+                      int32_t partition_size, void *workspace, size_t workspace_bytes,
+                      pa_dtype dtype, int32_t *d_error, void *stream,
+                      const pa::ReshapeArgs *write) {
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq < 0 || max_context_len < 0 ||
       partition_size < 0)
@@ -311,8 +346,59 @@ pa_status pa_decode(void *out, int64_t out_row_stride, const void *query, int64_
       !encode_rows_map(&a.tm_v, value_cache, dtype, head_dim, num_kv_heads, rows, row_stride,
                        a.box_rows))
     return cuda_fail(cudaErrorInvalidValue);
+  a.after_write = false;
+  if (write) {
+    pa::ReshapeArgs w = *write;
+    w.num_sms = a.num_sms;
+    e = pa::launch_reshape_and_cache(w, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    a.after_write = true;
+  }
   e = pa::launch_decode(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_decode(void *out, int64_t out_row_stride, const void *query, int64_t q_row_stride,
+                    const void *key_cache, const void *value_cache, const int32_t *block_table,
+                    int64_t block_table_stride, int32_t max_blocks_per_seq,
+                    const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                    int64_t num_blocks, float scale, int32_t max_context_len,
+                    int32_t partition_size, void *workspace, size_t workspace_bytes,
+                    pa_dtype dtype, int32_t *d_error, void *stream) {
+  return decode_call(out, out_row_stride, query, q_row_stride, key_cache, value_cache,
+                     block_table, block_table_stride, max_blocks_per_seq, context_lens, num_seqs,
+                     num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                     max_context_len, partition_size, workspace, workspace_bytes, dtype, d_error,
+                     stream, nullptr);
+}
+
+pa_status pa_decode_write(void *out, int64_t out_row_stride, const void *query,
+                          int64_t q_row_stride, const void *key, const void *value,
+                          int64_t kv_row_stride, void *key_cache, void *value_cache,
+                          const int64_t *slot_mapping, int32_t num_new_tokens,
+                          const int32_t *block_table, int64_t block_table_stride,
+                          int32_t max_blocks_per_seq, const int32_t *context_lens,
+                          int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t head_dim, int32_t block_size, int64_t num_blocks, float scale,
+                          int32_t max_context_len, int32_t partition_size, void *workspace,
+                          size_t workspace_bytes, pa_dtype dtype, int32_t *d_error,
+                          void *stream) {
+  pa::ReshapeArgs w;
+  bool empty = true;
+  const pa_status st = prepare_write(key, value, kv_row_stride, key_cache, value_cache,
+                                     slot_mapping, num_new_tokens, num_kv_heads, head_dim,
+                                     block_size, num_blocks, dtype, d_error, &w, &empty);
+  if (st != PA_OK) return st;
+  return decode_call(out, out_row_stride, query, q_row_stride, key_cache, value_cache,
+                     block_table, block_table_stride, max_blocks_per_seq, context_lens, num_seqs,
+                     num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                     max_context_len, partition_size, workspace, workspace_bytes, dtype, d_error,
+                     stream, empty ? nullptr : &w);
 }
 
 pa_status pa_prefill_varlen(void *out, int64_t out_row_stride, const void *query,

@@ -71,6 +71,10 @@ struct DecodeArgs {
   float *ws_o;     // fixed: [S, Hq, num_partitions, D]; balanced: [pieces, G, D]
   float *ws_ml;    // same rows, 2 floats: max (log2 units), sum
   int32_t *ws_pref;  // balanced: [S + 1] prefix sums for the merge kernel
+  // The previous kernel in the stream is this library's cache write, which
+  // writes only K/V pool rows: the decode kernel may read everything else
+  // before waiting for it.
+  bool after_write;
   int32_t *d_error;
   pa_dtype dtype;
   CUtensorMap tm_k, tm_v;  // pool maps, box (64, 1, box_rows), 128B swizzle

@@ -116,6 +116,32 @@ def test_reshape_host_validation(lib):
     assert f(FAKE, FAKE, 256, FAKE, FAKE, FAKE, 3, 2, 64, 16, 8, 5, None, None) == 3
 
 
+def decode_write_call(lib, **kw):
+    a = dict(out=FAKE, q=FAKE, q_stride=8 * 128, k=FAKE, v=FAKE, kv_stride=2 * 128, kc=FAKE,
+             vc=FAKE, slots=FAKE, n=4, bt=FAKE, bt_stride=16, mbps=16, ctx=FAKE, s=4, hq=8,
+             hkv=2, d=128, bs=16, nb=64, scale=0.125, maxctx=100, part=0, dtype=0)
+    a.update(kw)
+    return lib.pa_decode_write(a["out"], a["q_stride"], a["q"], a["q_stride"], a["k"], a["v"],
+                               a["kv_stride"], a["kc"], a["vc"], a["slots"], a["n"], a["bt"],
+                               a["bt_stride"], a["mbps"], a["ctx"], a["s"], a["hq"], a["hkv"],
+                               a["d"], a["bs"], a["nb"], a["scale"], a["maxctx"], a["part"],
+                               None, 0, a["dtype"], None, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(kv_stride=100), 2),      # the write's row stride is below Hkv*D
+    (dict(slots=None), 1),         # the write's slot_mapping is missing
+    (dict(k=MISALIGNED), 4),       # the write's key is misaligned
+    (dict(hkv=3), 2),              # the decode's Hq % Hkv != 0
+    (dict(d=96), 3),               # the decode's head_dim is not built
+    (dict(q=None), 1),             # the decode's query is missing
+    (dict(part=100), 2),           # the decode's partition is not a multiple of 16
+])
+def test_decode_write_checks_both_halves_before_enqueueing(lib, kw, status):
+    # every case fails on the host, before any CUDA call
+    assert decode_write_call(lib, **kw) == status
+
+
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         pa.library(str(tmp_path / "libpa.so"))
