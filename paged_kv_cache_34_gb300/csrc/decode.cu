@@ -261,7 +261,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   // and waits only before its first K/V load (in the producer below).
   if (!p.after_write) griddep_wait();
   griddep_launch_dependents();
-
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(full + s), 1);
@@ -688,11 +687,13 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
   constexpr int V = D / 32;  // output elements per lane
   __shared__ float s_m[kCombineWarps], s_l[kCombineWarps];
   __shared__ float s_o[kCombineWarps][D];
-  griddep_wait();  // the partial states of the decode kernel
-  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x / p.hq, h = blockIdx.x - b * p.hq;
+  // context_lens is an input of the decode kernel, not its output: read it
+  // while the decode kernel is still running.
   const int L = checked_context_len(__ldg(p.context_lens + b), p.capacity, p.max_ctx, p.err, false);
+  griddep_wait();  // the partial states of the decode kernel
+  griddep_launch_dependents();
   int n;
   int64_t row0, rstride;
   if (p.balanced) {
