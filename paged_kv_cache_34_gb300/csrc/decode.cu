@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const bool feeder = lane < kWorkers;
     int cur = 0, endt = 0, gq = 0, sel = 0, lblk = 0, off = 0;
     int nstart = 0, nend = 0, ng = 0, nbuf = 0;
-    bool act = false, have_next = false;
+    bool act = false, have_next = false, want_next = false;
     Cursor pc = first_cursor(sc, blockIdx.x * kWorkers + lane);
     // Finds this worker's next piece with tokens (items of empty sequences
     // carry none: the worker writes their zeros itself) and starts copying
@@ -350,7 +350,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       nbuf = buf;
     };
-    // Makes the prefetched piece current and prefetches the one after it.
+    // Makes the prefetched piece current; the one after it is prefetched
+    // once this piece's first copies are issued.
     auto promote = [&]() {
       act = have_next;
       if (!act) return;
@@ -361,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       sel = nbuf;
       lblk = 0;
       off = nstart % bs;
-      prefetch(nbuf ^ 1);
+      want_next = true;  // prefetch the next piece once this one's first copies are out
     };
     if (feeder) {
       prefetch(0);
@@ -448,6 +449,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             tma_load_3d(kdst + h * kHalfBytes + o, &tmk, bar, h * 64, gq, rows[k]);
             tma_load_3d(vdst + h * kHalfBytes + o, &tmv, bar, h * 64, gq, rows[k]);
           }
+        }
+        if (want_next) {
+          want_next = false;
+          prefetch(sel ^ 1);
         }
       }
     }
