@@ -233,7 +233,7 @@ __device__ __forceinline__ void load_q(uint32_t (&qf)[D / 16][2], const DecodePa
   }
 }
 
-template <class E, int D, int BOXR>
+template <class E, int D, int BOXR, bool BAL>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_persistent_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                              const __grid_constant__ CUtensorMap tmv) {
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int L = checked_context_len(__ldg(p.context_lens + b), p.capacity, p.max_ctx,
                                           p.err, blockIdx.x == 0);
         s_len[b] = L;
-        items = (p.balanced ? ceil16(L) : (L > 0 ? (L + P - 1) / P : 1)) * p.hkv;
+        items = (BAL ? ceil16(L) : (L > 0 ? (L + P - 1) / P : 1)) * p.hkv;
       }
       int incl = items;
 #pragma unroll
@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   sc.P = P;
   sc.NP = p.num_partitions;
   sc.NW = gridDim.x * kWorkers;
-  sc.balanced = p.balanced != 0;
+  sc.balanced = BAL;  // compile-time: each kernel carries one schedule's code
   sc.total = s_pref[nseq];
   sc.C = sc.balanced ? balanced_chunk(sc.total, sc.NW, p.chunk_cap) : 0;
   sc.chunks = sc.balanced ? (sc.total + sc.C - 1) / sc.C : 0;
@@ -362,13 +362,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       sel = nbuf;
       lblk = 0;
       off = nstart % bs;
-      want_next = true;  // prefetch the next piece once this one's first copies are out
+      want_next = true;  // prefetched after this piece's first copies are issued
     };
-    if (feeder) {
-      prefetch(0);
-      promote();
-    }
-    if (p.after_write) griddep_wait();  // the cache write has landed
+    // The first iteration prefetches the first piece into buffer 0 and
+    // promotes it, from the same call sites as every later piece.
+    want_next = true;
+    sel = 1;
+    act = true;
     const int *ids = s_ids;
     for (int c = 0;; ++c) {
       const int s = c % kStages;
@@ -376,6 +376,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       int nb = 0;
       bool bad = false;
       if (feeder) {
+        if (want_next) {  // the piece after the current one: its ids
+          want_next = false;
+          prefetch(sel ^ 1);
+        }
         if (act && cur >= endt) promote();
         ids = s_ids + (lane * 2 + sel) * p.max_ids;
 #pragma unroll
@@ -401,6 +405,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           cur += kSub;
         }
       }
+      if (c == 0 && p.after_write) griddep_wait();  // the cache write has landed
       const unsigned live = __ballot_sync(0xffffffffu, feeder && act);
       const unsigned badmask = __ballot_sync(0xffffffffu, bad);
       int nbox = nb;
@@ -449,10 +454,6 @@ __global__ void __launch_bounds__(kThreads, 2)
             tma_load_3d(kdst + h * kHalfBytes + o, &tmk, bar, h * 64, gq, rows[k]);
             tma_load_3d(vdst + h * kHalfBytes + o, &tmv, bar, h * 64, gq, rows[k]);
           }
-        }
-        if (want_next) {
-          want_next = false;
-          prefetch(sel ^ 1);
         }
       }
     }
@@ -572,14 +573,20 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         return true;
       }
-      finalize(m, false);  // empty sequence: zeros
+      if constexpr (!BAL) finalize(m, false);  // empty sequence: zeros
     }
     return false;
   };
-  bool active = begin();
+  // The next piece starts at the top of the loop, before its first stage is
+  // waited for (its query loads overlap the wait).
+  bool active = false, need_piece = true;
 
   for (int c = 0;; ++c) {
     const int s = c % kStages;
+    if (need_piece) {
+      active = begin();
+      need_piece = false;
+    }
     if (!mbar_wait_bounded(smem_u32(full + s), (c / kStages) & 1)) {
       raise_error(p.err, PA_DEVERR_TIMEOUT);
       *s_abort = 1;
@@ -667,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       cur += kSub;
       if (cur >= end) {
         finalize(cur_item, item_bad);
-        active = begin();
+        need_piece = true;
       }
     }
     __syncwarp();
@@ -802,15 +809,21 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
   }
 }
 
-template <class E, int D, int BOXR>
-cudaError_t launch_typed(const DecodeArgs &a, const DecodeParams &p, cudaStream_t stream) {
+template <class E, int D, int BOXR, bool BAL>
+cudaError_t launch_kernel(const DecodeArgs &a, const DecodeParams &p, cudaStream_t stream) {
   using S = DecodeSmem<D>;
   const int smem = S::bytes(a.num_seqs, p.max_ids);
-  auto kernel = decode_persistent_kernel<E, D, BOXR>;
-  cudaError_t e = allow_dynamic_smem<decode_persistent_kernel<E, D, BOXR>>();
+  auto kernel = decode_persistent_kernel<E, D, BOXR, BAL>;
+  cudaError_t e = allow_dynamic_smem<decode_persistent_kernel<E, D, BOXR, BAL>>();
   if (e != cudaSuccess) return e;
-  e = launch_pdl(kernel, dim3(static_cast<unsigned>(a.grid)), dim3(kThreads), smem, stream, p,
-                 a.tm_k, a.tm_v);
+  return launch_pdl(kernel, dim3(static_cast<unsigned>(a.grid)), dim3(kThreads), smem, stream,
+                    p, a.tm_k, a.tm_v);
+}
+
+template <class E, int D, int BOXR>
+cudaError_t launch_typed(const DecodeArgs &a, const DecodeParams &p, cudaStream_t stream) {
+  const cudaError_t e = p.balanced ? launch_kernel<E, D, BOXR, true>(a, p, stream)
+                                   : launch_kernel<E, D, BOXR, false>(a, p, stream);
   if (e != cudaSuccess || !a.merge) return e;
   const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.num_q_heads;
   return launch_pdl(decode_combine_kernel<E, D>, dim3(static_cast<unsigned>(rows)),
