@@ -100,7 +100,10 @@ constexpr int kItemRing = 4;
 constexpr int kItemTakers = 13;  // 8 softmax warps, 4 epilogue warps, MMA
 constexpr int kLOff = kBarOff + kNumBars * 8;   // float l[2][128]: row sums per tile
 constexpr int kMiscOff = kLOff + 2 * 128 * 4;   // ints: [2] TMEM base, [3] abort, [8..11] items
-constexpr int kSmemBytes = 1024 + kMiscOff + 64;
+constexpr int kItemWords = 16;                  // one decoded work item (PairItem fields)
+constexpr int kItemOff = kMiscOff + 64;         // the decoded items of the ring
+constexpr int kSmemBytes = 1024 + kItemOff + kItemRing * kItemWords * 4;
+static_assert(kSmemBytes <= 227 * 1024, "prefill shared memory");
 constexpr uint32_t kTmemCols = 512;         // S_A | S_B | O_A | O_B (P_t overlays S_t)
 constexpr float kRescaleThreshold = 8.0f;   // log2 of the largest P allowed
 
@@ -203,6 +206,38 @@ struct PairItem {
   bool has_b;
 };
 
+// A decoded item in shared memory (the item ring), field by field.
+__device__ __forceinline__ void store_item(volatile int *w, const PairItem &it) {
+  w[0] = it.seq;
+  w[1] = it.h;
+  w[2] = it.q_start;
+  w[3] = it.q_len;
+  w[4] = it.L;
+  w[5] = it.lim_base;
+  w[6] = it.row0[0];
+  w[7] = it.row0[1];
+  w[8] = it.nkv_t[0];
+  w[9] = it.nkv_t[1];
+  w[10] = it.nkv;
+  w[11] = it.has_b ? 1 : 0;
+}
+__device__ __forceinline__ PairItem load_item(const volatile int *w) {
+  PairItem it;
+  it.seq = w[0];
+  it.h = w[1];
+  it.q_start = w[2];
+  it.q_len = w[3];
+  it.L = w[4];
+  it.lim_base = w[5];
+  it.row0[0] = w[6];
+  it.row0[1] = w[7];
+  it.nkv_t[0] = w[8];
+  it.nkv_t[1] = w[9];
+  it.nkv = w[10];
+  it.has_b = w[11] != 0;
+  return it;
+}
+
 // Item x of the work list (see find_item).  Warp-collective.
 __device__ PairItem item_at(const PrefillParams &p, int x, int lane, bool report) {
   PairItem it;
@@ -255,16 +290,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Item j of this CTA: index published by the TMA warp in ring entry j % 4;
   // every other role takes it from there (lane 0 waits, the warp shares it).
   // Returns false when a wait gave up; *x < 0 ends the list.
-  auto take_item = [&](int j, int *x) {
+  // Item j of the ring: its index (-1: end of the list) and, decoded by
+  // the TMA warp that claimed it, its parameters.  Warp-collective.
+  volatile int *s_items = reinterpret_cast<volatile int *>(smem + kItemOff);
+  auto take_item = [&](int j, int *x, PairItem *it) {
+    const int slot = j % kItemRing;
     bool ok = true;
+    if (lane == 0) ok = mbar_wait_bounded(bar(kItemFull + slot), (j / kItemRing) & 1);
+    __syncwarp();
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     int v = -1;
-    if (lane == 0) {
-      ok = mbar_wait_bounded(bar(kItemFull + j % kItemRing), (j / kItemRing) & 1);
-      if (ok) v = misc[8 + j % kItemRing];
-      mbar_arrive(bar(kItemEmpty + j % kItemRing));
+    if (ok) {
+      v = misc[8 + slot];
+      if (v >= 0) *it = load_item(s_items + slot * kItemWords);
     }
-    *x = __shfl_sync(0xffffffffu, v, 0);
-    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    __syncwarp();  // every lane has read the slot
+    if (lane == 0) mbar_arrive(bar(kItemEmpty + slot));
+    *x = v;
+    return ok;
   };
   // Lane 0 waits, the warp learns the outcome.
   auto warp_wait = [&](uint32_t b, uint32_t parity) {
@@ -324,6 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           if (j >= kItemRing)
             ok = mbar_wait_bounded(bar(kItemEmpty + j % kItemRing), ((j / kItemRing) - 1) & 1);
+          if (it.seq >= 0 && ok) store_item(s_items + (j % kItemRing) * kItemWords, it);
           misc[8 + j % kItemRing] = it.seq >= 0 && ok ? x : -1;
           mbar_arrive(bar(kItemFull + j % kItemRing));
         }
@@ -483,9 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int j = 0;; ++j) {
         int x;
-        ok = take_item(j, &x);
+        PairItem it;
+        ok = take_item(j, &x, &it);
         if (!ok || x < 0) break;
-        const PairItem it = item_at(p, x, lane, false);
         // the item's last V tile reaches past the context end: its tail rows
         // are cleared by the TMA warp before any PV reads it
         const bool v_tail = it.nkv > 0 && it.L < it.nkv * 128;
@@ -600,9 +644,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0;; ++j) {
       int x;
-      ok = take_item(j, &x);
+      PairItem it;
+      ok = take_item(j, &x, &it);
       if (!ok || x < 0) break;
-      const PairItem it = item_at(p, x, lane, false);
 #pragma unroll 1
       for (int t = 0; t < 2; ++t) {
         const int nkv_t = it.nkv_t[t];
@@ -663,9 +707,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0;; ++j) {
       int x;
-      ok = take_item(j, &x);
+      PairItem it;
+      ok = take_item(j, &x, &it);
       if (!ok || x < 0) break;
-      const PairItem it = item_at(p, x, lane, false);
       const int my_nkv = it.nkv_t[t];
       if (my_nkv == 0) {  // the MMA thread's empty S commit for this tile
         ok = mbar_wait_bounded(bar(kSFull + t), n & 1);
