@@ -693,6 +693,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 // rows (u + c) * G + h).
 constexpr int kCombineWarps = 4;
 constexpr int kCombineBatch = 8;
+constexpr int kCombineLocalPref = 64;  // most sequences whose prefix sums a CTA forms itself
 
 template <class E, int D>
 __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const DecodeParams p) {
@@ -704,6 +705,23 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
   // context_lens is an input of the decode kernel, not its output: read it
   // while the decode kernel is still running.
   const int L = checked_context_len(__ldg(p.context_lens + b), p.capacity, p.max_ctx, p.err, false);
+  // Balanced schedule, few sequences: the prefix sums of the token stream
+  // from context_lens too (as the decode kernel forms them), so that after
+  // the wait only the partial states remain to be read.
+  const bool local_pref = p.balanced && p.num_seqs <= kCombineLocalPref;
+  int pref_b = 0, total = 0;
+  if (local_pref) {
+    for (int base = 0; base < p.num_seqs; base += 32) {
+      const int sq = base + lane;
+      int v = 0;
+      if (sq < p.num_seqs)
+        v = ceil16(checked_context_len(__ldg(p.context_lens + sq), p.capacity, p.max_ctx, p.err,
+                                       false)) *
+            p.hkv;
+      pref_b += __reduce_add_sync(0xffffffffu, sq < b ? v : 0);
+      total += __reduce_add_sync(0xffffffffu, v);
+    }
+  }
   griddep_wait();  // the partial states of the decode kernel
   griddep_launch_dependents();
   int n;
@@ -711,9 +729,13 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
   if (p.balanced) {
     if (L <= 0) return;  // zeros written by the decode kernel
     const int G = p.group, g = h / G;
-    const int T = p.ws_pref[p.num_seqs];
+    if (!local_pref) {
+      total = p.ws_pref[p.num_seqs];
+      pref_b = p.ws_pref[b];
+    }
+    const int T = total;
     const int C = balanced_chunk(T, p.num_workers, p.chunk_cap);
-    const int U = p.ws_pref[b] + g * ceil16(L);  // the unit's first position
+    const int U = pref_b + g * ceil16(L);  // the unit's first position
     const int c0 = U / C, c1 = (U + L - 1) / C;
     n = c1 - c0 + 1;
     row0 = (static_cast<int64_t>(b) * p.hkv + g + c0) * G + (h - g * G);
