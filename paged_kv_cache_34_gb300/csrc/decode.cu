@@ -722,28 +722,36 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
       total += __reduce_add_sync(0xffffffffu, v);
     }
   }
+  // The unit's pieces: workspace rows row0 + i * rstride, i < n.
+  int n = 0;
+  int64_t row0 = 0, rstride = 1;
+  auto locate = [&]() {
+    if (p.balanced) {
+      if (L <= 0) return;  // zeros written by the decode kernel
+      const int G = p.group, g = h / G;
+      const int C = balanced_chunk(total, p.num_workers, p.chunk_cap);
+      const int U = pref_b + g * ceil16(L);  // the unit's first position
+      const int c0 = U / C, c1 = (U + L - 1) / C;
+      n = c1 - c0 + 1;
+      row0 = (static_cast<int64_t>(b) * p.hkv + g + c0) * G + (h - g * G);
+      rstride = G;
+    } else {
+      n = (L + p.partition_size - 1) / p.partition_size;
+      row0 = (static_cast<int64_t>(b) * p.hq + h) * p.num_partitions;
+      rstride = 1;
+    }
+  };
+  const bool early = !p.balanced || local_pref;  // known before the decode kernel ends
+  if (early) {
+    locate();
+    if (n <= 1) return;  // written by the decode kernel itself
+  }
   griddep_wait();  // the partial states of the decode kernel
   griddep_launch_dependents();
-  int n;
-  int64_t row0, rstride;
-  if (p.balanced) {
-    if (L <= 0) return;  // zeros written by the decode kernel
-    const int G = p.group, g = h / G;
-    if (!local_pref) {
-      total = p.ws_pref[p.num_seqs];
-      pref_b = p.ws_pref[b];
-    }
-    const int T = total;
-    const int C = balanced_chunk(T, p.num_workers, p.chunk_cap);
-    const int U = pref_b + g * ceil16(L);  // the unit's first position
-    const int c0 = U / C, c1 = (U + L - 1) / C;
-    n = c1 - c0 + 1;
-    row0 = (static_cast<int64_t>(b) * p.hkv + g + c0) * G + (h - g * G);
-    rstride = G;
-  } else {
-    n = (L + p.partition_size - 1) / p.partition_size;
-    row0 = (static_cast<int64_t>(b) * p.hq + h) * p.num_partitions;
-    rstride = 1;
+  if (!early) {
+    total = p.ws_pref[p.num_seqs];
+    pref_b = p.ws_pref[b];
+    locate();
   }
   if (n <= 1) return;  // written by the decode kernel itself
   const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml);
