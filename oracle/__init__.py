@@ -33,7 +33,7 @@ _SRC = os.path.join(_HERE, "pa_oracle.c")
 _LIB = os.path.join(_HERE, "libpa_oracle.so")
 
 F16, BF16 = 0, 1
-OK, ERR_ARG, ERR_SLOT, ERR_BLOCK, ERR_LEN, ERR_NOMEM = range(6)
+OK, ERR_ARG, ERR_SLOT, ERR_BLOCK, ERR_LEN, ERR_NOMEM, ERR_SCALE = range(7)
 
 _lock = threading.Lock()
 _lib = None
@@ -76,6 +76,15 @@ def _bind(lib):
                                P, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int,
                                c.c_int64, c.c_double, c.c_int]
     lib.pao_decode.restype = c.c_int
+    lib.pao_quantize_int8.argtypes = [P, P, c.c_int64, c.c_int, c.c_float]
+    lib.pao_quantize_int8.restype = c.c_int
+    lib.pao_write_int8.argtypes = [P, P, P, P, c.c_int64, P, c.c_int64, c.c_int,
+                                   c.c_int, c.c_int, c.c_int64, c.c_int, P, P]
+    lib.pao_write_int8.restype = c.c_int
+    lib.pao_decode_int8.argtypes = [P, P, c.c_int64, P, P, P, c.c_int64, c.c_int,
+                                    P, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int,
+                                    c.c_int64, c.c_double, c.c_int, P, P]
+    lib.pao_decode_int8.restype = c.c_int
     lib.pao_prefill.argtypes = [P, P, c.c_int64, P, P, P, c.c_int64, c.c_int,
                                 P, P, c.c_int, c.c_int64, c.c_int, c.c_int,
                                 c.c_int, c.c_int, c.c_int64, c.c_double,
@@ -168,6 +177,69 @@ def decode(q, k_pool, v_pool, block_table, context_lens, num_kv_heads: int,
     st = lib.pao_decode(_ptr(out), _ptr(qu), hq * d, _ptr(ku), _ptr(vu),
                         _ptr(bt), bt.shape[1], bt.shape[1], _ptr(ctx), s, hq,
                         num_kv_heads, d, block_size, nb, float(scale), dtype)
+    return (out, st) if return_status else out
+
+
+def quantize_int8(x, scale: float, dtype: int | None = None, lib=None,
+                  return_status: bool = False):
+    """INT8 codes of fp16/bf16 values (a tensor, or uint16 patterns with
+    ``dtype``) under one scale: round-half-even(x / scale) in fp32, clamped
+    to [-127, 127]."""
+    lib = lib or load()
+    if dtype is None:
+        dtype = dtype_code(x.dtype)
+    xu = _u16(x)
+    codes = np.zeros(xu.shape, dtype=np.int8)
+    st = lib.pao_quantize_int8(_ptr(codes), _ptr(xu), xu.size, int(dtype),
+                               float(np.float32(scale)))
+    return (codes, st) if return_status else codes
+
+
+def _scales(a, n: int) -> np.ndarray:
+    v = np.ascontiguousarray(np.asarray(a, dtype=np.float32).reshape(-1))
+    assert v.size == n, (v.size, n)
+    return v
+
+
+def write_int8(k_pool: np.ndarray, v_pool: np.ndarray, k_new, v_new, slot_mapping,
+               block_size: int, k_scale, v_scale, dtype: int | None = None,
+               lib=None) -> int:
+    """The cache write into INT8 pools [NB, bs, Hkv, D], quantising each new
+    row per KV head with k_scale / v_scale ([Hkv] fp32).  Returns the status."""
+    lib = lib or load()
+    if dtype is None:
+        dtype = dtype_code(k_new.dtype)
+    kn, vn = _u16(k_new), _u16(v_new)
+    n, hkv, d = kn.shape
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    assert k_pool.dtype == np.int8 and k_pool.flags.c_contiguous
+    assert v_pool.dtype == np.int8 and v_pool.flags.c_contiguous
+    ks, vs = _scales(k_scale, hkv), _scales(v_scale, hkv)
+    return lib.pao_write_int8(_ptr(k_pool), _ptr(v_pool), _ptr(kn), _ptr(vn),
+                              hkv * d, _ptr(slots), n, hkv, d, block_size,
+                              k_pool.shape[0], int(dtype), _ptr(ks), _ptr(vs))
+
+
+def decode_int8(q, k_pool: np.ndarray, v_pool: np.ndarray, block_table, context_lens,
+                num_kv_heads: int, block_size: int, scale: float, k_scale, v_scale,
+                dtype: int | None = None, lib=None, return_status: bool = False):
+    """Oracle decode over INT8 pools ([NB, bs, Hkv, D] int8, dequantised per
+    KV head).  Returns fp64 [S, Hq, D]."""
+    lib = lib or load()
+    if dtype is None:
+        dtype = dtype_code(q.dtype)
+    qu = _u16(q)
+    ku = np.ascontiguousarray(k_pool, dtype=np.int8)
+    vu = np.ascontiguousarray(v_pool, dtype=np.int8)
+    bt = np.ascontiguousarray(np.asarray(block_table), dtype=np.int32)
+    ctx = np.ascontiguousarray(np.asarray(context_lens), dtype=np.int32)
+    s, hq, d = qu.shape
+    ks, vs = _scales(k_scale, num_kv_heads), _scales(v_scale, num_kv_heads)
+    out = np.zeros((s, hq, d), dtype=np.float64)
+    st = lib.pao_decode_int8(_ptr(out), _ptr(qu), hq * d, _ptr(ku), _ptr(vu), _ptr(bt),
+                             bt.shape[1], bt.shape[1], _ptr(ctx), s, hq, num_kv_heads,
+                             d, block_size, ku.shape[0], float(scale), dtype,
+                             _ptr(ks), _ptr(vs))
     return (out, st) if return_status else out
 
 

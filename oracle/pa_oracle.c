@@ -55,7 +55,8 @@ enum {
   PAO_ERR_BLOCK = 3, /* a block id outside [0, num_blocks)             */
   PAO_ERR_LEN = 4,   /* a length beyond the block table's capacity,
                         or cu_seqlens not a valid prefix sum           */
-  PAO_ERR_NOMEM = 5
+  PAO_ERR_NOMEM = 5,
+  PAO_ERR_SCALE = 6  /* an INT8 scale that is not a positive finite number */
 };
 
 /* ---- exact 16-bit decoders -------------------------------------------- */
@@ -171,6 +172,91 @@ static int gather(double *kc, double *vc, const uint16_t *k_pool,
   return PAO_OK;
 }
 
+/* ---- INT8 pool: per-KV-head symmetric quantisation --------------------- */
+
+/* [SKILL] App. A lists the fused operator's quantised-KV parameters (one
+ * dequantisation scale for the key and one for the value) and the page's
+ * "advanced features" note names an INT8 KV cache; neither prints the
+ * formula.  Reading taken: one fp32 scale per KV head for K and one for V,
+ * codes in [-127, 127], code = round-half-to-even(x / scale) with the
+ * division and the rounding done in fp32 (IEEE, round to nearest -- the
+ * precision the kernels decide the code in), a NaN input gives code 0, and
+ * the dequantised value is code * scale. */
+static int scale_ok(float s) { return s > 0.0f && s <= 3.4028234663852886e38f; }
+
+static int8_t quantize1(float x, float scale) {
+  if (x != x) return 0;
+  float y = x / scale;
+  if (y >= 127.0f) return 127;
+  if (y <= -127.0f) return -127;
+  return (int8_t)rintf(y);
+}
+
+/* Codes of n 16-bit values under one scale (all 0 for a bad scale). */
+int pao_quantize_int8(int8_t *codes, const uint16_t *x, int64_t n, int dtype,
+                      float scale) {
+  if (!codes || (n > 0 && !x) || n < 0) return PAO_ERR_ARG;
+  const int good = scale_ok(scale);
+  for (int64_t i = 0; i < n; ++i)
+    codes[i] = good ? quantize1((float)decode16(x[i], dtype), scale) : 0;
+  return good ? PAO_OK : PAO_ERR_SCALE;
+}
+
+/* The write of pao_write into INT8 pools: each new row is quantised per KV
+ * head g with k_scale[g] / v_scale[g]. */
+int pao_write_int8(int8_t *k_pool, int8_t *v_pool, const uint16_t *k_new,
+                   const uint16_t *v_new, int64_t row_stride,
+                   const int64_t *slot_mapping, int64_t n, int hkv, int d,
+                   int block_size, int64_t num_blocks, int dtype,
+                   const float *k_scale, const float *v_scale) {
+  if (!k_pool || !v_pool || !k_scale || !v_scale ||
+      (n > 0 && (!k_new || !v_new || !slot_mapping)))
+    return PAO_ERR_ARG;
+  if (hkv <= 0 || d <= 0 || block_size <= 0 || num_blocks < 0 || n < 0)
+    return PAO_ERR_ARG;
+  int status = PAO_OK;
+  for (int g = 0; g < hkv; ++g)
+    if (!scale_ok(k_scale[g]) || !scale_ok(v_scale[g])) status = PAO_ERR_SCALE;
+  const int64_t row = (int64_t)hkv * d;
+  for (int64_t t = 0; t < n; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= num_blocks * (int64_t)block_size) {
+      status = PAO_ERR_SLOT;
+      continue;
+    }
+    int64_t block = slot / block_size, offset = slot % block_size;
+    int64_t dst = (block * block_size + offset) * row;
+    for (int g = 0; g < hkv; ++g) {
+      const float ks = k_scale[g], vs = v_scale[g];
+      const int good = scale_ok(ks) && scale_ok(vs);
+      for (int x = 0; x < d; ++x) {
+        int64_t i = (int64_t)g * d + x;
+        k_pool[dst + i] = good ? quantize1((float)decode16(k_new[t * row_stride + i], dtype), ks) : 0;
+        v_pool[dst + i] = good ? quantize1((float)decode16(v_new[t * row_stride + i], dtype), vs) : 0;
+      }
+    }
+  }
+  return status;
+}
+
+/* gather from INT8 pools: the rows dequantised with KV head g's scales. */
+static int gather_int8(double *kc, double *vc, const int8_t *k_pool,
+                       const int8_t *v_pool, const int32_t *bt_row, int len,
+                       int g, int hkv, int d, int block_size, int64_t num_blocks,
+                       double k_scale, double v_scale) {
+  for (int j = 0; j < len; ++j) {
+    int32_t block = bt_row[j / block_size];
+    if (block < 0 || block >= num_blocks) return PAO_ERR_BLOCK;
+    int64_t base = (((int64_t)block * block_size + j % block_size) * hkv + g) * d;
+    for (int x = 0; x < d; ++x) {
+      kc[(int64_t)j * d + x] = (double)k_pool[base + x] * k_scale;
+      vc[(int64_t)j * d + x] = (double)v_pool[base + x] * v_scale;
+    }
+  }
+  return PAO_OK;
+}
+
 /* ---- attend: naive two-pass softmax attention for one query row -------- */
 
 /* o[d] = sum_j softmax(scale * q.K_j) V_j over keys 0..n-1; o = 0 if n <= 0.
@@ -206,12 +292,15 @@ static void attend(double *o, const double *q, const double *kc,
  * sequences (heads contiguous).  out: [num_seqs, hq, d] doubles.
  * block_table: [num_seqs, bt_stride] int32 of which the first
  * max_blocks_per_seq columns may be used.  context_lens: [num_seqs]. */
-int pao_decode(double *out, const uint16_t *q, int64_t q_row_stride,
-               const uint16_t *k_pool, const uint16_t *v_pool,
-               const int32_t *block_table, int64_t bt_stride,
-               int max_blocks_per_seq, const int32_t *context_lens,
-               int num_seqs, int hq, int hkv, int d, int block_size,
-               int64_t num_blocks, double scale, int dtype) {
+/* Pools of 16-bit patterns (k_scale == NULL) or INT8 codes with per-KV-head
+ * scales k_scale / v_scale. */
+static int decode_common(double *out, const uint16_t *q, int64_t q_row_stride,
+                         const void *k_pool, const void *v_pool,
+                         const int32_t *block_table, int64_t bt_stride,
+                         int max_blocks_per_seq, const int32_t *context_lens,
+                         int num_seqs, int hq, int hkv, int d, int block_size,
+                         int64_t num_blocks, double scale, int dtype,
+                         const float *k_scale, const float *v_scale) {
   if (!out || !q || !k_pool || !v_pool || !block_table || !context_lens)
     return PAO_ERR_ARG;
   if (hq <= 0 || hkv <= 0 || hq % hkv != 0 || d <= 0 || block_size <= 0)
@@ -235,9 +324,14 @@ int pao_decode(double *out, const uint16_t *q, int64_t q_row_stride,
       qd = (double *)malloc((size_t)d * sizeof(double));
       if (!kc || !vc || !s || !qd) err = PAO_ERR_NOMEM;
     }
-    if (err == PAO_OK)
-      err = gather(kc, vc, k_pool, v_pool, block_table + (int64_t)b * bt_stride,
-                   len, g, hkv, d, block_size, num_blocks, dtype);
+    if (err == PAO_OK && k_scale)
+      err = gather_int8(kc, vc, (const int8_t *)k_pool, (const int8_t *)v_pool,
+                        block_table + (int64_t)b * bt_stride, len, g, hkv, d,
+                        block_size, num_blocks, k_scale[g], v_scale[g]);
+    else if (err == PAO_OK)
+      err = gather(kc, vc, (const uint16_t *)k_pool, (const uint16_t *)v_pool,
+                   block_table + (int64_t)b * bt_stride, len, g, hkv, d,
+                   block_size, num_blocks, dtype);
     for (int h = g * group; h < (g + 1) * group; ++h) {
       double *o = out + ((int64_t)b * hq + h) * d;
       if (err != PAO_OK) {
@@ -258,6 +352,33 @@ int pao_decode(double *out, const uint16_t *q, int64_t q_row_stride,
     }
   }
   return status;
+}
+
+int pao_decode(double *out, const uint16_t *q, int64_t q_row_stride,
+               const uint16_t *k_pool, const uint16_t *v_pool,
+               const int32_t *block_table, int64_t bt_stride,
+               int max_blocks_per_seq, const int32_t *context_lens,
+               int num_seqs, int hq, int hkv, int d, int block_size,
+               int64_t num_blocks, double scale, int dtype) {
+  return decode_common(out, q, q_row_stride, k_pool, v_pool, block_table,
+                       bt_stride, max_blocks_per_seq, context_lens, num_seqs,
+                       hq, hkv, d, block_size, num_blocks, scale, dtype, NULL,
+                       NULL);
+}
+
+/* Decode over INT8 pools, dequantised per KV head (see pao_write_int8). */
+int pao_decode_int8(double *out, const uint16_t *q, int64_t q_row_stride,
+                    const int8_t *k_pool, const int8_t *v_pool,
+                    const int32_t *block_table, int64_t bt_stride,
+                    int max_blocks_per_seq, const int32_t *context_lens,
+                    int num_seqs, int hq, int hkv, int d, int block_size,
+                    int64_t num_blocks, double scale, int dtype,
+                    const float *k_scale, const float *v_scale) {
+  if (!k_scale || !v_scale) return PAO_ERR_ARG;
+  return decode_common(out, q, q_row_stride, k_pool, v_pool, block_table,
+                       bt_stride, max_blocks_per_seq, context_lens, num_seqs,
+                       hq, hkv, d, block_size, num_blocks, scale, dtype, k_scale,
+                       v_scale);
 }
 
 /* ---- prefill: packed variable-length queries --------------------------- */

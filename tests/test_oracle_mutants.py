@@ -38,6 +38,14 @@ MUTANTS = {
                              "v = ldexp((double)f, -126);"),
     "write_offset_swapped": ("int64_t offset = slot % block_size; /* position in block   */",
                              "int64_t offset = slot / block_size;"),
+    "int8_round_half_away": ("return (int8_t)rintf(y);", "return (int8_t)roundf(y);"),
+    "int8_clamp_late": ("if (y >= 127.0f) return 127;", "if (y >= 128.0f) return 127;"),
+    "int8_value_uses_key_scale": ("(double)v_pool[base + x] * v_scale;",
+                                  "(double)v_pool[base + x] * k_scale;"),
+    "int8_decode_head0_scale": ("block_size, num_blocks, k_scale[g], v_scale[g]);",
+                                "block_size, num_blocks, k_scale[0], v_scale[0]);"),
+    "int8_write_head0_scale": ("const float ks = k_scale[g], vs = v_scale[g];",
+                               "const float ks = k_scale[0], vs = v_scale[0];"),
     "decode_heads_strided": (
         "for (int h = g * group; h < (g + 1) * group; ++h) {\n      double *o = out + ((int64_t)b * hq + h) * d;",
         "for (int h = g; h < hq; h += hkv) {\n      double *o = out + ((int64_t)b * hq + h) * d;"),
@@ -169,8 +177,77 @@ def _pin_saturated_softmax(lib):
     return True
 
 
+def _bf16(vals):
+    return torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16)
+
+
+def _pin_int8_codes(lib):
+    # round half to even on x / scale, clamped to +-127; NaN -> 0
+    x = _bf16([1.0, 0.25, 0.75, 1.25, -0.75, 100.0, -100.0, float("nan"),
+               float("inf"), float("-inf"), 2.5, -1.25, 0.0, 63.75, -63.75])
+    want = [2, 0, 2, 2, -2, 127, -127, 0, 127, -127, 5, -2, 0, 127, -127]
+    codes, st = oracle.quantize_int8(x, 0.5, lib=lib, return_status=True)
+    if st != oracle.OK or codes.tolist() != want:
+        return False
+    # exact multiples of a power-of-two scale come back as themselves
+    c = np.arange(-127, 128)
+    codes = oracle.quantize_int8(_bf16((c / 64.0).tolist()), 1.0 / 64, lib=lib)
+    if codes.tolist() != c.tolist():
+        return False
+    bad, st = oracle.quantize_int8(x, 0.0, lib=lib, return_status=True)
+    return st == oracle.ERR_SCALE and not bad.any()
+
+
+def _pin_int8_write(lib):
+    nb, bs, hkv, d = 4, 8, 2, 2
+    kp = np.zeros((nb, bs, hkv, d), np.int8)
+    vp = np.zeros((nb, bs, hkv, d), np.int8)
+    kn = _bf16([[[1.0, -2.0], [3.0, 4.0]]])
+    vn = _bf16([[[0.5, 0.25], [-1.0, 8.0]]])
+    st = oracle.write_int8(kp, vp, kn, vn, np.array([2 * bs + 3]), bs,
+                           [0.5, 1.0], [0.25, 2.0], lib=lib)
+    return (st == oracle.OK and kp[2, 3].tolist() == [[2, -4], [3, 4]]
+            and vp[2, 3].tolist() == [[2, 1], [0, 4]]
+            and int(np.abs(kp).sum()) == 13 and int(np.abs(vp).sum()) == 7)
+
+
+def _pin_int8_decode(lib):
+    # INT8 pools whose dequantised values are exact in bf16 must decode
+    # exactly like bf16 pools holding those values (the pinned 16-bit path)
+    x = W.make_inputs(_cfg("decode", 4, 2, 64, 16, 24, [1, 37, 90], "identity",
+                           dtype="bf16"), seed=47)
+    rng = np.random.default_rng(5)
+    shape = tuple(x.k_pool.shape)
+    kc = rng.integers(-127, 128, shape).astype(np.int8)
+    vc = rng.integers(-127, 128, shape).astype(np.int8)
+    ks, vs = np.array([2.0 ** -6, 2.0 ** -4], np.float32), np.array([2.0 ** -3, 2.0 ** -7], np.float32)
+    kb = torch.from_numpy(kc.astype(np.float32) * ks[None, None, :, None]).to(torch.bfloat16)
+    vb = torch.from_numpy(vc.astype(np.float32) * vs[None, None, :, None]).to(torch.bfloat16)
+    want = oracle.decode(x.q, kb, vb, x.block_table, x.context_lens, 2, 16, x.scale,
+                         lib=lib)
+    got = oracle.decode_int8(x.q, kc, vc, x.block_table, x.context_lens, 2, 16, x.scale,
+                             ks, vs, lib=lib)
+    return np.array_equal(got, want)
+
+
+def _pin_int8_nearest(lib):
+    # every code is the nearest integer to x / scale (ties to even), clamped
+    rng = np.random.default_rng(9)
+    x = torch.from_numpy(rng.standard_normal(4096).astype(np.float32) * 3).to(torch.bfloat16)
+    s = np.float32(0.0371)
+    y = x.float().numpy() / s
+    c = oracle.quantize_int8(x, float(s), lib=lib).astype(np.float64)
+    inside = np.abs(y) < 127
+    ci = c[inside]
+    err = np.abs(y[inside] - ci)
+    ties = err == 0.5
+    return (bool((err <= 0.5).all()) and bool((ci[ties] % 2 == 0).all())
+            and bool((c[~inside] == np.sign(y[~inside]) * 127).all()))
+
+
 PINS = [_pin_decode_sdpa, _pin_prefill_sdpa, _pin_chunked_tail,
-        _pin_decoders, _pin_write, _pin_saturated_softmax]
+        _pin_decoders, _pin_write, _pin_saturated_softmax, _pin_int8_codes,
+        _pin_int8_write, _pin_int8_decode, _pin_int8_nearest]
 
 
 @pytest.fixture(scope="module")
