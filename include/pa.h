@@ -89,6 +89,7 @@ typedef enum pa_dtype { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
 #define PA_DEVERR_CU_SEQLENS 4 /* cu_seqlens not a prefix sum of the batch    */
 #define PA_DEVERR_CONTEXT 8    /* context_len < 0, > capacity or > host hint  */
 #define PA_DEVERR_TIMEOUT 16   /* a bounded pipeline wait gave up             */
+#define PA_DEVERR_SCALE 32     /* an INT8 scale not a positive finite number  */
 
 /* ABI version the library was built with (PA_ABI_VERSION). */
 int32_t pa_abi_version(void);
@@ -316,6 +317,74 @@ pa_status pa_decode_static_ws(void *out, int64_t out_row_stride,
                               int64_t num_blocks, float scale,
                               int32_t max_context_len, int32_t partition_size,
                               pa_dtype dtype, int32_t *d_error, void *stream);
+
+/*
+ * INT8 KV pools.
+ *
+ * The pages list the fused attention operator's quantised-KV parameters --
+ * one dequantisation scale for the key and one for the value ([SKILL] App.
+ * A) -- and name an INT8 KV cache among its advanced features ([SKILL]
+ * "advanced features"), without printing the formula.  This library's
+ * reading: one fp32 scale per KV head for K (k_scale[g]) and one for V
+ * (v_scale[g]); a value x is stored as the int8 code
+ *     c = round-half-to-even(x / scale), clamped to [-127, 127]
+ * with the division and the rounding in fp32 (IEEE round to nearest), a NaN
+ * input stored as 0, and it is read back as c * scale.  The pools are
+ * [num_blocks, block_size, num_kv_heads, head_dim] int8; everything else is
+ * as for the 16-bit calls.  Halving the pool's bytes halves what a decode
+ * step reads.
+ *
+ * A scale that is not a positive finite number sets PA_DEVERR_SCALE; the
+ * write then stores code 0 for that head, and the decode gives that head's
+ * queries a zero output.
+ */
+
+/*
+ * pa_reshape_and_cache_int8 -- pa_reshape_and_cache into INT8 pools.
+ *
+ *   key, value      [num_tokens, num_kv_heads, head_dim] fp16/bf16 (dtype),
+ *                   token t at element t * kv_row_stride.
+ *   key_cache,
+ *   value_cache     int8 pools; written, never read.
+ *   k_scale,
+ *   v_scale         device fp32 [num_kv_heads]; read, never written.
+ * Requirements: num_kv_heads * head_dim a multiple of 16 (16-byte int8 rows
+ * of the pool) and kv_row_stride * 2 bytes a multiple of 16.
+ */
+pa_status pa_reshape_and_cache_int8(const void *key, const void *value,
+                                    int64_t kv_row_stride, void *key_cache,
+                                    void *value_cache, const int64_t *slot_mapping,
+                                    int32_t num_tokens, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t block_size,
+                                    int64_t num_blocks, const float *k_scale,
+                                    const float *v_scale, pa_dtype dtype,
+                                    int32_t *d_error, void *stream);
+
+/*
+ * pa_decode_int8 -- pa_decode over INT8 pools.
+ *
+ * out[b, h, :] = sum_j softmax_j(scale * q . (k_scale[g] * Kc_j))
+ *                      (v_scale[g] * Vc_j)
+ * with Kc_j, Vc_j the int8 codes of key/value row j of KV head g.  The
+ * scores and the weighted sum are accumulated in fp32 from the codes widened
+ * exactly to fp16 and the query rounded to fp16 (its nearest fp16 value; a
+ * query beyond the fp16 range is not supported); the K scale multiplies the
+ * scores and the V scale the output.  query / out are fp16 or bf16 (dtype).
+ * Workspace: as pa_decode_plan reports for the same shape.
+ * Supported: head_dim 128; num_q_heads / num_kv_heads in 1..8; block_size 8,
+ * 16, 32, 64 or 128.
+ */
+pa_status pa_decode_int8(void *out, int64_t out_row_stride, const void *query,
+                         int64_t q_row_stride, const void *key_cache,
+                         const void *value_cache, const int32_t *block_table,
+                         int64_t block_table_stride, int32_t max_blocks_per_seq,
+                         const int32_t *context_lens, int32_t num_seqs,
+                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t block_size, int64_t num_blocks, const float *k_scale,
+                         const float *v_scale, float scale, int32_t max_context_len,
+                         int32_t partition_size, void *workspace,
+                         size_t workspace_bytes, pa_dtype dtype, int32_t *d_error,
+                         void *stream);
 
 #ifdef __cplusplus
 }

@@ -22,14 +22,15 @@ import threading
 import torch
 
 __all__ = ["pa_reshape_and_cache", "pa_decode", "pa_decode_plan", "pa_decode_write",
-           "pa_prefill_varlen", "PaError", "library", "DEVERR_SLOT",
-           "DEVERR_BLOCK_ID", "DEVERR_CU_SEQLENS", "DEVERR_CONTEXT",
-           "DEVERR_TIMEOUT", "LIB_PATH"]
+           "pa_prefill_varlen", "pa_reshape_and_cache_int8", "pa_decode_int8", "PaError",
+           "library", "DEVERR_SLOT", "DEVERR_BLOCK_ID", "DEVERR_CU_SEQLENS",
+           "DEVERR_CONTEXT", "DEVERR_TIMEOUT", "DEVERR_SCALE", "LIB_PATH"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpa.so")
 
 # Device error bits (include/pa.h PA_DEVERR_*).
 DEVERR_SLOT, DEVERR_BLOCK_ID, DEVERR_CU_SEQLENS, DEVERR_CONTEXT, DEVERR_TIMEOUT = 1, 2, 4, 8, 16
+DEVERR_SCALE = 32
 
 _STATUS = {0: "PA_OK", 1: "PA_ERR_NULL", 2: "PA_ERR_SHAPE", 3: "PA_ERR_UNSUPPORTED",
            4: "PA_ERR_ALIGN", 5: "PA_ERR_WORKSPACE", 6: "PA_ERR_CUDA"}
@@ -80,6 +81,12 @@ def library(path: str | None = None):
                                           I32, I32, I32, I32, I32, I32, I64, F, I32, c.c_int,
                                           V, V]
         lib.pa_prefill_varlen.restype = c.c_int
+        lib.pa_reshape_and_cache_int8.argtypes = [V, V, I64, V, V, V, I32, I32, I32, I32, I64,
+                                                  V, V, c.c_int, V, V]
+        lib.pa_reshape_and_cache_int8.restype = c.c_int
+        lib.pa_decode_int8.argtypes = [V, I64, V, I64, V, V, V, I64, I32, V, I32, I32, I32,
+                                       I32, I32, I64, V, V, F, I32, I32, V, SZ, c.c_int, V, V]
+        lib.pa_decode_int8.restype = c.c_int
         if path is None:
             _lib = lib
         return lib
@@ -130,6 +137,34 @@ def pa_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, *,
     _check(lib, st, "pa_reshape_and_cache")
 
 
+def _scales(t, hkv, what):
+    if t.dtype != torch.float32 or t.numel() != hkv or not t.is_contiguous():
+        raise ValueError(f"{what} must be a contiguous float32 tensor of num_kv_heads values")
+    return _ptr(t)
+
+
+def pa_reshape_and_cache_int8(key, value, key_cache, value_cache, slot_mapping, k_scale,
+                              v_scale, *, d_error=None, stream=None, lib=None):
+    """pa_reshape_and_cache into INT8 pools: caches int8 [NB, bs, Hkv, D];
+    k_scale / v_scale float32 [Hkv] (per-KV-head dequantisation scales)."""
+    lib = lib or library()
+    ks = _rows(key, "key")
+    if _rows(value, "value") != ks:
+        raise ValueError("key and value must share a row stride")
+    if key_cache.dtype != torch.int8 or value_cache.dtype != torch.int8:
+        raise ValueError("INT8 caches must be int8")
+    if not key_cache.is_contiguous() or not value_cache.is_contiguous():
+        raise ValueError("caches must be contiguous [num_blocks, block_size, Hkv, D]")
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    nb, bs, hkv, d = key_cache.shape
+    st = lib.pa_reshape_and_cache_int8(
+        _ptr(key), _ptr(value), ks, _ptr(key_cache), _ptr(value_cache), _ptr(slot_mapping),
+        key.shape[0], hkv, d, bs, nb, _scales(k_scale, hkv, "k_scale"),
+        _scales(v_scale, hkv, "v_scale"), _DTYPE[key.dtype], _ptr(d_error), _stream(stream))
+    _check(lib, st, "pa_reshape_and_cache_int8")
+
+
 def pa_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
                    partition_size=0, lib=None):
     """(partition_size, workspace_bytes) that pa_decode will use."""
@@ -165,6 +200,33 @@ def pa_decode(out, query, key_cache, value_cache, block_table, context_lens, *, 
                        _ptr(workspace), wbytes, _DTYPE[query.dtype], _ptr(d_error),
                        _stream(stream))
     _check(lib, st, "pa_decode")
+    return out
+
+
+def pa_decode_int8(out, query, key_cache, value_cache, block_table, context_lens, k_scale,
+                   v_scale, *, scale, max_context_len, partition_size=0, workspace=None,
+                   d_error=None, stream=None, lib=None):
+    """pa_decode over INT8 pools (int8 [NB, bs, Hkv, D], head_dim 128) with
+    per-KV-head float32 scales k_scale / v_scale [Hkv]."""
+    lib = lib or library()
+    s, hq, d = query.shape
+    nb, bs, hkv, _ = key_cache.shape
+    if key_cache.dtype != torch.int8 or value_cache.dtype != torch.int8:
+        raise ValueError("INT8 caches must be int8")
+    P, need = pa_decode_plan(s, hq, hkv, d, max_context_len, partition_size, lib=lib)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if block_table.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_table and context_lens must be int32")
+    st = lib.pa_decode_int8(_ptr(out), _rows(out, "out"), _ptr(query), _rows(query, "query"),
+                            _ptr(key_cache), _ptr(value_cache), _ptr(block_table),
+                            block_table.stride(0), block_table.shape[1], _ptr(context_lens), s,
+                            hq, hkv, d, bs, nb, _scales(k_scale, hkv, "k_scale"),
+                            _scales(v_scale, hkv, "v_scale"), float(scale),
+                            int(max_context_len), P, _ptr(workspace), wbytes,
+                            _DTYPE[query.dtype], _ptr(d_error), _stream(stream))
+    _check(lib, st, "pa_decode_int8")
     return out
 
 

@@ -46,6 +46,8 @@
 //  * Exponentials are base 2 with the scale pre-multiplied by log2(e).
 #include <math.h>
 
+#include <type_traits>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -60,11 +62,20 @@ constexpr int kSub = kDecodeSub;               // tokens per worker per stage
 constexpr int kHalfBytes = kWorkers * kSub * 128;  // 64 rows x 64 elements x 2 B
 constexpr uint32_t kTerminate = 0x100u;        // stage header: no more data
 
-template <int D>
+// A stage holds, per K and V, `kRegions` regions of kWorkers x kSub rows of
+// 128 bytes (128-byte swizzle): 16-bit pools in 64-element halves, INT8 pools
+// (head_dim 128) in one region of whole rows.  INT8 stages are widened by
+// each worker into its own fp16 scratch (two 64-element halves of kSub rows
+// for K and for V) that the tensor-core code reads like a 16-bit stage.
+template <int D, bool KV8 = false>
 struct DecodeSmem {
   static constexpr int kHalves = D / 64;
-  static constexpr int kStageBytes = 2 * kHalves * kHalfBytes;  // K + V
-  static constexpr int kBarOffset = kStages * kStageBytes;      // full[3], empty[3]
+  static constexpr int kRegions = KV8 ? 1 : kHalves;
+  static constexpr int kStageBytes = 2 * kRegions * kHalfBytes;  // K + V
+  static constexpr int kScratchHalf = kSub * 128;                 // one worker, one half
+  static constexpr int kScratchWorker = 2 * kHalves * kScratchHalf;
+  static constexpr int kScratchOffset = kStages * kStageBytes;
+  static constexpr int kBarOffset = kScratchOffset + (KV8 ? kWorkers * kScratchWorker : 0);
   static constexpr int kHdrOffset = kBarOffset + 2 * kStages * 8;
   static constexpr int kVarOffset = kHdrOffset + 32;  // pref[S+1], len[S], ids
   static int bytes(int num_seqs, int max_ids) {
@@ -88,6 +99,7 @@ struct DecodeParams {
   int32_t balanced, chunk_cap, num_workers;  // balanced schedule (see above)
   float *ws_o, *ws_ml;
   int32_t *ws_pref;  // balanced: the prefix sums, for the merge kernel
+  const float *k_scale, *v_scale;  // INT8 pools: per-KV-head dequantisation scales
   int32_t after_write;  // launched directly after this step's cache write
   int32_t *err;
 };
@@ -219,7 +231,15 @@ __device__ __forceinline__ float shfl_xor(float v, int m) {
   return __shfl_xor_sync(0xffffffffu, v, m);
 }
 
-template <class E, int D>
+// A pair of query values as the tensor core's operand type: as stored, or
+// (TOF16) rounded from bf16 to the nearest fp16 pair.
+template <class E, bool TOF16>
+__device__ __forceinline__ uint32_t q_pair(uint32_t w) {
+  if constexpr (TOF16 && E::kBF16) return F16::pack2(E::lo(w), E::hi(w));
+  return w;
+}
+
+template <class E, int D, bool TOF16 = false>
 __device__ __forceinline__ void load_q(uint32_t (&qf)[D / 16][2], const DecodeParams &p,
                                        const Item &m, int lane) {
   const int G = p.group;
@@ -228,17 +248,60 @@ __device__ __forceinline__ void load_q(uint32_t (&qf)[D / 16][2], const DecodePa
                               m.b * p.q_row_stride + (m.g * G + qh) * D + 2 * (lane & 3);
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
-    qf[ks][0] = qh < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16)) : 0u;
-    qf[ks][1] = qh < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8)) : 0u;
+    qf[ks][0] = qh < G ? q_pair<E, TOF16>(__ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16)))
+                       : 0u;
+    qf[ks][1] =
+        qh < G ? q_pair<E, TOF16>(__ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8)))
+               : 0u;
   }
 }
 
-template <class E, int D, int BOXR, bool BAL>
+// Widens int8 codes c (four per word) to fp16 pairs exactly: with the sign
+// bit flipped a code is the byte u = c + 128, the fp16 with bits 0x6400 | u
+// is 1024 + u, and subtracting 1152 leaves c.  lo gets bytes 0-1, hi 2-3.
+__device__ __forceinline__ void widen4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+  const __half2 off = __floats2half2_rn(1152.0f, 1152.0f);
+  __half2 ha = __hsub2(*reinterpret_cast<__half2 *>(&a), off);
+  __half2 hb = __hsub2(*reinterpret_cast<__half2 *>(&b), off);
+  lo = *reinterpret_cast<uint32_t *>(&ha);
+  hi = *reinterpret_cast<uint32_t *>(&hb);
+}
+
+// One worker's kSub int8 rows of 128 codes (a TMA tile with the 128-byte
+// swizzle: 16-byte chunk j of row r at chunk j ^ (r & 7)) -> fp16 rows in two
+// 64-element halves of the same swizzled layout, kScratchHalf bytes apart.
+// Lane l widens row l / 2, half l % 2.
+template <class S>
+__device__ __forceinline__ void widen_rows(const uint8_t *src, uint8_t *dst, int lane) {
+  const int r = lane >> 1, h = lane & 1;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int j = h * 4 + q;  // int8 chunk: elements 16j .. 16j+15
+    const uint4 c = *reinterpret_cast<const uint4 *>(src + r * 128 + ((j ^ (r & 7)) << 4));
+    uint4 a, b;  // fp16 elements 16j .. 16j+7 and 16j+8 .. 16j+15
+    widen4(c.x, a.x, a.y);
+    widen4(c.y, a.z, a.w);
+    widen4(c.z, b.x, b.y);
+    widen4(c.w, b.z, b.w);
+    const int c0 = (2 * j) & 7, c1 = (2 * j + 1) & 7;  // fp16 chunks within half h
+    uint8_t *row = dst + h * S::kScratchHalf + r * 128;
+    *reinterpret_cast<uint4 *>(row + ((c0 ^ (r & 7)) << 4)) = a;
+    *reinterpret_cast<uint4 *>(row + ((c1 ^ (r & 7)) << 4)) = b;
+  }
+}
+
+template <class E, int D, int BOXR, bool BAL, bool KV8>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_persistent_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                              const __grid_constant__ CUtensorMap tmv) {
-  using S = DecodeSmem<D>;
+  using S = DecodeSmem<D, KV8>;
+  using M = std::conditional_t<KV8, F16, E>;  // the tensor cores' operand type
   constexpr int NH = S::kHalves;
+  constexpr int NR = S::kRegions;
   constexpr int KSTEPS = D / 16;
 
   extern __shared__ uint8_t smem_raw[];
@@ -439,18 +502,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         s_hdr[s] = badmask & ((1u << kWorkers) - 1);
         if (badmask) raise_error(p.err, PA_DEVERR_BLOCK_ID);
         // The barrier must expect exactly the bytes that land.
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nbox) * BOXR * 128 * NH * 2);
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nbox) * BOXR * 128 * NR * 2);
       }
       __syncwarp();
       if (feeder) {
         const uint32_t kdst = smem_u32(smem + s * S::kStageBytes);
-        const uint32_t vdst = kdst + NH * kHalfBytes;
+        const uint32_t vdst = kdst + NR * kHalfBytes;
 #pragma unroll
         for (int k = 0; k < kSub / BOXR; ++k) {
           if (rows[k] < 0) continue;
           const uint32_t o = (lane * kSub + k * BOXR) * 128;
 #pragma unroll
-          for (int h = 0; h < NH; ++h) {
+          for (int h = 0; h < NR; ++h) {
             tma_load_3d(kdst + h * kHalfBytes + o, &tmk, bar, h * 64, gq, rows[k]);
             tma_load_3d(vdst + h * kHalfBytes + o, &tmv, bar, h * 64, gq, rows[k]);
           }
@@ -461,7 +524,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   // ----------------------------------------------------- consumer = worker --
   const int G = p.group;
-  const float sl = p.scale_log2;
+  float sl = p.scale_log2;  // INT8 pools: times the piece's K scale
+  float vsc = 1.f;          // INT8 pools: the piece's V scale
   const int r0 = warp * kSub;  // this worker's rows in a stage
   const int mj = lane >> 3, mr = lane & 7;
   const int h0 = 2 * (lane & 3), h1 = h0 + 1;
@@ -501,12 +565,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int mt = 0; mt < KSTEPS; ++mt) {
         const int d0 = mt * 16 + (lane >> 2), d1 = d0 + 8;
         if (h0 < G) {
-          out[h0 * D + d0] = E::from_float(o[mt][0] * i0);
-          out[h0 * D + d1] = E::from_float(o[mt][2] * i0);
+          out[h0 * D + d0] = E::from_float(o[mt][0] * (i0 * vsc));
+          out[h0 * D + d1] = E::from_float(o[mt][2] * (i0 * vsc));
         }
         if (h1 < G) {
-          out[h1 * D + d0] = E::from_float(o[mt][1] * i1);
-          out[h1 * D + d1] = E::from_float(o[mt][3] * i1);
+          out[h1 * D + d0] = E::from_float(o[mt][1] * (i1 * vsc));
+          out[h1 * D + d1] = E::from_float(o[mt][3] * (i1 * vsc));
         }
       }
     } else {
@@ -517,13 +581,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int d0 = mt * 16 + (lane >> 2), d1 = d0 + 8;
         if (h0 < G) {
           float *w0 = p.ws_o + (row0 + h0 * hstride) * D;
-          w0[d0] = bad_item ? 0.f : o[mt][0];
-          w0[d1] = bad_item ? 0.f : o[mt][2];
+          w0[d0] = bad_item ? 0.f : o[mt][0] * vsc;
+          w0[d1] = bad_item ? 0.f : o[mt][2] * vsc;
         }
         if (h1 < G) {
           float *w1 = p.ws_o + (row0 + h1 * hstride) * D;
-          w1[d0] = bad_item ? 0.f : o[mt][1];
-          w1[d1] = bad_item ? 0.f : o[mt][3];
+          w1[d0] = bad_item ? 0.f : o[mt][1] * vsc;
+          w1[d1] = bad_item ? 0.f : o[mt][3] * vsc;
         }
       }
       if (lane < 4) {
@@ -556,17 +620,30 @@ __global__ void __launch_bounds__(kThreads, 2)
             qf[ks][1] = qn[ks][1];
           }
         } else {
-          load_q<E, D>(qf, p, m, lane);
+          load_q<E, D, KV8>(qf, p, m, lane);
         }
         cur_item = m;
         cur = m.start;
+        if constexpr (KV8) {
+          // The piece's KV head's scales: K's scales the scores, V's the
+          // output.  One that is not a positive finite number makes the
+          // piece contribute nothing (zeros / an empty softmax state).
+          const float ks = __ldg(p.k_scale + m.g), vs = __ldg(p.v_scale + m.g);
+          const float big = 3.4028234663852886e38f;
+          sl = p.scale_log2 * ks;
+          vsc = vs;
+          if (!(ks > 0.f && ks <= big && vs > 0.f && vs <= big)) {
+            item_bad = true;
+            if (lane == 0) raise_error(p.err, PA_DEVERR_SCALE);
+          }
+        }
         // Prefetch the next piece's query one piece ahead.
         Cursor peek = wc;
         Item nm;
         qn_b = qn_g = -1;
         while (next_piece(sc, peek, nm)) {
           if (nm.end <= nm.start) continue;
-          load_q<E, D>(qn, p, nm, lane);
+          load_q<E, D, KV8>(qn, p, nm, lane);
           qn_b = nm.b;
           qn_g = nm.g;
           break;
@@ -594,14 +671,35 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     const uint32_t hdr = s_hdr[s];
     if (hdr & kTerminate) break;
+    bool released = false;
     if (active) {
       const int end = cur_item.end;
       const int j0 = cur;
       uint8_t *kst = smem + s * S::kStageBytes;
-      const uint32_t kb = smem_u32(kst);
-      const uint32_t vb = kb + NH * kHalfBytes;
+      // Where this worker's K and V rows are read from: the stage itself,
+      // rows r0.. of halves kHalfBytes apart, or (INT8) its fp16 scratch,
+      // rows 0.. of halves kScratchHalf apart.
+      constexpr int HB = KV8 ? S::kScratchHalf : kHalfBytes;
+      const int rb = KV8 ? 0 : r0;
+      uint32_t kb, vb;
       bool zeroed = false;
-      if (j0 + kSub > end) {
+      if constexpr (KV8) {
+        // Widen this worker's int8 rows (finite whatever the pool held, so
+        // rows past the context need no clearing), then hand the stage back.
+        uint8_t *scr = smem + S::kScratchOffset + warp * S::kScratchWorker;
+        __syncwarp();  // the previous stage's reads of the scratch are done
+        widen_rows<S>(kst + r0 * 128, scr, lane);
+        widen_rows<S>(kst + kHalfBytes + r0 * 128, scr + NH * S::kScratchHalf, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(empty + s));
+        released = true;
+        kb = smem_u32(scr);
+        vb = kb + NH * S::kScratchHalf;
+      } else {
+        kb = smem_u32(kst);
+        vb = kb + NH * kHalfBytes;
+      }
+      if (!KV8 && j0 + kSub > end) {
         // Rows past the context may hold anything (even NaN); their weight is
         // zero, so make their V rows exact zeros before the P.V product.
         uint8_t *vrows = kst + NH * kHalfBytes;
@@ -618,13 +716,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int ks = 0; ks < KSTEPS; ++ks) {
-        const int row = r0 + (mj & 1) * 8 + mr;
+        const int row = rb + (mj & 1) * 8 + mr;
         const int c16 = ks * 2 + (mj >> 1);
         const uint32_t addr =
-            kb + (c16 >> 3) * kHalfBytes + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
+            kb + (c16 >> 3) * HB + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
         uint32_t a0, a1, a2, a3;
         ldmatrix_x4(addr, a0, a1, a2, a3);
-        mma_16816<E::kBF16>(sc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+        mma_16816<M::kBF16>(sc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
       }
       const int t0 = j0 + (lane >> 2), t1 = t0 + 8;
       const float s00 = t0 < end ? sc[0] * sl : -INFINITY;
@@ -644,10 +742,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       // P is rounded to the input type for the tensor core; the row sums use
       // the same rounded values, so the output is an exact weighted mean of
       // V under the rounded weights.
-      const uint32_t w0 = E::pack2(exp2f(s00 - mn0), exp2f(s01 - mn1));  // token t0
-      const uint32_t w1 = E::pack2(exp2f(s10 - mn0), exp2f(s11 - mn1));  // token t1
-      l0 = l0 * cr0 + (E::lo(w0) + E::lo(w1));
-      l1 = l1 * cr1 + (E::hi(w0) + E::hi(w1));
+      const uint32_t w0 = M::pack2(exp2f(s00 - mn0), exp2f(s01 - mn1));  // token t0
+      const uint32_t w1 = M::pack2(exp2f(s10 - mn0), exp2f(s11 - mn1));  // token t1
+      l0 = l0 * cr0 + (M::lo(w0) + M::lo(w1));
+      l1 = l1 * cr1 + (M::hi(w0) + M::hi(w1));
 #pragma unroll
       for (int mt = 0; mt < KSTEPS; ++mt) {
         o[mt][0] *= cr0;
@@ -661,13 +759,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       // O^T += V^T P^T, one 16-wide slice of D at a time.
 #pragma unroll
       for (int mt = 0; mt < KSTEPS; ++mt) {
-        const int row = r0 + (mj >> 1) * 8 + mr;
+        const int row = rb + (mj >> 1) * 8 + mr;
         const int c16 = mt * 2 + (mj & 1);
         const uint32_t addr =
-            vb + (c16 >> 3) * kHalfBytes + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
+            vb + (c16 >> 3) * HB + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
         uint32_t a0, a1, a2, a3;
         ldmatrix_x4_trans(addr, a0, a1, a2, a3);
-        mma_16816<E::kBF16>(o[mt], a0, a1, a2, a3, pb0, pb1);
+        mma_16816<M::kBF16>(o[mt], a0, a1, a2, a3, pb0, pb1);
       }
       if (zeroed) fence_proxy_async_smem();  // generic writes before the next TMA
       if (hdr & (1u << warp)) item_bad = true;
@@ -677,8 +775,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         need_piece = true;
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(empty + s));
+    if (!released) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(empty + s));
+    }
   }
 }
 
@@ -839,32 +939,32 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
   }
 }
 
-template <class E, int D, int BOXR, bool BAL>
+template <class E, int D, int BOXR, bool BAL, bool KV8>
 cudaError_t launch_kernel(const DecodeArgs &a, const DecodeParams &p, cudaStream_t stream) {
-  using S = DecodeSmem<D>;
+  using S = DecodeSmem<D, KV8>;
   const int smem = S::bytes(a.num_seqs, p.max_ids);
-  auto kernel = decode_persistent_kernel<E, D, BOXR, BAL>;
-  cudaError_t e = allow_dynamic_smem<decode_persistent_kernel<E, D, BOXR, BAL>>();
+  auto kernel = decode_persistent_kernel<E, D, BOXR, BAL, KV8>;
+  cudaError_t e = allow_dynamic_smem<decode_persistent_kernel<E, D, BOXR, BAL, KV8>>();
   if (e != cudaSuccess) return e;
   return launch_pdl(kernel, dim3(static_cast<unsigned>(a.grid)), dim3(kThreads), smem, stream,
                     p, a.tm_k, a.tm_v);
 }
 
-template <class E, int D, int BOXR>
+template <class E, int D, int BOXR, bool KV8>
 cudaError_t launch_typed(const DecodeArgs &a, const DecodeParams &p, cudaStream_t stream) {
-  const cudaError_t e = p.balanced ? launch_kernel<E, D, BOXR, true>(a, p, stream)
-                                   : launch_kernel<E, D, BOXR, false>(a, p, stream);
+  const cudaError_t e = p.balanced ? launch_kernel<E, D, BOXR, true, KV8>(a, p, stream)
+                                   : launch_kernel<E, D, BOXR, false, KV8>(a, p, stream);
   if (e != cudaSuccess || !a.merge) return e;
   const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.num_q_heads;
   return launch_pdl(decode_combine_kernel<E, D>, dim3(static_cast<unsigned>(rows)),
                     dim3(kCombineWarps * 32), 0, stream, p);
 }
 
-template <class E, int D>
+template <class E, int D, bool KV8 = false>
 cudaError_t launch_box(const DecodeArgs &a, const DecodeParams &p, cudaStream_t stream) {
   switch (a.box_rows) {
-    case 8: return launch_typed<E, D, 8>(a, p, stream);
-    case 16: return launch_typed<E, D, 16>(a, p, stream);
+    case 8: return launch_typed<E, D, 8, KV8>(a, p, stream);
+    case 16: return launch_typed<E, D, 16, KV8>(a, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -873,8 +973,10 @@ cudaError_t launch_box(const DecodeArgs &a, const DecodeParams &p, cudaStream_t 
 
 // Largest dynamic shared memory the decode kernel needs for this shape, so
 // the host can reject shapes that cannot launch.
-size_t decode_smem_bytes(int head_dim, int num_seqs, int partition_size, int block_size) {
+size_t decode_smem_bytes(int head_dim, int num_seqs, int partition_size, int block_size,
+                         bool kv_int8) {
   const int max_ids = (partition_size > 0 ? partition_size : kDecodeChunkCap) / block_size + 2;
+  if (kv_int8) return DecodeSmem<128, true>::bytes(num_seqs, max_ids);
   return head_dim == 128 ? DecodeSmem<128>::bytes(num_seqs, max_ids)
                          : DecodeSmem<64>::bytes(num_seqs, max_ids);
 }
@@ -907,10 +1009,15 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
   p.ws_ml = a.ws_ml;
   p.ws_pref = a.ws_pref;
   p.after_write = a.after_write ? 1 : 0;
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
   p.err = a.d_error;
   const bool bf = a.dtype == PA_BF16;
   if (a.head_dim == 128)
-    return bf ? launch_box<BF16, 128>(a, p, stream) : launch_box<F16, 128>(a, p, stream);
+    return a.kv_int8
+               ? (bf ? launch_box<BF16, 128, true>(a, p, stream)
+                     : launch_box<F16, 128, true>(a, p, stream))
+               : (bf ? launch_box<BF16, 128>(a, p, stream) : launch_box<F16, 128>(a, p, stream));
   if (a.head_dim == 64)
     return bf ? launch_box<BF16, 64>(a, p, stream) : launch_box<F16, 64>(a, p, stream);
   return cudaErrorInvalidValue;

@@ -69,18 +69,24 @@ EncodeTiledFn encode_fn() {
 //   dim0 = head_dim (contiguous), dim1 = heads, dim2 = rows,
 // with `row_stride` elements between rows; box (64, 1, box_rows) and
 // 128-byte swizzle (the box's 64 elements are exactly one 128-byte line).
+// A pool viewed as [rows, heads, head_dim] for TMA: boxes of 128 bytes of one
+// head's row (64 16-bit elements, or 128 int8 codes) by box_rows rows, with
+// the 128-byte swizzle the kernels' shared-memory reads expect.
 bool encode_rows_map(CUtensorMap *map, const void *base, pa_dtype dtype, int head_dim,
-                     int heads, int64_t rows, int64_t row_stride, int box_rows) {
+                     int heads, int64_t rows, int64_t row_stride, int box_rows,
+                     bool int8 = false) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
+  const cuuint64_t eb = int8 ? 1 : 2;  // element bytes
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(heads),
                               static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
-                                 static_cast<cuuint64_t>(row_stride) * 2};
-  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * eb,
+                                 static_cast<cuuint64_t>(row_stride) * eb};
+  const cuuint32_t box[3] = {int8 ? 128u : 64u, 1, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUtensorMapDataType dt =
-      dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType dt = int8               ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUresult r = enc(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -200,6 +206,36 @@ pa_status pa_reshape_and_cache(const void *key, const void *value, int64_t kv_ro
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
+pa_status pa_reshape_and_cache_int8(const void *key, const void *value, int64_t kv_row_stride,
+                                    void *key_cache, void *value_cache,
+                                    const int64_t *slot_mapping, int32_t num_tokens,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                    int64_t num_blocks, const float *k_scale,
+                                    const float *v_scale, pa_dtype dtype, int32_t *d_error,
+                                    void *stream) {
+  pa::ReshapeArgs w;
+  bool empty = true;
+  const pa_status st = prepare_write(key, value, kv_row_stride, key_cache, value_cache,
+                                     slot_mapping, num_tokens, num_kv_heads, head_dim, block_size,
+                                     num_blocks, dtype, d_error, &w, &empty);
+  if (st != PA_OK) return st;
+  if (!k_scale || !v_scale) return PA_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(k_scale) | reinterpret_cast<uintptr_t>(v_scale)) & 3u)
+    return PA_ERR_ALIGN;
+  // int8 pool rows in 16-byte chunks, a chunk within one head
+  if (head_dim % 16 != 0) return PA_ERR_ALIGN;
+  if (empty) return PA_OK;
+  w.int8 = true;
+  w.dtype = dtype;
+  w.head_dim = head_dim;
+  w.k_scale = k_scale;
+  w.v_scale = v_scale;
+  cudaError_t e = current_num_sms(&w.num_sms);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = pa::launch_reshape_and_cache(w, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
 pa_status pa_decode_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                          int32_t head_dim, int32_t max_context_len, int32_t partition_size,
                          int32_t *partition_size_out, size_t *workspace_bytes_out) {
@@ -247,7 +283,9 @@ pa_status decode_call(void *out, int64_t out_row_stride, const void *query, int6
                       int64_t num_blocks, float scale, int32_t max_context_len,
                       int32_t partition_size, void *workspace, size_t workspace_bytes,
                       pa_dtype dtype, int32_t *d_error, void *stream,
-                      const pa::ReshapeArgs *write) {
+                      const pa::ReshapeArgs *write, const float *k_scale = nullptr,
+                      const float *v_scale = nullptr) {
+  const bool int8 = k_scale != nullptr || v_scale != nullptr;
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq < 0 || max_context_len < 0 ||
       partition_size < 0)
@@ -259,6 +297,7 @@ pa_status decode_call(void *out, int64_t out_row_stride, const void *query, int6
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (num_q_heads / num_kv_heads > pa::kDecodeMaxGroup) return PA_ERR_UNSUPPORTED;
   if (!valid_block_size(block_size)) return PA_ERR_UNSUPPORTED;
+  if (int8 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (num_blocks * block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
   if (partition_size % pa::kDecodeSub != 0) return PA_ERR_SHAPE;
   if (num_seqs == 0) return PA_OK;
@@ -269,6 +308,11 @@ pa_status decode_call(void *out, int64_t out_row_stride, const void *query, int6
   if (q_row_stride % 8 || out_row_stride % 8) return PA_ERR_ALIGN;
   if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache))
     return PA_ERR_ALIGN;
+  if (int8) {
+    if (!k_scale || !v_scale) return PA_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(k_scale) | reinterpret_cast<uintptr_t>(v_scale)) & 3u)
+      return PA_ERR_ALIGN;
+  }
 
   int32_t P = 0;
   size_t need = 0;
@@ -337,15 +381,18 @@ pa_status decode_call(void *out, int64_t out_row_stride, const void *query, int6
   a.dtype = dtype;
   a.box_rows = block_size < pa::kDecodeSub ? block_size : pa::kDecodeSub;
   // The item schedule keeps per-sequence prefix sums in shared memory.
-  if (pa::decode_smem_bytes(head_dim, num_seqs, P, block_size) > 227 * 1024)
+  if (pa::decode_smem_bytes(head_dim, num_seqs, P, block_size, int8) > 227 * 1024)
     return PA_ERR_UNSUPPORTED;
   const int64_t rows = num_blocks * block_size;
   const int64_t row_stride = static_cast<int64_t>(num_kv_heads) * head_dim;
   if (!encode_rows_map(&a.tm_k, key_cache, dtype, head_dim, num_kv_heads, rows, row_stride,
-                       a.box_rows) ||
+                       a.box_rows, int8) ||
       !encode_rows_map(&a.tm_v, value_cache, dtype, head_dim, num_kv_heads, rows, row_stride,
-                       a.box_rows))
+                       a.box_rows, int8))
     return cuda_fail(cudaErrorInvalidValue);
+  a.kv_int8 = int8;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   a.after_write = false;
   if (write) {
     pa::ReshapeArgs w = *write;
@@ -375,6 +422,24 @@ pa_status pa_decode(void *out, int64_t out_row_stride, const void *query, int64_
                      num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
                      max_context_len, partition_size, workspace, workspace_bytes, dtype, d_error,
                      stream, nullptr);
+}
+
+pa_status pa_decode_int8(void *out, int64_t out_row_stride, const void *query,
+                         int64_t q_row_stride, const void *key_cache, const void *value_cache,
+                         const int32_t *block_table, int64_t block_table_stride,
+                         int32_t max_blocks_per_seq, const int32_t *context_lens,
+                         int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                         const float *k_scale, const float *v_scale, float scale,
+                         int32_t max_context_len, int32_t partition_size, void *workspace,
+                         size_t workspace_bytes, pa_dtype dtype, int32_t *d_error,
+                         void *stream) {
+  if (!k_scale || !v_scale) return PA_ERR_NULL;
+  return decode_call(out, out_row_stride, query, q_row_stride, key_cache, value_cache,
+                     block_table, block_table_stride, max_blocks_per_seq, context_lens, num_seqs,
+                     num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                     max_context_len, partition_size, workspace, workspace_bytes, dtype, d_error,
+                     stream, nullptr, k_scale, v_scale);
 }
 
 pa_status pa_decode_write(void *out, int64_t out_row_stride, const void *query,

@@ -22,6 +22,12 @@ struct ReshapeArgs {
   int64_t num_slots;  // num_blocks * block_size
   int32_t *d_error;
   int num_sms;
+  // INT8 pools: the inputs are `dtype` (fp16/bf16), the pools int8 codes
+  // under the per-KV-head scales; row_bytes counts the 16-bit input row.
+  bool int8 = false;
+  pa_dtype dtype = PA_F16;
+  int32_t head_dim = 0;
+  const float *k_scale = nullptr, *v_scale = nullptr;
 };
 cudaError_t launch_reshape_and_cache(const ReshapeArgs &a, cudaStream_t stream);
 
@@ -77,12 +83,15 @@ struct DecodeArgs {
   bool after_write;
   int32_t *d_error;
   pa_dtype dtype;
-  CUtensorMap tm_k, tm_v;  // pool maps, box (64, 1, box_rows), 128B swizzle
+  CUtensorMap tm_k, tm_v;  // pool maps, box (64 | 128 for INT8, 1, box_rows), 128B swizzle
   int box_rows;
   int num_sms;
+  bool kv_int8 = false;  // INT8 pools (head_dim 128) with per-KV-head scales
+  const float *k_scale = nullptr, *v_scale = nullptr;
 };
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
-size_t decode_smem_bytes(int head_dim, int num_seqs, int partition_size, int block_size);
+size_t decode_smem_bytes(int head_dim, int num_seqs, int partition_size, int block_size,
+                         bool kv_int8 = false);
 
 struct PrefillArgs {
   void *out;

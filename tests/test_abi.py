@@ -145,3 +145,40 @@ def test_decode_write_checks_both_halves_before_enqueueing(lib, kw, status):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         pa.library(str(tmp_path / "libpa.so"))
+
+
+def decode_int8_call(lib, **kw):
+    a = dict(out=FAKE, out_stride=8 * 128, q=FAKE, q_stride=8 * 128, kc=FAKE, vc=FAKE,
+             bt=FAKE, bt_stride=16, mbps=16, ctx=FAKE, s=4, hq=8, hkv=2, d=128, bs=16,
+             nb=64, ks=FAKE, vs=FAKE, scale=0.125, maxctx=100, part=0, dtype=1)
+    a.update(kw)
+    return lib.pa_decode_int8(a["out"], a["out_stride"], a["q"], a["q_stride"], a["kc"],
+                              a["vc"], a["bt"], a["bt_stride"], a["mbps"], a["ctx"], a["s"],
+                              a["hq"], a["hkv"], a["d"], a["bs"], a["nb"], a["ks"], a["vs"],
+                              a["scale"], a["maxctx"], a["part"], None, 0, a["dtype"], None,
+                              None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(ks=None), 1),                     # the per-head scales are required
+    (dict(vs=None), 1),
+    (dict(ks=ctypes.c_void_p(0x10002)), 4),  # scales are fp32: 4-byte aligned
+    (dict(d=64), 3),                        # INT8 pools: head_dim 128 only
+    (dict(hkv=3), 2),                       # Hq % Hkv != 0
+    (dict(kc=MISALIGNED), 4),
+    (dict(q=None), 1),
+])
+def test_decode_int8_host_validation(lib, kw, status):
+    assert decode_int8_call(lib, **kw) == status
+
+
+def test_reshape_int8_host_validation(lib):
+    f = lib.pa_reshape_and_cache_int8
+    # key, value, stride, k_cache, v_cache, slots, n, hkv, d, bs, nb, k_scale, v_scale, dtype
+    assert f(FAKE, FAKE, 256, FAKE, FAKE, FAKE, 0, 2, 128, 16, 8, FAKE, FAKE, 0, None, None) == 0
+    assert f(FAKE, FAKE, 256, FAKE, FAKE, FAKE, 3, 2, 128, 16, 8, None, FAKE, 0, None, None) == 1
+    assert f(FAKE, FAKE, 256, FAKE, FAKE, FAKE, 3, 2, 128, 16, 8, FAKE,
+             ctypes.c_void_p(0x10002), 0, None, None) == 4
+    # head_dim 40: 16-bit rows are fine, but an int8 pool row chunk would span heads
+    assert f(FAKE, FAKE, 80, FAKE, FAKE, FAKE, 3, 2, 40, 16, 8, FAKE, FAKE, 0, None, None) == 4
+    assert f(None, FAKE, 256, FAKE, FAKE, FAKE, 3, 2, 128, 16, 8, FAKE, FAKE, 0, None, None) == 1
