@@ -57,27 +57,24 @@ namespace {
 
 constexpr int kWorkers = kDecodeWarps;
 constexpr int kThreads = (kWorkers + 1) * 32;  // + producer warp
-constexpr int kStages = 3;
 constexpr int kSub = kDecodeSub;               // tokens per worker per stage
 constexpr int kHalfBytes = kWorkers * kSub * 128;  // 64 rows x 64 elements x 2 B
 constexpr uint32_t kTerminate = 0x100u;        // stage header: no more data
 
 // A stage holds, per K and V, `kRegions` regions of kWorkers x kSub rows of
 // 128 bytes (128-byte swizzle): 16-bit pools in 64-element halves, INT8 pools
-// (head_dim 128) in one region of whole rows.  INT8 stages are widened by
-// each worker into its own fp16 scratch (two 64-element halves of kSub rows
-// for K and for V) that the tensor-core code reads like a 16-bit stage.
+// (head_dim 128) in one region of whole rows.  INT8 stages are half the
+// bytes, so there are twice as many: the same bytes in flight per CTA.
 template <int D, bool KV8 = false>
 struct DecodeSmem {
+  static constexpr int kStages = KV8 ? 6 : 3;
   static constexpr int kHalves = D / 64;
   static constexpr int kRegions = KV8 ? 1 : kHalves;
   static constexpr int kStageBytes = 2 * kRegions * kHalfBytes;  // K + V
-  static constexpr int kScratchHalf = kSub * 128;                 // one worker, one half
-  static constexpr int kScratchWorker = 2 * kHalves * kScratchHalf;
-  static constexpr int kScratchOffset = kStages * kStageBytes;
-  static constexpr int kBarOffset = kScratchOffset + (KV8 ? kWorkers * kScratchWorker : 0);
+  static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kHdrOffset = kBarOffset + 2 * kStages * 8;
-  static constexpr int kVarOffset = kHdrOffset + 32;  // pref[S+1], len[S], ids
+  static constexpr int kAbortOffset = kHdrOffset + 32;  // after kStages (<= 8) headers
+  static constexpr int kVarOffset = kAbortOffset + 16;  // pref[S+1], len[S], ids
   static int bytes(int num_seqs, int max_ids) {
     return 1024 + kVarOffset + 4 * (2 * num_seqs + 1) + 4 * kWorkers * 2 * max_ids;
   }
@@ -239,20 +236,28 @@ __device__ __forceinline__ uint32_t q_pair(uint32_t w) {
   return w;
 }
 
-template <class E, int D, bool TOF16 = false>
+// The query as the B operand of S^T = K Q^T: lane (head qh = lane / 4,
+// t = lane % 4) feeds k-step ks.  16-bit pools: elements 16ks + 2t, +1 and
+// 16ks + 2t + 8, +9 (the ldmatrix order of K).  INT8 pools (D = 128, fp16
+// operands): elements 32t + 4ks .. 32t + 4ks + 3, the order in which the
+// K fragments are widened -- a dot product over D takes any order both
+// operands share.
+template <class E, int D, bool KV8 = false>
 __device__ __forceinline__ void load_q(uint32_t (&qf)[D / 16][2], const DecodeParams &p,
                                        const Item &m, int lane) {
+  static_assert(!KV8 || D == 128, "INT8 pools: head_dim 128");
   const int G = p.group;
   const int qh = lane >> 2;  // head column this lane feeds to Q^T
   const typename E::T *qrow = static_cast<const typename E::T *>(p.q) +
-                              m.b * p.q_row_stride + (m.g * G + qh) * D + 2 * (lane & 3);
+                              m.b * p.q_row_stride + (m.g * G + qh) * D +
+                              (KV8 ? 32 : 2) * (lane & 3);
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
-    qf[ks][0] = qh < G ? q_pair<E, TOF16>(__ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16)))
-                       : 0u;
+    const int e0 = KV8 ? 4 * ks : 16 * ks, e1 = KV8 ? 4 * ks + 2 : 16 * ks + 8;
+    qf[ks][0] =
+        qh < G ? q_pair<E, KV8>(__ldg(reinterpret_cast<const uint32_t *>(qrow + e0))) : 0u;
     qf[ks][1] =
-        qh < G ? q_pair<E, TOF16>(__ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8)))
-               : 0u;
+        qh < G ? q_pair<E, KV8>(__ldg(reinterpret_cast<const uint32_t *>(qrow + e1))) : 0u;
   }
 }
 
@@ -271,27 +276,21 @@ __device__ __forceinline__ void widen4(uint32_t w, uint32_t &lo, uint32_t &hi) {
   hi = *reinterpret_cast<uint32_t *>(&hb);
 }
 
-// One worker's kSub int8 rows of 128 codes (a TMA tile with the 128-byte
-// swizzle: 16-byte chunk j of row r at chunk j ^ (r & 7)) -> fp16 rows in two
-// 64-element halves of the same swizzled layout, kScratchHalf bytes apart.
-// Lane l widens row l / 2, half l % 2.
-template <class S>
-__device__ __forceinline__ void widen_rows(const uint8_t *src, uint8_t *dst, int lane) {
-  const int r = lane >> 1, h = lane & 1;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int j = h * 4 + q;  // int8 chunk: elements 16j .. 16j+15
-    const uint4 c = *reinterpret_cast<const uint4 *>(src + r * 128 + ((j ^ (r & 7)) << 4));
-    uint4 a, b;  // fp16 elements 16j .. 16j+7 and 16j+8 .. 16j+15
-    widen4(c.x, a.x, a.y);
-    widen4(c.y, a.z, a.w);
-    widen4(c.z, b.x, b.y);
-    widen4(c.w, b.z, b.w);
-    const int c0 = (2 * j) & 7, c1 = (2 * j + 1) & 7;  // fp16 chunks within half h
-    uint8_t *row = dst + h * S::kScratchHalf + r * 128;
-    *reinterpret_cast<uint4 *>(row + ((c0 ^ (r & 7)) << 4)) = a;
-    *reinterpret_cast<uint4 *>(row + ((c1 ^ (r & 7)) << 4)) = b;
-  }
+// Two int8 words a, b holding the same four elements of two tokens -> the
+// fp16 pairs (a.byte i, b.byte i): e0 for i = 0, e1 for 1, e2 for 2, e3 for 3.
+__device__ __forceinline__ void widen_tokens(uint32_t a, uint32_t b, uint32_t &e0,
+                                             uint32_t &e1, uint32_t &e2, uint32_t &e3) {
+  uint32_t x, y;
+  asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(x) : "r"(a), "r"(b));
+  asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(y) : "r"(a), "r"(b));
+  widen4(x, e0, e1);
+  widen4(y, e2, e3);
+}
+
+__device__ __forceinline__ void lds128(uint32_t addr, uint32_t (&w)[4]) {
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+               : "r"(addr));
 }
 
 template <class E, int D, int BOXR, bool BAL, bool KV8>
@@ -303,14 +302,16 @@ __global__ void __launch_bounds__(kThreads, 2)
   constexpr int NH = S::kHalves;
   constexpr int NR = S::kRegions;
   constexpr int KSTEPS = D / 16;
+  constexpr int NS = S::kStages;
+  static_assert(NS <= 8, "stage headers");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::kBarOffset);
-  uint64_t *empty = full + kStages;
+  uint64_t *empty = full + NS;
   volatile uint32_t *s_hdr = reinterpret_cast<volatile uint32_t *>(smem + S::kHdrOffset);
-  volatile int *s_abort = reinterpret_cast<volatile int *>(smem + S::kHdrOffset + 16);
+  volatile int *s_abort = reinterpret_cast<volatile int *>(smem + S::kAbortOffset);
   int *s_pref = reinterpret_cast<int *>(smem + S::kVarOffset);
   int *s_len = s_pref + p.num_seqs + 1;
   int *s_ids = s_len + p.num_seqs;  // [kWorkers][2][max_ids]
@@ -325,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (!p.after_write) griddep_wait();
   griddep_launch_dependents();
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(smem_u32(full + s), 1);
       mbar_init(smem_u32(empty + s), kWorkers);
     }
@@ -434,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     act = true;
     const int *ids = s_ids;
     for (int c = 0;; ++c) {
-      const int s = c % kStages;
+      const int s = c % NS;
       int rows[kSub / BOXR];
       int nb = 0;
       bool bad = false;
@@ -475,16 +476,16 @@ __global__ void __launch_bounds__(kThreads, 2)
       nbox += __shfl_xor_sync(0xffffffffu, nbox, 1);
       nbox += __shfl_xor_sync(0xffffffffu, nbox, 2);  // lanes 0-3 hold all feeders
       bool ok = true;
-      if (lane == 0 && c >= kStages)
-        ok = mbar_wait_bounded(smem_u32(empty + s), ((c / kStages) - 1) & 1);
+      if (lane == 0 && c >= NS)
+        ok = mbar_wait_bounded(smem_u32(empty + s), ((c / NS) - 1) & 1);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok || *s_abort) {
         if (lane == 0) {
           if (!ok) raise_error(p.err, PA_DEVERR_TIMEOUT);
           *s_abort = 1;
           // Do not leave while copies this CTA issued may still land.
-          for (int k = c - 1; k >= 0 && k >= c - kStages; --k)
-            mbar_wait_bounded(smem_u32(full + (k % kStages)), (k / kStages) & 1);
+          for (int k = c - 1; k >= 0 && k >= c - NS; --k)
+            mbar_wait_bounded(smem_u32(full + (k % NS)), (k / NS) & 1);
         }
         cp_async_wait_all();
         return;
@@ -556,6 +557,57 @@ __global__ void __launch_bounds__(kThreads, 2)
       l0 += shfl_xor(l0, s);
       l1 += shfl_xor(l1, s);
     }
+    if constexpr (KV8) {
+      // O^T rows in the INT8 order: lane (g, t) holds elements 16g .. 16g + 15
+      // of heads 2t and 2t + 1, element 16g + i in o[i / 2][i % 2 ? 2 : 0]
+      // (head 2t) and o[i / 2][i % 2 ? 3 : 1] (head 2t + 1).
+      const int e0 = 16 * (lane >> 2);
+      if (m.direct) {
+        typename E::T *out =
+            static_cast<typename E::T *>(p.out) + m.b * p.out_row_stride + m.g * G * D + e0;
+        const float i0 = (!bad_item && l0 > 0.f) ? vsc / l0 : 0.f;
+        const float i1 = (!bad_item && l1 > 0.f) ? vsc / l1 : 0.f;
+        uint32_t u0[8], u1[8];
+#pragma unroll
+        for (int mt = 0; mt < KSTEPS; ++mt) {
+          u0[mt] = E::pack2(o[mt][0] * i0, o[mt][2] * i0);
+          u1[mt] = E::pack2(o[mt][1] * i1, o[mt][3] * i1);
+        }
+        if (h0 < G) {
+          uint4 *d0 = reinterpret_cast<uint4 *>(out + h0 * D);
+          d0[0] = make_uint4(u0[0], u0[1], u0[2], u0[3]);
+          d0[1] = make_uint4(u0[4], u0[5], u0[6], u0[7]);
+        }
+        if (h1 < G) {
+          uint4 *d1 = reinterpret_cast<uint4 *>(out + h1 * D);
+          d1[0] = make_uint4(u1[0], u1[1], u1[2], u1[3]);
+          d1[1] = make_uint4(u1[4], u1[5], u1[6], u1[7]);
+        }
+      } else {
+        const float f = bad_item ? 0.f : vsc;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int h = h0 + hh;
+          if (h >= G) continue;
+          float4 *w = reinterpret_cast<float4 *>(p.ws_o + (m.prow + h * m.pstride) * D + e0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            w[q] = make_float4(o[2 * q][hh] * f, o[2 * q][hh + 2] * f, o[2 * q + 1][hh] * f,
+                               o[2 * q + 1][hh + 2] * f);
+        }
+        if (lane < 4) {
+          if (h0 < G) {
+            p.ws_ml[(m.prow + h0 * m.pstride) * 2 + 0] = bad_item ? -INFINITY : m0;
+            p.ws_ml[(m.prow + h0 * m.pstride) * 2 + 1] = bad_item ? 0.f : l0;
+          }
+          if (h1 < G) {
+            p.ws_ml[(m.prow + h1 * m.pstride) * 2 + 0] = bad_item ? -INFINITY : m1;
+            p.ws_ml[(m.prow + h1 * m.pstride) * 2 + 1] = bad_item ? 0.f : l1;
+          }
+        }
+      }
+      return;
+    }
     if (m.direct) {
       const float i0 = (!bad_item && l0 > 0.f) ? 1.f / l0 : 0.f;
       const float i1 = (!bad_item && l1 > 0.f) ? 1.f / l1 : 0.f;
@@ -565,12 +617,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int mt = 0; mt < KSTEPS; ++mt) {
         const int d0 = mt * 16 + (lane >> 2), d1 = d0 + 8;
         if (h0 < G) {
-          out[h0 * D + d0] = E::from_float(o[mt][0] * (i0 * vsc));
-          out[h0 * D + d1] = E::from_float(o[mt][2] * (i0 * vsc));
+          out[h0 * D + d0] = E::from_float(o[mt][0] * i0);
+          out[h0 * D + d1] = E::from_float(o[mt][2] * i0);
         }
         if (h1 < G) {
-          out[h1 * D + d0] = E::from_float(o[mt][1] * (i1 * vsc));
-          out[h1 * D + d1] = E::from_float(o[mt][3] * (i1 * vsc));
+          out[h1 * D + d0] = E::from_float(o[mt][1] * i1);
+          out[h1 * D + d1] = E::from_float(o[mt][3] * i1);
         }
       }
     } else {
@@ -581,13 +633,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int d0 = mt * 16 + (lane >> 2), d1 = d0 + 8;
         if (h0 < G) {
           float *w0 = p.ws_o + (row0 + h0 * hstride) * D;
-          w0[d0] = bad_item ? 0.f : o[mt][0] * vsc;
-          w0[d1] = bad_item ? 0.f : o[mt][2] * vsc;
+          w0[d0] = bad_item ? 0.f : o[mt][0];
+          w0[d1] = bad_item ? 0.f : o[mt][2];
         }
         if (h1 < G) {
           float *w1 = p.ws_o + (row0 + h1 * hstride) * D;
-          w1[d0] = bad_item ? 0.f : o[mt][1] * vsc;
-          w1[d1] = bad_item ? 0.f : o[mt][3] * vsc;
+          w1[d0] = bad_item ? 0.f : o[mt][1];
+          w1[d1] = bad_item ? 0.f : o[mt][3];
         }
       }
       if (lane < 4) {
@@ -659,12 +711,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   bool active = false, need_piece = true;
 
   for (int c = 0;; ++c) {
-    const int s = c % kStages;
+    const int s = c % NS;
     if (need_piece) {
       active = begin();
       need_piece = false;
     }
-    if (!mbar_wait_bounded(smem_u32(full + s), (c / kStages) & 1)) {
+    if (!mbar_wait_bounded(smem_u32(full + s), (c / NS) & 1)) {
       raise_error(p.err, PA_DEVERR_TIMEOUT);
       *s_abort = 1;
       break;
@@ -676,53 +728,73 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int end = cur_item.end;
       const int j0 = cur;
       uint8_t *kst = smem + s * S::kStageBytes;
-      // Where this worker's K and V rows are read from: the stage itself,
-      // rows r0.. of halves kHalfBytes apart, or (INT8) its fp16 scratch,
-      // rows 0.. of halves kScratchHalf apart.
-      constexpr int HB = KV8 ? S::kScratchHalf : kHalfBytes;
-      const int rb = KV8 ? 0 : r0;
-      uint32_t kb, vb;
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
       bool zeroed = false;
+      uint32_t vw[4][4];  // INT8: this lane's V codes (see below)
       if constexpr (KV8) {
-        // Widen this worker's int8 rows (finite whatever the pool held, so
-        // rows past the context need no clearing), then hand the stage back.
-        uint8_t *scr = smem + S::kScratchOffset + warp * S::kScratchWorker;
-        __syncwarp();  // the previous stage's reads of the scratch are done
-        widen_rows<S>(kst + r0 * 128, scr, lane);
-        widen_rows<S>(kst + kHalfBytes + r0 * 128, scr + NH * S::kScratchHalf, lane);
+        // This worker's 16 int8 K and V rows go straight to registers and
+        // the stage is handed back before any arithmetic.  Codes widen to
+        // exact fp16 whatever the pool held, so rows past the context need
+        // no clearing: their weight is zero.
+        //  K, the A operand of S^T = K Q^T (rows: tokens g, g + 8): k-step
+        //   ks of lane (g, t) is elements 32t + 4ks .. +3 of its two rows
+        //   (16-byte chunks 2t and 2t + 1), the query following suit.
+        //  V, the A operand of O^T += V^T P^T (rows: elements of D;
+        //   columns: tokens 2t, 2t + 1, 2t + 8, 2t + 9): the D order of O^T
+        //   is free as well, so lane (g, t) owns elements 16g .. 16g + 15
+        //   (chunk g of its four token rows), row g of M-tile mt holding
+        //   element 16g + 2mt and row g + 8 element 16g + 2mt + 1.
+        const int g8 = lane >> 2, t4 = lane & 3;
+        const uint32_t kr = smem_u32(kst) + r0 * 128;
+        const uint32_t vr = kr + kHalfBytes;
+        uint32_t kw[2][2][4];  // [row g8 | g8 + 8][chunk 2t | 2t + 1][word]
+        // 128-byte swizzle: chunk c of row r sits at chunk c ^ (r & 7).
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            lds128(kr + (g8 + 8 * r) * 128 + (((2 * t4 + c) ^ g8) << 4), kw[r][c]);
+        const int v0 = 2 * t4;
+        lds128(vr + v0 * 128 + ((g8 ^ v0) << 4), vw[0]);
+        lds128(vr + (v0 + 1) * 128 + ((g8 ^ (v0 + 1)) << 4), vw[1]);
+        lds128(vr + (v0 + 8) * 128 + ((g8 ^ v0) << 4), vw[2]);
+        lds128(vr + (v0 + 9) * 128 + ((g8 ^ (v0 + 1)) << 4), vw[3]);
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(empty + s));
         released = true;
-        kb = smem_u32(scr);
-        vb = kb + NH * S::kScratchHalf;
-      } else {
-        kb = smem_u32(kst);
-        vb = kb + NH * kHalfBytes;
-      }
-      if (!KV8 && j0 + kSub > end) {
-        // Rows past the context may hold anything (even NaN); their weight is
-        // zero, so make their V rows exact zeros before the P.V product.
-        uint8_t *vrows = kst + NH * kHalfBytes;
-        for (int i = lane; i < kSub * NH * 8; i += 32) {
-          const int rr = i / (NH * 8), h = (i / 8) % NH, cc = i % 8;
-          if (j0 + rr >= end)
-            *reinterpret_cast<uint4 *>(vrows + h * kHalfBytes + (r0 + rr) * 128 + cc * 16) =
-                make_uint4(0, 0, 0, 0);
-        }
-        __syncwarp();
-        zeroed = true;
-      }
-      // S^T = K Q^T for this worker's 16 tokens.
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int ks = 0; ks < KSTEPS; ++ks) {
-        const int row = rb + (mj & 1) * 8 + mr;
-        const int c16 = ks * 2 + (mj >> 1);
-        const uint32_t addr =
-            kb + (c16 >> 3) * HB + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
-        uint32_t a0, a1, a2, a3;
-        ldmatrix_x4(addr, a0, a1, a2, a3);
-        mma_16816<M::kBF16>(sc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          widen4(kw[0][ks >> 2][ks & 3], a0, a2);
+          widen4(kw[1][ks >> 2][ks & 3], a1, a3);
+          mma_16816<false>(sc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+        }
+      } else {
+        const uint32_t kb = smem_u32(kst);
+        if (j0 + kSub > end) {
+          // Rows past the context may hold anything (even NaN); their weight
+          // is zero, so make their V rows exact zeros before the P.V product.
+          uint8_t *vrows = kst + NH * kHalfBytes;
+          for (int i = lane; i < kSub * NH * 8; i += 32) {
+            const int rr = i / (NH * 8), h = (i / 8) % NH, cc = i % 8;
+            if (j0 + rr >= end)
+              *reinterpret_cast<uint4 *>(vrows + h * kHalfBytes + (r0 + rr) * 128 + cc * 16) =
+                  make_uint4(0, 0, 0, 0);
+          }
+          __syncwarp();
+          zeroed = true;
+        }
+        // S^T = K Q^T for this worker's 16 tokens.
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+          const int row = r0 + (mj & 1) * 8 + mr;
+          const int c16 = ks * 2 + (mj >> 1);
+          const uint32_t addr =
+              kb + (c16 >> 3) * kHalfBytes + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
+          uint32_t a0, a1, a2, a3;
+          ldmatrix_x4(addr, a0, a1, a2, a3);
+          mma_16816<E::kBF16>(sc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+        }
       }
       const int t0 = j0 + (lane >> 2), t1 = t0 + 8;
       const float s00 = t0 < end ? sc[0] * sl : -INFINITY;
@@ -757,15 +829,28 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint32_t pb0 = movmatrix_trans(w0);
       const uint32_t pb1 = movmatrix_trans(w1);
       // O^T += V^T P^T, one 16-wide slice of D at a time.
+      if constexpr (KV8) {
+        // Word w of the four token rows: M-tiles 2w and 2w + 1.
 #pragma unroll
-      for (int mt = 0; mt < KSTEPS; ++mt) {
-        const int row = rb + (mj >> 1) * 8 + mr;
-        const int c16 = mt * 2 + (mj & 1);
-        const uint32_t addr =
-            vb + (c16 >> 3) * HB + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
-        uint32_t a0, a1, a2, a3;
-        ldmatrix_x4_trans(addr, a0, a1, a2, a3);
-        mma_16816<M::kBF16>(o[mt], a0, a1, a2, a3, pb0, pb1);
+        for (int w = 0; w < 4; ++w) {
+          uint32_t a0, a1, b0, b1, a2, a3, b2, b3;
+          widen_tokens(vw[0][w], vw[1][w], a0, a1, b0, b1);  // tokens 2t, 2t + 1
+          widen_tokens(vw[2][w], vw[3][w], a2, a3, b2, b3);  // tokens 2t + 8, 2t + 9
+          mma_16816<false>(o[2 * w], a0, a1, a2, a3, pb0, pb1);
+          mma_16816<false>(o[2 * w + 1], b0, b1, b2, b3, pb0, pb1);
+        }
+      } else {
+        const uint32_t vb = smem_u32(kst) + NH * kHalfBytes;
+#pragma unroll
+        for (int mt = 0; mt < KSTEPS; ++mt) {
+          const int row = r0 + (mj >> 1) * 8 + mr;
+          const int c16 = mt * 2 + (mj & 1);
+          const uint32_t addr =
+              vb + (c16 >> 3) * kHalfBytes + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
+          uint32_t a0, a1, a2, a3;
+          ldmatrix_x4_trans(addr, a0, a1, a2, a3);
+          mma_16816<E::kBF16>(o[mt], a0, a1, a2, a3, pb0, pb1);
+        }
       }
       if (zeroed) fence_proxy_async_smem();  // generic writes before the next TMA
       if (hdr & (1u << warp)) item_bad = true;
