@@ -57,20 +57,21 @@ namespace {
 
 constexpr int kWorkers = kDecodeWarps;
 constexpr int kThreads = (kWorkers + 1) * 32;  // + producer warp
-constexpr int kSub = kDecodeSub;               // tokens per worker per stage
-constexpr int kHalfBytes = kWorkers * kSub * 128;  // 64 rows x 64 elements x 2 B
 constexpr uint32_t kTerminate = 0x100u;        // stage header: no more data
 
-// A stage holds, per K and V, `kRegions` regions of kWorkers x kSub rows of
-// 128 bytes (128-byte swizzle): 16-bit pools in 64-element halves, INT8 pools
-// (head_dim 128) in one region of whole rows.  INT8 stages are half the
-// bytes, so there are twice as many: the same bytes in flight per CTA.
+// A stage holds, per K and V, `kRegions` regions of kWorkers x kRows rows of
+// 128 bytes (128-byte swizzle): 16-bit pools in 64-element halves, 16 rows
+// per worker; INT8 pools (head_dim 128) in one region of whole rows, 32 rows
+// per worker -- the same bytes per stage, and twice the tokens per softmax
+// step for the widening consumer.
 template <int D, bool KV8 = false>
 struct DecodeSmem {
-  static constexpr int kStages = KV8 ? 6 : 3;
+  static constexpr int kStages = 3;
+  static constexpr int kRows = KV8 ? 2 * kDecodeSub : kDecodeSub;  // per worker
+  static constexpr int kRegionBytes = kWorkers * kRows * 128;
   static constexpr int kHalves = D / 64;
   static constexpr int kRegions = KV8 ? 1 : kHalves;
-  static constexpr int kStageBytes = 2 * kRegions * kHalfBytes;  // K + V
+  static constexpr int kStageBytes = 2 * kRegions * kRegionBytes;  // K + V
   static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kHdrOffset = kBarOffset + 2 * kStages * 8;
   static constexpr int kAbortOffset = kHdrOffset + 32;  // after kStages (<= 8) headers
@@ -303,6 +304,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   constexpr int NR = S::kRegions;
   constexpr int KSTEPS = D / 16;
   constexpr int NS = S::kStages;
+  constexpr int ROWS = S::kRows;       // tokens per worker per stage
+  constexpr int RB = S::kRegionBytes;  // one region of a stage
+  constexpr int NT = ROWS / 16;        // score tiles per stage
   static_assert(NS <= 8, "stage headers");
 
   extern __shared__ uint8_t smem_raw[];
@@ -436,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int *ids = s_ids;
     for (int c = 0;; ++c) {
       const int s = c % NS;
-      int rows[kSub / BOXR];
+      int rows[ROWS / BOXR];
       int nb = 0;
       bool bad = false;
       if (feeder) {
@@ -447,11 +451,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (act && cur >= endt) promote();
         ids = s_ids + (lane * 2 + sel) * p.max_ids;
 #pragma unroll
-        for (int k = 0; k < kSub / BOXR; ++k) rows[k] = -1;
+        for (int k = 0; k < ROWS / BOXR; ++k) rows[k] = -1;
         if (act) {
-          const int ntok = min(kSub, endt - cur);
+          const int ntok = min(ROWS, endt - cur);
 #pragma unroll
-          for (int k = 0; k < kSub / BOXR; ++k) {
+          for (int k = 0; k < ROWS / BOXR; ++k) {
             if (k * BOXR >= ntok) break;
             const int id = ids[lblk];
             if (id >= 0 && id < p.num_blocks) {
@@ -466,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 2)
               ++lblk;
             }
           }
-          cur += kSub;
+          cur += ROWS;
         }
       }
       if (c == 0 && p.after_write) griddep_wait();  // the cache write has landed
@@ -508,15 +512,15 @@ __global__ void __launch_bounds__(kThreads, 2)
       __syncwarp();
       if (feeder) {
         const uint32_t kdst = smem_u32(smem + s * S::kStageBytes);
-        const uint32_t vdst = kdst + NR * kHalfBytes;
+        const uint32_t vdst = kdst + NR * RB;
 #pragma unroll
-        for (int k = 0; k < kSub / BOXR; ++k) {
+        for (int k = 0; k < ROWS / BOXR; ++k) {
           if (rows[k] < 0) continue;
-          const uint32_t o = (lane * kSub + k * BOXR) * 128;
+          const uint32_t o = (lane * ROWS + k * BOXR) * 128;
 #pragma unroll
           for (int h = 0; h < NR; ++h) {
-            tma_load_3d(kdst + h * kHalfBytes + o, &tmk, bar, h * 64, gq, rows[k]);
-            tma_load_3d(vdst + h * kHalfBytes + o, &tmv, bar, h * 64, gq, rows[k]);
+            tma_load_3d(kdst + h * RB + o, &tmk, bar, h * 64, gq, rows[k]);
+            tma_load_3d(vdst + h * RB + o, &tmv, bar, h * 64, gq, rows[k]);
           }
         }
       }
@@ -527,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int G = p.group;
   float sl = p.scale_log2;  // INT8 pools: times the piece's K scale
   float vsc = 1.f;          // INT8 pools: the piece's V scale
-  const int r0 = warp * kSub;  // this worker's rows in a stage
+  const int r0 = warp * ROWS;  // this worker's rows in a stage
   const int mj = lane >> 3, mr = lane & 7;
   const int h0 = 2 * (lane & 3), h1 = h0 + 1;
 
@@ -728,57 +732,69 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int end = cur_item.end;
       const int j0 = cur;
       uint8_t *kst = smem + s * S::kStageBytes;
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      float sc[NT][4];
+#pragma unroll
+      for (int u = 0; u < NT; ++u) sc[u][0] = sc[u][1] = sc[u][2] = sc[u][3] = 0.f;
       bool zeroed = false;
-      uint32_t vw[4][4];  // INT8: this lane's V codes (see below)
+      uint32_t vw[NT][4][4];  // INT8: this lane's V codes (see below)
       if constexpr (KV8) {
-        // This worker's 16 int8 K and V rows go straight to registers and
-        // the stage is handed back before any arithmetic.  Codes widen to
-        // exact fp16 whatever the pool held, so rows past the context need
-        // no clearing: their weight is zero.
-        //  K, the A operand of S^T = K Q^T (rows: tokens g, g + 8): k-step
-        //   ks of lane (g, t) is elements 32t + 4ks .. +3 of its two rows
+        // This worker's 32 int8 K and V rows (two 16-token tiles u) go
+        // straight to registers, and the stage is handed back once they are
+        // read.  Codes widen to exact fp16 whatever the pool held, so
+        // rows past the context need no clearing: their weight is zero.
+        //  K, the A operand of S^T = K Q^T (rows: tokens 16u + g, +8): k-step
+        //   ks of lane (g, t) is elements 32t + 4ks .. +3 of its rows
         //   (16-byte chunks 2t and 2t + 1), the query following suit.
         //  V, the A operand of O^T += V^T P^T (rows: elements of D;
-        //   columns: tokens 2t, 2t + 1, 2t + 8, 2t + 9): the D order of O^T
-        //   is free as well, so lane (g, t) owns elements 16g .. 16g + 15
-        //   (chunk g of its four token rows), row g of M-tile mt holding
-        //   element 16g + 2mt and row g + 8 element 16g + 2mt + 1.
+        //   columns: tokens 16u + 2t, +1, +8, +9): the D order of O^T is
+        //   free as well, so lane (g, t) owns elements 16g .. 16g + 15
+        //   (chunk g of its token rows), row g of M-tile mt holding element
+        //   16g + 2mt and row g + 8 element 16g + 2mt + 1.
+        // 128-byte swizzle: chunk c of row r sits at chunk c ^ (r & 7).
         const int g8 = lane >> 2, t4 = lane & 3;
         const uint32_t kr = smem_u32(kst) + r0 * 128;
-        const uint32_t vr = kr + kHalfBytes;
-        uint32_t kw[2][2][4];  // [row g8 | g8 + 8][chunk 2t | 2t + 1][word]
-        // 128-byte swizzle: chunk c of row r sits at chunk c ^ (r & 7).
+        const uint32_t vr = kr + RB;
+        uint32_t kw[NT][2][2][4];  // [tile][row g | g + 8][chunk 2t | 2t + 1][word]
 #pragma unroll
-        for (int r = 0; r < 2; ++r)
+        for (int u = 0; u < NT; ++u)
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
-            lds128(kr + (g8 + 8 * r) * 128 + (((2 * t4 + c) ^ g8) << 4), kw[r][c]);
+          for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+              lds128(kr + (16 * u + g8 + 8 * r) * 128 + (((2 * t4 + c) ^ g8) << 4), kw[u][r][c]);
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks)
+#pragma unroll
+          for (int u = 0; u < NT; ++u) {
+            uint32_t a0, a1, a2, a3;
+            widen4(kw[u][0][ks >> 2][ks & 3], a0, a2);
+            widen4(kw[u][1][ks >> 2][ks & 3], a1, a3);
+            mma_16816<false>(sc[u], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+          }
+        // V's codes once K's are spent (fewer live registers); their loads
+        // overlap the softmax below.
         const int v0 = 2 * t4;
-        lds128(vr + v0 * 128 + ((g8 ^ v0) << 4), vw[0]);
-        lds128(vr + (v0 + 1) * 128 + ((g8 ^ (v0 + 1)) << 4), vw[1]);
-        lds128(vr + (v0 + 8) * 128 + ((g8 ^ v0) << 4), vw[2]);
-        lds128(vr + (v0 + 9) * 128 + ((g8 ^ (v0 + 1)) << 4), vw[3]);
+#pragma unroll
+        for (int u = 0; u < NT; ++u) {
+          const uint32_t vu = vr + 16 * u * 128;
+          lds128(vu + v0 * 128 + ((g8 ^ v0) << 4), vw[u][0]);
+          lds128(vu + (v0 + 1) * 128 + ((g8 ^ (v0 + 1)) << 4), vw[u][1]);
+          lds128(vu + (v0 + 8) * 128 + ((g8 ^ v0) << 4), vw[u][2]);
+          lds128(vu + (v0 + 9) * 128 + ((g8 ^ (v0 + 1)) << 4), vw[u][3]);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(empty + s));
         released = true;
-#pragma unroll
-        for (int ks = 0; ks < KSTEPS; ++ks) {
-          uint32_t a0, a1, a2, a3;
-          widen4(kw[0][ks >> 2][ks & 3], a0, a2);
-          widen4(kw[1][ks >> 2][ks & 3], a1, a3);
-          mma_16816<false>(sc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
-        }
       } else {
         const uint32_t kb = smem_u32(kst);
-        if (j0 + kSub > end) {
+        if (j0 + ROWS > end) {
           // Rows past the context may hold anything (even NaN); their weight
           // is zero, so make their V rows exact zeros before the P.V product.
-          uint8_t *vrows = kst + NH * kHalfBytes;
-          for (int i = lane; i < kSub * NH * 8; i += 32) {
+          uint8_t *vrows = kst + NH * RB;
+          for (int i = lane; i < ROWS * NH * 8; i += 32) {
             const int rr = i / (NH * 8), h = (i / 8) % NH, cc = i % 8;
             if (j0 + rr >= end)
-              *reinterpret_cast<uint4 *>(vrows + h * kHalfBytes + (r0 + rr) * 128 + cc * 16) =
+              *reinterpret_cast<uint4 *>(vrows + h * RB + (r0 + rr) * 128 + cc * 16) =
                   make_uint4(0, 0, 0, 0);
           }
           __syncwarp();
@@ -790,18 +806,26 @@ __global__ void __launch_bounds__(kThreads, 2)
           const int row = r0 + (mj & 1) * 8 + mr;
           const int c16 = ks * 2 + (mj >> 1);
           const uint32_t addr =
-              kb + (c16 >> 3) * kHalfBytes + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
+              kb + (c16 >> 3) * RB + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
           uint32_t a0, a1, a2, a3;
           ldmatrix_x4(addr, a0, a1, a2, a3);
-          mma_16816<E::kBF16>(sc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+          mma_16816<E::kBF16>(sc[0], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
         }
       }
-      const int t0 = j0 + (lane >> 2), t1 = t0 + 8;
-      const float s00 = t0 < end ? sc[0] * sl : -INFINITY;
-      const float s01 = t0 < end ? sc[1] * sl : -INFINITY;
-      const float s10 = t1 < end ? sc[2] * sl : -INFINITY;
-      const float s11 = t1 < end ? sc[3] * sl : -INFINITY;
-      float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+      // Scores of tile u: tokens j0 + 16u + g (sc[u][0..1], heads 2t, 2t + 1)
+      // and j0 + 16u + g + 8 (sc[u][2..3]).
+      float sv[NT][4];
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < NT; ++u) {
+        const int t0 = j0 + 16 * u + (lane >> 2), t1 = t0 + 8;
+        sv[u][0] = t0 < end ? sc[u][0] * sl : -INFINITY;
+        sv[u][1] = t0 < end ? sc[u][1] * sl : -INFINITY;
+        sv[u][2] = t1 < end ? sc[u][2] * sl : -INFINITY;
+        sv[u][3] = t1 < end ? sc[u][3] * sl : -INFINITY;
+        mx0 = fmaxf(mx0, fmaxf(sv[u][0], sv[u][2]));
+        mx1 = fmaxf(mx1, fmaxf(sv[u][1], sv[u][3]));
+      }
 #pragma unroll
       for (int m = 4; m < 32; m <<= 1) {
         mx0 = fmaxf(mx0, shfl_xor(mx0, m));
@@ -814,10 +838,17 @@ __global__ void __launch_bounds__(kThreads, 2)
       // P is rounded to the input type for the tensor core; the row sums use
       // the same rounded values, so the output is an exact weighted mean of
       // V under the rounded weights.
-      const uint32_t w0 = M::pack2(exp2f(s00 - mn0), exp2f(s01 - mn1));  // token t0
-      const uint32_t w1 = M::pack2(exp2f(s10 - mn0), exp2f(s11 - mn1));  // token t1
-      l0 = l0 * cr0 + (M::lo(w0) + M::lo(w1));
-      l1 = l1 * cr1 + (M::hi(w0) + M::hi(w1));
+      uint32_t pw[NT][2];
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+      for (int u = 0; u < NT; ++u) {
+        pw[u][0] = M::pack2(exp2f(sv[u][0] - mn0), exp2f(sv[u][1] - mn1));  // token t0
+        pw[u][1] = M::pack2(exp2f(sv[u][2] - mn0), exp2f(sv[u][3] - mn1));  // token t1
+        ls0 += M::lo(pw[u][0]) + M::lo(pw[u][1]);
+        ls1 += M::hi(pw[u][0]) + M::hi(pw[u][1]);
+      }
+      l0 = l0 * cr0 + ls0;
+      l1 = l1 * cr1 + ls1;
 #pragma unroll
       for (int mt = 0; mt < KSTEPS; ++mt) {
         o[mt][0] *= cr0;
@@ -826,35 +857,41 @@ __global__ void __launch_bounds__(kThreads, 2)
         o[mt][3] *= cr1;
       }
       // P^T fragments (tokens x heads) from the S^T accumulator layout.
-      const uint32_t pb0 = movmatrix_trans(w0);
-      const uint32_t pb1 = movmatrix_trans(w1);
+      uint32_t pb[NT][2];
+#pragma unroll
+      for (int u = 0; u < NT; ++u) {
+        pb[u][0] = movmatrix_trans(pw[u][0]);
+        pb[u][1] = movmatrix_trans(pw[u][1]);
+      }
       // O^T += V^T P^T, one 16-wide slice of D at a time.
       if constexpr (KV8) {
-        // Word w of the four token rows: M-tiles 2w and 2w + 1.
+        // Word w of the token rows: M-tiles 2w and 2w + 1.
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          uint32_t a0, a1, b0, b1, a2, a3, b2, b3;
-          widen_tokens(vw[0][w], vw[1][w], a0, a1, b0, b1);  // tokens 2t, 2t + 1
-          widen_tokens(vw[2][w], vw[3][w], a2, a3, b2, b3);  // tokens 2t + 8, 2t + 9
-          mma_16816<false>(o[2 * w], a0, a1, a2, a3, pb0, pb1);
-          mma_16816<false>(o[2 * w + 1], b0, b1, b2, b3, pb0, pb1);
-        }
+        for (int w = 0; w < 4; ++w)
+#pragma unroll
+          for (int u = 0; u < NT; ++u) {
+            uint32_t a0, a1, b0, b1, a2, a3, b2, b3;
+            widen_tokens(vw[u][0][w], vw[u][1][w], a0, a1, b0, b1);  // tokens 2t, 2t + 1
+            widen_tokens(vw[u][2][w], vw[u][3][w], a2, a3, b2, b3);  // tokens 2t + 8, + 9
+            mma_16816<false>(o[2 * w], a0, a1, a2, a3, pb[u][0], pb[u][1]);
+            mma_16816<false>(o[2 * w + 1], b0, b1, b2, b3, pb[u][0], pb[u][1]);
+          }
       } else {
-        const uint32_t vb = smem_u32(kst) + NH * kHalfBytes;
+        const uint32_t vb = smem_u32(kst) + NH * RB;
 #pragma unroll
         for (int mt = 0; mt < KSTEPS; ++mt) {
           const int row = r0 + (mj >> 1) * 8 + mr;
           const int c16 = mt * 2 + (mj & 1);
           const uint32_t addr =
-              vb + (c16 >> 3) * kHalfBytes + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
+              vb + (c16 >> 3) * RB + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
           uint32_t a0, a1, a2, a3;
           ldmatrix_x4_trans(addr, a0, a1, a2, a3);
-          mma_16816<E::kBF16>(o[mt], a0, a1, a2, a3, pb0, pb1);
+          mma_16816<E::kBF16>(o[mt], a0, a1, a2, a3, pb[0][0], pb[0][1]);
         }
       }
       if (zeroed) fence_proxy_async_smem();  // generic writes before the next TMA
       if (hdr & (1u << warp)) item_bad = true;
-      cur += kSub;
+      cur += ROWS;
       if (cur >= end) {
         finalize(cur_item, item_bad);
         need_piece = true;
