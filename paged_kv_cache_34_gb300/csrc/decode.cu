@@ -119,10 +119,13 @@ __host__ __device__ __forceinline__ int ceil16(int x) { return (x + 15) & ~15; }
 // over NW workers, each taking at most `cap` tokens per chunk (and then
 // several chunks).  The decode and merge kernels must agree on it.
 __host__ __device__ __forceinline__ int balanced_chunk(int T, int NW, int cap) {
-  const int64_t per = static_cast<int64_t>(NW) * cap;
-  const int k = T > 0 ? static_cast<int>((T + per - 1) / per) : 1;
-  const int64_t kn = static_cast<int64_t>(k) * NW;
-  const int c = ceil16(static_cast<int>((T + kn - 1) / kn));
+  // 32-bit unsigned arithmetic is exact while T < 2^31 and NW * cap < 2^31
+  // (no sum below exceeds 2^32).
+  const uint32_t t = T > 0 ? static_cast<uint32_t>(T) : 0u;
+  const uint32_t per = static_cast<uint32_t>(NW) * static_cast<uint32_t>(cap);
+  const uint32_t k = t > 0 ? (t + per - 1) / per : 1u;
+  const uint32_t kn = k * static_cast<uint32_t>(NW);
+  const int c = ceil16(static_cast<int>((t + kn - 1) / kn));
   return c > 0 ? c : 16;
 }
 
@@ -390,16 +393,18 @@ __global__ void __launch_bounds__(kThreads, 2)
     // block, keeping the current item's position as (logical block, offset)
     // counters, and copies the block ids of the worker's next item into
     // shared memory with cp.async while the current item streams.  Lane 0
-    // owns the stage barriers.
+    // owns the stage barriers.  Lanes w + 4, w + 8, ... shadow worker w's
+    // walk up to its first piece and help copy that piece's ids.
     const bool feeder = lane < kWorkers;
+    const int wk = lane % kWorkers;
     int cur = 0, endt = 0, gq = 0, sel = 0, lblk = 0, off = 0;
     int nstart = 0, nend = 0, ng = 0, nbuf = 0;
     bool act = false, have_next = false, want_next = false;
-    Cursor pc = first_cursor(sc, blockIdx.x * kWorkers + lane);
+    Cursor pc = first_cursor(sc, blockIdx.x * kWorkers + wk);
     // Finds this worker's next piece with tokens (items of empty sequences
     // carry none: the worker writes their zeros itself) and starts copying
-    // its block ids into buffer `buf`.
-    auto prefetch = [&](int buf) {
+    // its block ids into buffer `buf`, ids k0, k0 + kstep, ... from this lane.
+    auto prefetch = [&](int buf, int k0, int kstep) {
       Item m;
       have_next = false;
       while (next_piece(sc, pc, m)) {
@@ -407,8 +412,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int l0 = m.start / bs;
         const int nblk = (m.end - 1) / bs - l0 + 1;
         const int32_t *src = p.block_table + static_cast<int64_t>(m.b) * p.bt_stride + l0;
-        const uint32_t dst = smem_u32(s_ids + (lane * 2 + buf) * p.max_ids);
-        for (int k = 0; k < nblk; ++k) cp_async_4(dst + 4 * k, src + k);
+        const uint32_t dst = smem_u32(s_ids + (wk * 2 + buf) * p.max_ids);
+        for (int k = k0; k < nblk; k += kstep) cp_async_4(dst + 4 * k, src + k);
         cp_async_commit();
         nstart = m.start;
         nend = m.end;
@@ -432,11 +437,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       off = nstart % bs;
       want_next = true;  // prefetched after this piece's first copies are issued
     };
-    // The first iteration prefetches the first piece into buffer 0 and
-    // promotes it, from the same call sites as every later piece.
-    want_next = true;
-    sel = 1;
-    act = true;
+    // The first piece: the whole warp copies its ids into buffer 0.
+    prefetch(0, lane / kWorkers, 32 / kWorkers);
+    cp_async_wait_all();
+    __syncwarp();
+    if (feeder) promote();
     const int *ids = s_ids;
     for (int c = 0;; ++c) {
       const int s = c % NS;
@@ -444,9 +449,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       int nb = 0;
       bool bad = false;
       if (feeder) {
-        if (want_next) {  // the piece after the current one: its ids
+        if (want_next && c > 0) {  // the piece after the current one: its ids
           want_next = false;
-          prefetch(sel ^ 1);
+          prefetch(sel ^ 1, 0, 1);
         }
         if (act && cur >= endt) promote();
         ids = s_ids + (lane * 2 + sel) * p.max_ids;
