@@ -72,6 +72,8 @@ def _bind(lib):
     lib.pao_write.argtypes = [P, P, P, P, c.c_int64, P, c.c_int64, c.c_int,
                               c.c_int, c.c_int, c.c_int64]
     lib.pao_write.restype = c.c_int
+    lib.pao_copy_blocks.argtypes = [P, P, c.c_int64, c.c_int64, P, c.c_int64]
+    lib.pao_copy_blocks.restype = c.c_int
     lib.pao_decode.argtypes = [P, P, c.c_int64, P, P, P, c.c_int64, c.c_int,
                                P, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int,
                                c.c_int64, c.c_double, c.c_int]
@@ -159,6 +161,24 @@ def write(k_pool: np.ndarray, v_pool: np.ndarray, k_new, v_new, slot_mapping,
     return lib.pao_write(_ptr(k_pool), _ptr(v_pool), _ptr(kn), _ptr(vn),
                          hkv * d, _ptr(slots), n, hkv, d, block_size, nb)
 
+
+
+def copy_blocks(k_pool: np.ndarray, v_pool: np.ndarray, block_mapping, lib=None) -> int:
+    """Copy-on-write of whole blocks in place: for each (src, dst) row of
+    block_mapping (int [n, 2]), block dst of both pools receives block src,
+    byte for byte, in order.  Pools are C-contiguous numpy arrays
+    [num_blocks, ...] of any dtype.  Returns OK, or ERR_BLOCK if a pair named
+    a block outside the pool (that pair copies nothing)."""
+    lib = lib or load()
+    assert k_pool.flags.c_contiguous and v_pool.flags.c_contiguous
+    assert k_pool.shape == v_pool.shape and k_pool.dtype == v_pool.dtype
+    bm = np.ascontiguousarray(np.asarray(block_mapping, dtype=np.int64).reshape(-1, 2))
+    nb = k_pool.shape[0]
+    block_bytes = k_pool.nbytes // nb if nb else 0
+    if nb == 0:
+        return OK if bm.shape[0] == 0 else ERR_BLOCK
+    return lib.pao_copy_blocks(_ptr(k_pool), _ptr(v_pool), block_bytes, nb, _ptr(bm),
+                               bm.shape[0])
 
 def decode(q, k_pool, v_pool, block_table, context_lens, num_kv_heads: int,
            block_size: int, scale: float, dtype: int | None = None,

@@ -15,11 +15,15 @@
  *   [MHPQ]  "Paged KV Cache and Packed Sequence in cann-recipes-infer"
  *           (mhpq.cn) §3.3: ops.paged_attention parameters, all-zero
  *           context_lengths give an all-zero output.
+ *   [ATB]   "Ascend CANN ATB KV Cache and PagedAttention" (coreui.cn): the
+ *           page pool, and copy-on-write of a shared page before an append.
  *
  * What it computes, in the pages' order:
  *   write  : for each new token t with slot s >= 0, the row of the pool at
  *            physical block s / block_size, offset s % block_size receives
  *            the token's K (and V) row, bit for bit   ([SKILL] §3.1, §3.3).
+ *   copy   : copy-on-write of whole blocks, source to destination, in
+ *            both pools ([ATB] page update race).
  *   gather : for sequence b and logical position j < L_b the key/value row
  *            is pool[block_table[b][j / block_size]][j % block_size]
  *            ([SKILL] §3.1; [VLLM] read_kv), copied into contiguous arrays.
@@ -146,6 +150,34 @@ int pao_write(uint16_t *k_pool, uint16_t *v_pool, const uint16_t *k_new,
       k_pool[dst + x] = k_new[t * row_stride + x];
       v_pool[dst + x] = v_new[t * row_stride + x];
     }
+  }
+  return status;
+}
+
+/* ---- copy_blocks: copy-on-write of whole blocks ------------------------- */
+
+/* [ATB] "page update race" section (copy-on-write): before a request appends
+ * K/V to a page it shares with other requests, a free page is taken and the
+ * whole old page is copied into it.  Here the pools are raw bytes, block b of
+ * a pool being bytes [b * block_bytes, (b + 1) * block_bytes).  Pairs are
+ * applied in order: block block_mapping[2p + 1] of the K pool and of the V
+ * pool receives block block_mapping[2p] byte for byte.  A pair naming a block
+ * outside [0, num_blocks) copies nothing and is reported. */
+int pao_copy_blocks(uint8_t *k_pool, uint8_t *v_pool, int64_t block_bytes,
+                    int64_t num_blocks, const int64_t *block_mapping, int64_t n) {
+  if (!k_pool || !v_pool || (n > 0 && !block_mapping)) return PAO_ERR_ARG;
+  if (block_bytes <= 0 || num_blocks < 0 || n < 0) return PAO_ERR_ARG;
+  int status = PAO_OK;
+  for (int64_t p = 0; p < n; ++p) {
+    const int64_t src = block_mapping[2 * p], dst = block_mapping[2 * p + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+      status = PAO_ERR_BLOCK;
+      continue;
+    }
+    memmove(k_pool + dst * block_bytes, k_pool + src * block_bytes,
+            (size_t)block_bytes);
+    memmove(v_pool + dst * block_bytes, v_pool + src * block_bytes,
+            (size_t)block_bytes);
   }
   return status;
 }

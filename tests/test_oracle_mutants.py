@@ -46,6 +46,15 @@ MUTANTS = {
                                 "block_size, num_blocks, k_scale[0], v_scale[0]);"),
     "int8_write_head0_scale": ("const float ks = k_scale[g], vs = v_scale[g];",
                                "const float ks = k_scale[0], vs = v_scale[0];"),
+    "copy_blocks_direction_swapped": (
+        "memmove(k_pool + dst * block_bytes, k_pool + src * block_bytes,",
+        "memmove(k_pool + src * block_bytes, k_pool + dst * block_bytes,"),
+    "copy_blocks_value_skipped": ("memmove(v_pool + dst * block_bytes, v_pool + src",
+                                  "(void)(v_pool + dst * block_bytes, v_pool + src"),
+    "copy_blocks_half_block": ("k_pool + src * block_bytes,\n            (size_t)block_bytes);",
+                               "k_pool + src * block_bytes,\n            (size_t)block_bytes / 2);"),
+    "copy_blocks_stops_at_bad_pair": ("      status = PAO_ERR_BLOCK;\n      continue;",
+                                      "      status = PAO_ERR_BLOCK;\n      break;"),
     "decode_heads_strided": (
         "for (int h = g * group; h < (g + 1) * group; ++h) {\n      double *o = out + ((int64_t)b * hq + h) * d;",
         "for (int h = g; h < hq; h += hkv) {\n      double *o = out + ((int64_t)b * hq + h) * d;"),
@@ -245,9 +254,74 @@ def _pin_int8_nearest(lib):
             and bool((c[~inside] == np.sign(y[~inside]) * 127).all()))
 
 
+def _pin_copy_blocks(lib):
+    # block dst of both pools becomes block src byte for byte, pair by pair;
+    # a pair naming a block outside the pool copies nothing and is reported
+    rng = np.random.default_rng(12)
+    shape = (7, 4, 2, 8)
+
+    def check(k0, v0, pairs, status, moved):
+        k, v = k0.copy(), v0.copy()
+        st = oracle.copy_blocks(k, v, pairs, lib=lib)
+        wk, wv = k0.copy(), v0.copy()
+        for src, dst in moved:
+            wk[dst], wv[dst] = k0[src], v0[src]
+        return st == status and np.array_equal(k, wk) and np.array_equal(v, wv)
+
+    k16 = rng.integers(0, 1 << 16, shape, dtype=np.uint16)
+    v16 = rng.integers(0, 1 << 16, shape, dtype=np.uint16)
+    k8 = rng.integers(-128, 128, shape, dtype=np.int8)
+    v8 = rng.integers(-128, 128, shape, dtype=np.int8)
+    return (check(k16, v16, [[1, 4], [3, 0], [5, 5]], oracle.OK, [(1, 4), (3, 0)])
+            and check(k16, v16, [[7, 2], [2, -1], [6, 1]], oracle.ERR_BLOCK, [(6, 1)])
+            and check(k8, v8, [[0, 6]], oracle.OK, [(0, 6)])
+            and check(k8, v8, [], oracle.OK, []))
+
+
+def _pin_copy_on_write_decode(lib):
+    # [ATB] copy-on-write: B forks from A and shares A's blocks; before it
+    # appends its own token it copies the shared, partly filled last block
+    # to a free block.  B then attends to A's tokens plus its own, and A
+    # still to its own only -- as if each sequence sat alone, contiguously.
+    # (The pool and block-table rows are roomier than needed so that every
+    # planted mistake -- e.g. a write offset of slot / bs -- stays in bounds.)
+    rng = np.random.default_rng(21)
+    bs, hkv, hq, d, nb = 4, 2, 4, 8, 16
+    L = 2 * bs + 3
+
+    def f16(shape):
+        return torch.from_numpy(rng.standard_normal(shape).astype(np.float32)).to(torch.float16)
+
+    def u16(t):
+        return t.view(torch.int16).numpy().view(np.uint16)
+    ka, va, kb, vb = f16((L, hkv, d)), f16((L, hkv, d)), f16((1, hkv, d)), f16((1, hkv, d))
+    kp = np.zeros((nb, bs, hkv, d), np.uint16)
+    vp = np.zeros_like(kp)
+    a_blocks = [5, 2, 7]
+    oracle.write(kp, vp, ka, va, np.array([a_blocks[j // bs] * bs + j % bs for j in range(L)]),
+                 bs, lib=lib)
+    st = oracle.copy_blocks(kp, vp, [[7, 0]], lib=lib)
+    oracle.write(kp, vp, kb, vb, np.array([0 * bs + L % bs]), bs, lib=lib)
+    q = f16((2, hq, d))
+    lens = np.array([L, L + 1], np.int32)
+    got = oracle.decode(q, kp, vp, np.array([[5, 2, 7, -1], [5, 2, 0, -1]], np.int32), lens,
+                        hkv, bs, 0.3, lib=lib)
+    kr = np.zeros((6, bs, hkv, d), np.uint16)
+    vr = np.zeros_like(kr)
+    for base in (0, 3 * bs):
+        kr.reshape(-1, hkv, d)[base:base + L] = u16(ka)
+        vr.reshape(-1, hkv, d)[base:base + L] = u16(va)
+    kr.reshape(-1, hkv, d)[3 * bs + L] = u16(kb)[0]
+    vr.reshape(-1, hkv, d)[3 * bs + L] = u16(vb)[0]
+    want = oracle.decode(q, kr, vr, np.array([[0, 1, 2, -1], [3, 4, 5, -1]], np.int32), lens,
+                         hkv, bs, 0.3, lib=lib)
+    return st == oracle.OK and np.array_equal(got, want)
+
+
 PINS = [_pin_decode_sdpa, _pin_prefill_sdpa, _pin_chunked_tail,
         _pin_decoders, _pin_write, _pin_saturated_softmax, _pin_int8_codes,
-        _pin_int8_write, _pin_int8_decode, _pin_int8_nearest]
+        _pin_int8_write, _pin_int8_decode, _pin_int8_nearest, _pin_copy_blocks,
+        _pin_copy_on_write_decode]
 
 
 @pytest.fixture(scope="module")
