@@ -7,11 +7,11 @@ slot_mapping, then paged decode over the whole context (split-KV plus the
 log-sum-exp merge) -- one pa_decode_write call, the public entry point for a
 decode step.  The headline value is the K/V bytes the step
 must read from HBM divided by the step's device time, with L2 flushed between
-timed steps.  The same line carries three secondary measurements (the
-packed-prefill workload in TFLOP/s, the long-context decode workload in GB/s
-and the headline decode over INT8 pools in GB/s), the roofline of the
-dominant kernel, the oracle's CPU time, and an end-to-end figure through host
-buffers.
+timed steps.  The same line carries four secondary measurements (the
+packed-prefill workload in TFLOP/s, the long-context decode workload in GB/s,
+the headline decode over INT8 pools in GB/s and copy-on-write block copies in
+GB/s), the roofline of the dominant kernel, the oracle's CPU time, and an
+end-to-end figure through host buffers.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -238,9 +238,9 @@ def bench_decode(pa, W, name, steps, warmup, flush_buf, stream, seed=None):
 def bench_decode_int8(pa, W, name, steps, warmup, flush_buf, stream):
     """The decode workload over INT8 pools.  The 16-bit pools are quantised
     once, whole, by pa_reshape_and_cache_int8 under per-KV-head absmax / 127
-    scales; a step is that call for this step's new tokens, then
-    pa_decode_int8.  Returns the inputs, the step times and the decode
-    launch's times."""
+    scales; a step is pa_decode_write_int8 (this step's new tokens written
+    into the INT8 pools, then the decode, in one call).  Returns the inputs,
+    the step times and the times of the decode call alone."""
     x = W.make_inputs(name, device="cuda")
     hkv, d = x.num_kv_heads, x.head_dim
 
@@ -265,15 +265,41 @@ def bench_decode_int8(pa, W, name, steps, warmup, flush_buf, stream):
                           partition_size=x.partition_size, workspace=ws, stream=stream)
 
     def step():
-        pa.pa_reshape_and_cache_int8(x.k_new, x.v_new, kc, vc, x.slot_mapping, ks, vs,
-                                     stream=stream)
-        dec()
+        pa.pa_decode_write_int8(out, x.q, x.k_new, x.v_new, kc, vc, x.slot_mapping,
+                                x.block_table, x.context_lens, ks, vs, scale=x.scale,
+                                max_context_len=x.max_context_len,
+                                partition_size=x.partition_size, workspace=ws, stream=stream)
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     t_step = time_steps(step, steps, flush_buf, stream)
     t_dec = time_steps(dec, steps, flush_buf, stream)
     return x, part, nparts, t_step, t_dec
+
+
+COPY_PAIRS = 1024
+
+
+def bench_copy_blocks(pa, steps, warmup, flush_buf, stream):
+    """Copy-on-write of whole blocks on pools shaped like llama7b-decode's
+    (8192 blocks of 16 tokens x 32 KV heads x 128, bf16: 128 KB per block and
+    pool): each call copies 1024 blocks to 1024 others in both pools.
+    Returns the bytes one call moves (read + written) and the call times."""
+    nb = 8192
+    g = torch.Generator(device="cuda").manual_seed(1234)
+    k = torch.randn(nb, 16, 32, 128, generator=g, device="cuda").to(torch.bfloat16)
+    v = torch.randn(nb, 16, 32, 128, generator=g, device="cuda").to(torch.bfloat16)
+    ids = torch.randperm(nb, generator=g, device="cuda")
+    mapping = torch.stack([ids[:COPY_PAIRS], ids[COPY_PAIRS:2 * COPY_PAIRS]], dim=1).contiguous()
+
+    def call():
+        pa.pa_copy_blocks(k, v, mapping, stream=stream)
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    t = time_steps(call, steps, flush_buf, stream)
+    moved = 2 * 2 * COPY_PAIRS * k[0].numel() * k.element_size()  # K+V, read+written
+    return moved, t
 
 
 def bench_prefill(pa, W, steps, warmup, flush_buf, stream):
@@ -487,6 +513,11 @@ def run_only(pa, W, args, flush_buf, stream):
                           "GBps": round((kv8 + decode_bytes(x) - kv_read_bytes(x))
                                         / (ms * 1e-3) / 1e9, 1),
                           "partition_size": part, "partitions": nparts}))
+    elif args.only == "copy-blocks":
+        moved, t = bench_copy_blocks(pa, args.steps, args.warmup, flush_buf, stream)
+        ms = statistics.fmean(t)
+        print(json.dumps({"only": "copy-blocks", "pairs": COPY_PAIRS, "ms": round(ms, 5),
+                          "GBps": round(moved / (ms * 1e-3) / 1e9, 1)}))
     else:
         x, _, t = bench_prefill(pa, W, args.steps, args.warmup, flush_buf, stream)
         ms = statistics.fmean(t)
@@ -501,10 +532,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-secondary", action="store_true",
-                    help="skip the packed-prefill, long-context and INT8 measurements")
+                    help="skip the packed-prefill, long-context, INT8 and copy-blocks measurements")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle time for the CPU baseline")
-    ap.add_argument("--only", choices=["decode", "decode-int8", "prefill"],
+    ap.add_argument("--only", choices=["decode", "decode-int8", "copy-blocks", "prefill"],
                     help="time one kernel's workload alone (a small profiling target)")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -637,6 +668,18 @@ def main():
                              "unit": "GB/s", "frac": round(gb8 / hbm_peak, 4),
                              "traffic": None}}
             del xi
+            moved, t_cp = bench_copy_blocks(pa, max(20, args.steps // 4), args.warmup,
+                                            flush_buf, stream)
+            ms_cp = statistics.fmean(t_cp)
+            gb_cp = moved / (ms_cp * 1e-3) / 1e9
+            sec["copy-blocks"] = {
+                "value": round(gb_cp, 1), "unit": "GB/s (read + written)",
+                "pairs": COPY_PAIRS, "bytes_per_call": moved, "ms_call": round(ms_cp, 5),
+                "workload": "1024 of 8192 llama7b-shaped blocks (128 KB per block and pool) "
+                            "copied in both pools",
+                "roofline": {"bound": "hbm", "achieved": round(gb_cp, 1), "peak": hbm_peak,
+                             "unit": "GB/s", "frac": round(gb_cp / hbm_peak, 4),
+                             "traffic": None}}
             line["secondary"] = sec
 
         # ---- the oracle on the host cores -------------------------------

@@ -13,6 +13,9 @@
  * pa_decode_write is one decode step as one call (the write, then the
  * decode, overlapped); pa_decode_plan sizes pa_decode's workspace;
  * pa_decode_static_ws is pa_decode without a caller-supplied workspace.
+ * pa_reshape_and_cache_int8 / pa_decode_int8 / pa_decode_write_int8 are the
+ * write, the decode and the step over INT8 pools; pa_copy_blocks copies
+ * whole blocks (copy-on-write).
  *
  * Sources (web pages on paged KV caches, cited by page and section):
  *   [SKILL] cannbot-skills "model-infer-kvcache" skill page: §3.1 physical
@@ -25,6 +28,8 @@
  *           cu_seqlens, §4.4 packed attention, §4.5 cache update, §5.1 pitch.
  *   [VLLM]  "vLLM on CANN": PagedKVCache.read_kv and the block-wise online
  *           softmax of its attention kernel.
+ *   [ATB]   "Ascend CANN ATB KV Cache and PagedAttention": the shared page
+ *           pool and copy-on-write of a shared page ("page update race").
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -385,6 +390,55 @@ pa_status pa_decode_int8(void *out, int64_t out_row_stride, const void *query,
                          int32_t partition_size, void *workspace,
                          size_t workspace_bytes, pa_dtype dtype, int32_t *d_error,
                          void *stream);
+
+/*
+ * pa_decode_write_int8 -- one decode step over INT8 pools in one call:
+ * pa_reshape_and_cache_int8(key, value, ..., slot_mapping, num_new_tokens,
+ * k_scale, v_scale), then pa_decode_int8 over the updated pools, overlapped
+ * like pa_decode_write (the decode reads everything but the K/V codes while
+ * the write runs).  Every argument is checked before anything is enqueued;
+ * arguments, requirements and errors are those of the two calls.
+ */
+pa_status pa_decode_write_int8(void *out, int64_t out_row_stride, const void *query,
+                               int64_t q_row_stride, const void *key, const void *value,
+                               int64_t kv_row_stride, void *key_cache, void *value_cache,
+                               const int64_t *slot_mapping, int32_t num_new_tokens,
+                               const int32_t *block_table, int64_t block_table_stride,
+                               int32_t max_blocks_per_seq, const int32_t *context_lens,
+                               int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                               const float *k_scale, const float *v_scale, float scale,
+                               int32_t max_context_len, int32_t partition_size,
+                               void *workspace, size_t workspace_bytes, pa_dtype dtype,
+                               int32_t *d_error, void *stream);
+
+/*
+ * pa_copy_blocks -- copy whole blocks of both pools (copy-on-write).
+ *
+ * Defines ([ATB] "page update race": before a request appends K/V to a page
+ * that other requests share, a free page is taken and the whole page is
+ * copied into it; the page table then points at the copy): for each pair p
+ * in [0, num_pairs) with src = block_mapping[2p], dst = block_mapping[2p+1]:
+ *     both in [0, num_blocks) -> block dst of key_cache and of value_cache
+ *                                receives block src, bit for bit;
+ *     otherwise               -> nothing is copied for p, PA_DEVERR_BLOCK_ID.
+ * Choosing the pairs (reference counts, the free page, the block-table
+ * update) is the caller's policy.
+ *
+ *   key_cache,
+ *   value_cache     pools of num_blocks blocks of block_bytes bytes each, of
+ *                   any element type (16-bit or INT8 pools alike).
+ *   block_mapping   int64 [num_pairs][2] device array of (src, dst).  A dst
+ *                   that is also some pair's src, or named by two pairs, is a
+ *                   caller error (the result is unspecified); src == dst
+ *                   leaves the block as it is.
+ *   d_error         nullable device int32, see above.
+ * Requirements: block_bytes a positive multiple of 16; the pools 16-byte and
+ * block_mapping 8-byte aligned.  num_pairs == 0 enqueues nothing.
+ */
+pa_status pa_copy_blocks(void *key_cache, void *value_cache, int64_t block_bytes,
+                         int64_t num_blocks, const int64_t *block_mapping,
+                         int32_t num_pairs, int32_t *d_error, void *stream);
 
 #ifdef __cplusplus
 }

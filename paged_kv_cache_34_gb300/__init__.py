@@ -10,6 +10,9 @@ first call raises.
     pa_reshape_and_cache  new K/V rows -> pool rows given by slot_mapping
     pa_decode             one query per sequence, split-KV + LSE combine
     pa_prefill_varlen     causal attention for cu_seqlens-packed queries
+    pa_reshape_and_cache_int8, pa_decode_int8
+                          the write and the decode over INT8 pools
+    pa_copy_blocks        copy whole blocks of both pools (copy-on-write)
 
 Build the library with ``python -m paged_kv_cache_34_gb300.build``.
 """
@@ -22,7 +25,8 @@ import threading
 import torch
 
 __all__ = ["pa_reshape_and_cache", "pa_decode", "pa_decode_plan", "pa_decode_write",
-           "pa_prefill_varlen", "pa_reshape_and_cache_int8", "pa_decode_int8", "PaError",
+           "pa_prefill_varlen", "pa_reshape_and_cache_int8", "pa_decode_int8",
+           "pa_decode_write_int8", "pa_copy_blocks", "PaError",
            "library", "DEVERR_SLOT", "DEVERR_BLOCK_ID", "DEVERR_CU_SEQLENS",
            "DEVERR_CONTEXT", "DEVERR_TIMEOUT", "DEVERR_SCALE", "LIB_PATH"]
 
@@ -84,9 +88,15 @@ def library(path: str | None = None):
         lib.pa_reshape_and_cache_int8.argtypes = [V, V, I64, V, V, V, I32, I32, I32, I32, I64,
                                                   V, V, c.c_int, V, V]
         lib.pa_reshape_and_cache_int8.restype = c.c_int
+        lib.pa_copy_blocks.argtypes = [V, V, I64, I64, V, I32, V, V]
+        lib.pa_copy_blocks.restype = c.c_int
         lib.pa_decode_int8.argtypes = [V, I64, V, I64, V, V, V, I64, I32, V, I32, I32, I32,
                                        I32, I32, I64, V, V, F, I32, I32, V, SZ, c.c_int, V, V]
         lib.pa_decode_int8.restype = c.c_int
+        lib.pa_decode_write_int8.argtypes = [V, I64, V, I64, V, V, I64, V, V, V, I32, V, I64,
+                                             I32, V, I32, I32, I32, I32, I32, I64, V, V, F, I32,
+                                             I32, V, SZ, c.c_int, V, V]
+        lib.pa_decode_write_int8.restype = c.c_int
         if path is None:
             _lib = lib
         return lib
@@ -163,6 +173,31 @@ def pa_reshape_and_cache_int8(key, value, key_cache, value_cache, slot_mapping, 
         key.shape[0], hkv, d, bs, nb, _scales(k_scale, hkv, "k_scale"),
         _scales(v_scale, hkv, "v_scale"), _DTYPE[key.dtype], _ptr(d_error), _stream(stream))
     _check(lib, st, "pa_reshape_and_cache_int8")
+
+
+def pa_copy_blocks(key_cache, value_cache, block_mapping, *, d_error=None, stream=None,
+                   lib=None):
+    """Copy-on-write of whole blocks: for each row (src, dst) of block_mapping
+    (int64 [n, 2] on the device), block dst of both pools receives block src.
+    The pools are contiguous [num_blocks, ...] tensors of one shape and dtype
+    (16-bit or INT8 pools alike)."""
+    lib = lib or library()
+    if key_cache.shape != value_cache.shape or key_cache.dtype != value_cache.dtype:
+        raise ValueError("key_cache and value_cache must share shape and dtype")
+    if not key_cache.is_contiguous() or not value_cache.is_contiguous():
+        raise ValueError("caches must be contiguous [num_blocks, ...]")
+    if block_mapping.dtype != torch.int64 or not block_mapping.is_contiguous():
+        raise ValueError("block_mapping must be a contiguous int64 tensor [n, 2]")
+    if block_mapping.numel() % 2:
+        raise ValueError("block_mapping must hold (src, dst) pairs")
+    nb = key_cache.shape[0]
+    block_bytes = key_cache.element_size()
+    for n in key_cache.shape[1:]:
+        block_bytes *= n
+    st = lib.pa_copy_blocks(_ptr(key_cache), _ptr(value_cache), block_bytes, nb,
+                            _ptr(block_mapping), block_mapping.numel() // 2, _ptr(d_error),
+                            _stream(stream))
+    _check(lib, st, "pa_copy_blocks")
 
 
 def pa_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
@@ -260,6 +295,41 @@ def pa_decode_write(out, query, key, value, key_cache, value_cache, slot_mapping
                              _ptr(workspace), wbytes, _DTYPE[query.dtype], _ptr(d_error),
                              _stream(stream))
     _check(lib, st, "pa_decode_write")
+    return out
+
+
+def pa_decode_write_int8(out, query, key, value, key_cache, value_cache, slot_mapping,
+                         block_table, context_lens, k_scale, v_scale, *, scale, max_context_len,
+                         partition_size=0, workspace=None, d_error=None, stream=None, lib=None):
+    """One decode step over INT8 pools in one call: pa_reshape_and_cache_int8
+    then pa_decode_int8, the decode overlapping the write.  Arguments as for
+    those two functions."""
+    lib = lib or library()
+    s, hq, d = query.shape
+    nb, bs, hkv, _ = key_cache.shape
+    ks = _rows(key, "key")
+    if _rows(value, "value") != ks:
+        raise ValueError("key and value must share a row stride")
+    if key_cache.dtype != torch.int8 or value_cache.dtype != torch.int8:
+        raise ValueError("INT8 caches must be int8")
+    if not key_cache.is_contiguous() or not value_cache.is_contiguous():
+        raise ValueError("caches must be contiguous [num_blocks, block_size, Hkv, D]")
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    if block_table.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_table and context_lens must be int32")
+    P, need = pa_decode_plan(s, hq, hkv, d, max_context_len, partition_size, lib=lib)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.pa_decode_write_int8(
+        _ptr(out), _rows(out, "out"), _ptr(query), _rows(query, "query"), _ptr(key),
+        _ptr(value), ks, _ptr(key_cache), _ptr(value_cache), _ptr(slot_mapping), key.shape[0],
+        _ptr(block_table), block_table.stride(0), block_table.shape[1], _ptr(context_lens), s,
+        hq, hkv, d, bs, nb, _scales(k_scale, hkv, "k_scale"), _scales(v_scale, hkv, "v_scale"),
+        float(scale), int(max_context_len), P, _ptr(workspace), wbytes, _DTYPE[query.dtype],
+        _ptr(d_error), _stream(stream))
+    _check(lib, st, "pa_decode_write_int8")
     return out
 
 

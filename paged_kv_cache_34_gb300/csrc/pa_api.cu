@@ -206,6 +206,30 @@ pa_status pa_reshape_and_cache(const void *key, const void *value, int64_t kv_ro
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
+pa_status pa_copy_blocks(void *key_cache, void *value_cache, int64_t block_bytes,
+                         int64_t num_blocks, const int64_t *block_mapping, int32_t num_pairs,
+                         int32_t *d_error, void *stream) {
+  if (num_pairs < 0 || num_blocks < 0 || block_bytes <= 0) return PA_ERR_SHAPE;
+  if (!key_cache || !value_cache) return PA_ERR_NULL;
+  if (block_bytes % 16 != 0 || !aligned16(key_cache) || !aligned16(value_cache))
+    return PA_ERR_ALIGN;
+  if (num_pairs == 0) return PA_OK;
+  if (!block_mapping) return PA_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(block_mapping) & 7u) return PA_ERR_ALIGN;
+  pa::CopyBlocksArgs a;
+  a.key_cache = key_cache;
+  a.value_cache = value_cache;
+  a.block_bytes = block_bytes;
+  a.num_blocks = num_blocks;
+  a.block_mapping = block_mapping;
+  a.num_pairs = num_pairs;
+  a.d_error = d_error;
+  cudaError_t e = current_num_sms(&a.num_sms);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = pa::launch_copy_blocks(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
 pa_status pa_reshape_and_cache_int8(const void *key, const void *value, int64_t kv_row_stride,
                                     void *key_cache, void *value_cache,
                                     const int64_t *slot_mapping, int32_t num_tokens,
@@ -464,6 +488,37 @@ pa_status pa_decode_write(void *out, int64_t out_row_stride, const void *query,
                      num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
                      max_context_len, partition_size, workspace, workspace_bytes, dtype, d_error,
                      stream, empty ? nullptr : &w);
+}
+
+pa_status pa_decode_write_int8(void *out, int64_t out_row_stride, const void *query,
+                               int64_t q_row_stride, const void *key, const void *value,
+                               int64_t kv_row_stride, void *key_cache, void *value_cache,
+                               const int64_t *slot_mapping, int32_t num_new_tokens,
+                               const int32_t *block_table, int64_t block_table_stride,
+                               int32_t max_blocks_per_seq, const int32_t *context_lens,
+                               int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                               const float *k_scale, const float *v_scale, float scale,
+                               int32_t max_context_len, int32_t partition_size,
+                               void *workspace, size_t workspace_bytes, pa_dtype dtype,
+                               int32_t *d_error, void *stream) {
+  if (!k_scale || !v_scale) return PA_ERR_NULL;
+  pa::ReshapeArgs w;
+  bool empty = true;
+  const pa_status st = prepare_write(key, value, kv_row_stride, key_cache, value_cache,
+                                     slot_mapping, num_new_tokens, num_kv_heads, head_dim,
+                                     block_size, num_blocks, dtype, d_error, &w, &empty);
+  if (st != PA_OK) return st;
+  w.int8 = true;
+  w.dtype = dtype;
+  w.head_dim = head_dim;
+  w.k_scale = k_scale;
+  w.v_scale = v_scale;
+  return decode_call(out, out_row_stride, query, q_row_stride, key_cache, value_cache,
+                     block_table, block_table_stride, max_blocks_per_seq, context_lens, num_seqs,
+                     num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                     max_context_len, partition_size, workspace, workspace_bytes, dtype, d_error,
+                     stream, empty ? nullptr : &w, k_scale, v_scale);
 }
 
 pa_status pa_prefill_varlen(void *out, int64_t out_row_stride, const void *query,

@@ -31,6 +31,18 @@ struct ReshapeArgs {
 };
 cudaError_t launch_reshape_and_cache(const ReshapeArgs &a, cudaStream_t stream);
 
+struct CopyBlocksArgs {
+  void *key_cache;
+  void *value_cache;
+  int64_t block_bytes;  // one block of one pool, a multiple of 16
+  int64_t num_blocks;
+  const int64_t *block_mapping;  // [num_pairs][2] (src, dst)
+  int32_t num_pairs;
+  int32_t *d_error;
+  int num_sms;
+};
+cudaError_t launch_copy_blocks(const CopyBlocksArgs &a, cudaStream_t stream);
+
 // Decode tiling shared by the planner and the kernels.
 constexpr int kDecodeWarps = 4;     // consumer warps (independent workers) per CTA
 constexpr int kDecodeSub = 16;      // tokens per worker per pipeline stage

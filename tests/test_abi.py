@@ -182,3 +182,33 @@ def test_reshape_int8_host_validation(lib):
     # head_dim 40: 16-bit rows are fine, but an int8 pool row chunk would span heads
     assert f(FAKE, FAKE, 80, FAKE, FAKE, FAKE, 3, 2, 40, 16, 8, FAKE, FAKE, 0, None, None) == 4
     assert f(None, FAKE, 256, FAKE, FAKE, FAKE, 3, 2, 128, 16, 8, FAKE, FAKE, 0, None, None) == 1
+
+
+def test_copy_blocks_host_validation(lib):
+    f = lib.pa_copy_blocks
+    # k_cache, v_cache, block_bytes, num_blocks, block_mapping, num_pairs, d_error, stream
+    assert f(FAKE, FAKE, 4096, 64, FAKE, 0, None, None) == 0  # nothing to copy
+    assert f(FAKE, FAKE, 4096, 64, None, 0, None, None) == 0
+    assert f(None, FAKE, 4096, 64, FAKE, 3, None, None) == 1
+    assert f(FAKE, FAKE, 4096, 64, None, 3, None, None) == 1
+    assert f(FAKE, FAKE, 0, 64, FAKE, 3, None, None) == 2
+    assert f(FAKE, FAKE, 4096, -1, FAKE, 3, None, None) == 2
+    assert f(FAKE, FAKE, 4096, 64, FAKE, -1, None, None) == 2
+    assert f(FAKE, FAKE, 4100, 64, FAKE, 3, None, None) == 4
+    assert f(MISALIGNED, FAKE, 4096, 64, FAKE, 3, None, None) == 4
+    assert f(FAKE, FAKE, 4096, 64, ctypes.c_void_p(0x10004), 3, None, None) == 4
+
+
+def test_decode_write_int8_host_validation(lib):
+    f = lib.pa_decode_write_int8
+
+    def call(ks=FAKE, vs=FAKE, slots=FAKE, n=4, d=128, kv_stride=2 * 128):
+        return f(FAKE, 8 * 128, FAKE, 8 * 128, FAKE, FAKE, kv_stride, FAKE, FAKE, slots, n, FAKE,
+                 16, 16, FAKE, 4, 8, 2, d, 16, 64, ks, vs, 0.125, 100, 0, None, 0, 0, None,
+                 None)
+    assert call(ks=None) == 1
+    assert call(vs=None) == 1
+    assert call(slots=None) == 1          # the write half is checked first
+    assert call(kv_stride=100) == 2
+    assert call(d=64, kv_stride=128) == 3  # INT8 decode: head_dim 128 only
+    assert call(ks=ctypes.c_void_p(0x10002)) == 4

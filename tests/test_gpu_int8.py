@@ -178,3 +178,32 @@ def test_write_int8_bad_scale():
                            ks.cpu().numpy(), vs.cpu().numpy())
     assert st == oracle.ERR_SCALE
     assert np.array_equal(kd.cpu().numpy(), kw) and np.array_equal(vd.cpu().numpy(), vw)
+
+
+def test_decode_write_int8_step():
+    """pa_decode_write_int8 = the oracle's INT8 write of the step's new tokens,
+    then its INT8 decode over the updated pools (llama7b-decode, full size)."""
+    require_gpu()
+    x = W.make_inputs("llama7b-decode")
+    kc, vc, ks, vs = int8_pools(x)  # the codes after this step's write
+    hkv, d = x.num_kv_heads, x.head_dim
+    slots = x.slot_mapping.numpy()
+    k0, v0 = kc.copy(), vc.copy()
+    k0.reshape(-1, hkv, d)[slots] = 0  # before the write
+    v0.reshape(-1, hkv, d)[slots] = 0
+    kw, vw = k0.copy(), v0.copy()
+    assert oracle.write_int8(kw, vw, x.k_new, x.v_new, slots, x.block_size, ks.numpy(),
+                             vs.numpy()) == oracle.OK
+    assert np.array_equal(kw, kc) and np.array_equal(vw, vc)
+
+    kd, vd, err = torch.from_numpy(k0).cuda(), torch.from_numpy(v0).cuda(), new_err()
+    q = x.q.cuda()
+    out = torch.full_like(q, float("nan"))
+    pa.pa_decode_write_int8(out, q, x.k_new.cuda(), x.v_new.cuda(), kd, vd,
+                            x.slot_mapping.cuda(), x.block_table.cuda(), x.context_lens.cuda(),
+                            ks.cuda(), vs.cuda(), scale=x.scale,
+                            max_context_len=x.max_context_len, d_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(kd.cpu().numpy(), kc) and np.array_equal(vd.cpu().numpy(), vc)
+    assert_close(out, oracle_decode_int8(x, kc, vc, ks, vs), x.dtype, what="INT8 step")
