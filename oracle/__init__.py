@@ -87,6 +87,14 @@ def _bind(lib):
                                     P, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int,
                                     c.c_int64, c.c_double, c.c_int, P, P]
     lib.pao_decode_int8.restype = c.c_int
+    lib.pao_fp8_value.argtypes = [P, P, c.c_int64]
+    lib.pao_fp8_value.restype = None
+    lib.pao_quantize_fp8.argtypes = [P, P, c.c_int64, c.c_int, c.c_float]
+    lib.pao_quantize_fp8.restype = c.c_int
+    lib.pao_write_fp8.argtypes = lib.pao_write_int8.argtypes
+    lib.pao_write_fp8.restype = c.c_int
+    lib.pao_decode_fp8.argtypes = lib.pao_decode_int8.argtypes
+    lib.pao_decode_fp8.restype = c.c_int
     lib.pao_prefill.argtypes = [P, P, c.c_int64, P, P, P, c.c_int64, c.c_int,
                                 P, P, c.c_int, c.c_int64, c.c_int, c.c_int,
                                 c.c_int, c.c_int, c.c_int64, c.c_double,
@@ -260,6 +268,72 @@ def decode_int8(q, k_pool: np.ndarray, v_pool: np.ndarray, block_table, context_
                              bt.shape[1], bt.shape[1], _ptr(ctx), s, hq, num_kv_heads,
                              d, block_size, ku.shape[0], float(scale), dtype,
                              _ptr(ks), _ptr(vs))
+    return (out, st) if return_status else out
+
+
+def fp8_value(codes, lib=None) -> np.ndarray:
+    """Values (fp64) of FP8 E4M3 codes (uint8), from the format's definition."""
+    lib = lib or load()
+    cu = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.zeros(cu.shape, dtype=np.float64)
+    lib.pao_fp8_value(_ptr(out), _ptr(cu), cu.size)
+    return out
+
+
+def quantize_fp8(x, scale: float, dtype: int | None = None, lib=None,
+                 return_status: bool = False):
+    """FP8 E4M3 codes (uint8) of fp16/bf16 values under one scale: the nearest
+    E4M3 value to x / scale (fp32 division; ties to even; saturating at
+    448); NaN -> 0."""
+    lib = lib or load()
+    if dtype is None:
+        dtype = dtype_code(x.dtype)
+    xu = _u16(x)
+    codes = np.zeros(xu.shape, dtype=np.uint8)
+    st = lib.pao_quantize_fp8(_ptr(codes), _ptr(xu), xu.size, int(dtype),
+                              float(np.float32(scale)))
+    return (codes, st) if return_status else codes
+
+
+def write_fp8(k_pool: np.ndarray, v_pool: np.ndarray, k_new, v_new, slot_mapping,
+              block_size: int, k_scale, v_scale, dtype: int | None = None,
+              lib=None) -> int:
+    """The cache write into FP8 pools [NB, bs, Hkv, D] (uint8 E4M3 codes),
+    quantising each new row per KV head.  Returns the status."""
+    lib = lib or load()
+    if dtype is None:
+        dtype = dtype_code(k_new.dtype)
+    kn, vn = _u16(k_new), _u16(v_new)
+    n, hkv, d = kn.shape
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    assert k_pool.dtype == np.uint8 and k_pool.flags.c_contiguous
+    assert v_pool.dtype == np.uint8 and v_pool.flags.c_contiguous
+    ks, vs = _scales(k_scale, hkv), _scales(v_scale, hkv)
+    return lib.pao_write_fp8(_ptr(k_pool), _ptr(v_pool), _ptr(kn), _ptr(vn),
+                             hkv * d, _ptr(slots), n, hkv, d, block_size,
+                             k_pool.shape[0], int(dtype), _ptr(ks), _ptr(vs))
+
+
+def decode_fp8(q, k_pool: np.ndarray, v_pool: np.ndarray, block_table, context_lens,
+               num_kv_heads: int, block_size: int, scale: float, k_scale, v_scale,
+               dtype: int | None = None, lib=None, return_status: bool = False):
+    """Oracle decode over FP8 pools ([NB, bs, Hkv, D] uint8 E4M3 codes,
+    dequantised per KV head).  Returns fp64 [S, Hq, D]."""
+    lib = lib or load()
+    if dtype is None:
+        dtype = dtype_code(q.dtype)
+    qu = _u16(q)
+    ku = np.ascontiguousarray(k_pool, dtype=np.uint8)
+    vu = np.ascontiguousarray(v_pool, dtype=np.uint8)
+    bt = np.ascontiguousarray(np.asarray(block_table), dtype=np.int32)
+    ctx = np.ascontiguousarray(np.asarray(context_lens), dtype=np.int32)
+    s, hq, d = qu.shape
+    ks, vs = _scales(k_scale, num_kv_heads), _scales(v_scale, num_kv_heads)
+    out = np.zeros((s, hq, d), dtype=np.float64)
+    st = lib.pao_decode_fp8(_ptr(out), _ptr(qu), hq * d, _ptr(ku), _ptr(vu), _ptr(bt),
+                            bt.shape[1], bt.shape[1], _ptr(ctx), s, hq, num_kv_heads,
+                            d, block_size, ku.shape[0], float(scale), dtype,
+                            _ptr(ks), _ptr(vs))
     return (out, st) if return_status else out
 
 

@@ -24,6 +24,9 @@
  *            the token's K (and V) row, bit for bit   ([SKILL] §3.1, §3.3).
  *   copy   : copy-on-write of whole blocks, source to destination, in
  *            both pools ([ATB] page update race).
+ *   8-bit pools: INT8 or FP8 (E4M3) codes with one scale per KV head for K
+ *            and for V; the write quantises, the gather dequantises
+ *            ([SKILL] App. A lists the dequantisation scales).
  *   gather : for sequence b and logical position j < L_b the key/value row
  *            is pool[block_table[b][j / block_size]][j % block_size]
  *            ([SKILL] §3.1; [VLLM] read_kv), copied into contiguous arrays.
@@ -272,6 +275,114 @@ int pao_write_int8(int8_t *k_pool, int8_t *v_pool, const uint16_t *k_new,
   return status;
 }
 
+/* ---- FP8 (E4M3) pools ---------------------------------------------------- */
+
+/* The value of an E4M3 code: 1 sign bit, 4 exponent bits (bias 7), 3
+ * fraction bits; exponent field 0 is subnormal (f / 8 * 2^-6); S.1111.111 is
+ * NaN; there are no infinities, so the largest finite value is 448. */
+static double e4m3_value(uint8_t c) {
+  const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) v = ldexp(m / 8.0, -6);
+  else v = ldexp(1.0 + m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+void pao_fp8_value(double *out, const uint8_t *codes, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = e4m3_value(codes[i]);
+}
+
+/* The E4M3 code nearest to y (ties to the even code), saturating to the
+ * largest finite value; the sign bit follows y's (so -0 and negative values
+ * that round to zero give 0x80).  Found by trying every finite magnitude. */
+static uint8_t e4m3_nearest(float y) {
+  const uint8_t sign = signbit(y) ? 0x80 : 0x00;
+  const double a = fabs((double)y);
+  int best = 0;
+  double best_err = a;
+  for (int c = 1; c <= 0x7E; ++c) {
+    const double err = fabs(e4m3_value((uint8_t)c) - a);
+    if (err < best_err || (err == best_err && (c & 1) == 0)) {
+      best = c;
+      best_err = err;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
+/* An FP8 code of x under `scale`: the nearest E4M3 value to x / scale, the
+ * division in fp32; a NaN input is stored as code 0. */
+static uint8_t quantize_fp8_1(float x, float scale) {
+  if (x != x) return 0;
+  return e4m3_nearest(x / scale);
+}
+
+int pao_quantize_fp8(uint8_t *codes, const uint16_t *x, int64_t n, int dtype,
+                     float scale) {
+  if (!codes || (n > 0 && !x) || n < 0) return PAO_ERR_ARG;
+  const int good = scale_ok(scale);
+  for (int64_t i = 0; i < n; ++i)
+    codes[i] = good ? quantize_fp8_1((float)decode16(x[i], dtype), scale) : 0;
+  return good ? PAO_OK : PAO_ERR_SCALE;
+}
+
+/* The write of pao_write into FP8 pools, quantised per KV head g with
+ * k_scale[g] / v_scale[g] (a head with a bad scale stores code 0). */
+int pao_write_fp8(uint8_t *k_pool, uint8_t *v_pool, const uint16_t *k_new,
+                  const uint16_t *v_new, int64_t row_stride,
+                  const int64_t *slot_mapping, int64_t n, int hkv, int d,
+                  int block_size, int64_t num_blocks, int dtype,
+                  const float *k_scale, const float *v_scale) {
+  if (!k_pool || !v_pool || !k_scale || !v_scale ||
+      (n > 0 && (!k_new || !v_new || !slot_mapping)))
+    return PAO_ERR_ARG;
+  if (hkv <= 0 || d <= 0 || block_size <= 0 || num_blocks < 0 || n < 0)
+    return PAO_ERR_ARG;
+  int status = PAO_OK;
+  for (int g = 0; g < hkv; ++g)
+    if (!scale_ok(k_scale[g]) || !scale_ok(v_scale[g])) status = PAO_ERR_SCALE;
+  const int64_t row = (int64_t)hkv * d;
+  for (int64_t t = 0; t < n; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= num_blocks * (int64_t)block_size) {
+      status = PAO_ERR_SLOT;
+      continue;
+    }
+    const int64_t dst = ((slot / block_size) * block_size + slot % block_size) * row;
+    for (int g = 0; g < hkv; ++g) {
+      const float fks = k_scale[g], fvs = v_scale[g];
+      const int good = scale_ok(fks) && scale_ok(fvs);
+      for (int x = 0; x < d; ++x) {
+        const int64_t i = (int64_t)g * d + x;
+        const float kx = (float)decode16(k_new[t * row_stride + i], dtype);
+        const float vx = (float)decode16(v_new[t * row_stride + i], dtype);
+        k_pool[dst + i] = good ? quantize_fp8_1(kx, fks) : 0;
+        v_pool[dst + i] = good ? quantize_fp8_1(vx, fvs) : 0;
+      }
+    }
+  }
+  return status;
+}
+
+/* gather from FP8 pools: the rows dequantised with KV head g's scales. */
+static int gather_fp8(double *kc, double *vc, const uint8_t *k_pool,
+                      const uint8_t *v_pool, const int32_t *bt_row, int len,
+                      int g, int hkv, int d, int block_size, int64_t num_blocks,
+                      double k_scale, double v_scale) {
+  for (int j = 0; j < len; ++j) {
+    int32_t block = bt_row[j / block_size];
+    if (block < 0 || block >= num_blocks) return PAO_ERR_BLOCK;
+    int64_t base = (((int64_t)block * block_size + j % block_size) * hkv + g) * d;
+    for (int x = 0; x < d; ++x) {
+      kc[(int64_t)j * d + x] = e4m3_value(k_pool[base + x]) * k_scale;
+      vc[(int64_t)j * d + x] = e4m3_value(v_pool[base + x]) * v_scale;
+    }
+  }
+  return PAO_OK;
+}
+
 /* gather from INT8 pools: the rows dequantised with KV head g's scales. */
 static int gather_int8(double *kc, double *vc, const int8_t *k_pool,
                        const int8_t *v_pool, const int32_t *bt_row, int len,
@@ -324,15 +435,15 @@ static void attend(double *o, const double *q, const double *kc,
  * sequences (heads contiguous).  out: [num_seqs, hq, d] doubles.
  * block_table: [num_seqs, bt_stride] int32 of which the first
  * max_blocks_per_seq columns may be used.  context_lens: [num_seqs]. */
-/* Pools of 16-bit patterns (k_scale == NULL) or INT8 codes with per-KV-head
- * scales k_scale / v_scale. */
+/* Pools of 16-bit patterns (k_scale == NULL), or INT8 codes (fp8 == 0) or
+ * FP8 E4M3 codes (fp8 != 0) with per-KV-head scales k_scale / v_scale. */
 static int decode_common(double *out, const uint16_t *q, int64_t q_row_stride,
                          const void *k_pool, const void *v_pool,
                          const int32_t *block_table, int64_t bt_stride,
                          int max_blocks_per_seq, const int32_t *context_lens,
                          int num_seqs, int hq, int hkv, int d, int block_size,
                          int64_t num_blocks, double scale, int dtype,
-                         const float *k_scale, const float *v_scale) {
+                         const float *k_scale, const float *v_scale, int fp8) {
   if (!out || !q || !k_pool || !v_pool || !block_table || !context_lens)
     return PAO_ERR_ARG;
   if (hq <= 0 || hkv <= 0 || hq % hkv != 0 || d <= 0 || block_size <= 0)
@@ -356,7 +467,11 @@ static int decode_common(double *out, const uint16_t *q, int64_t q_row_stride,
       qd = (double *)malloc((size_t)d * sizeof(double));
       if (!kc || !vc || !s || !qd) err = PAO_ERR_NOMEM;
     }
-    if (err == PAO_OK && k_scale)
+    if (err == PAO_OK && k_scale && fp8)
+      err = gather_fp8(kc, vc, (const uint8_t *)k_pool, (const uint8_t *)v_pool,
+                       block_table + (int64_t)b * bt_stride, len, g, hkv, d,
+                       block_size, num_blocks, k_scale[g], v_scale[g]);
+    else if (err == PAO_OK && k_scale)
       err = gather_int8(kc, vc, (const int8_t *)k_pool, (const int8_t *)v_pool,
                         block_table + (int64_t)b * bt_stride, len, g, hkv, d,
                         block_size, num_blocks, k_scale[g], v_scale[g]);
@@ -395,7 +510,7 @@ int pao_decode(double *out, const uint16_t *q, int64_t q_row_stride,
   return decode_common(out, q, q_row_stride, k_pool, v_pool, block_table,
                        bt_stride, max_blocks_per_seq, context_lens, num_seqs,
                        hq, hkv, d, block_size, num_blocks, scale, dtype, NULL,
-                       NULL);
+                       NULL, 0);
 }
 
 /* Decode over INT8 pools, dequantised per KV head (see pao_write_int8). */
@@ -410,7 +525,22 @@ int pao_decode_int8(double *out, const uint16_t *q, int64_t q_row_stride,
   return decode_common(out, q, q_row_stride, k_pool, v_pool, block_table,
                        bt_stride, max_blocks_per_seq, context_lens, num_seqs,
                        hq, hkv, d, block_size, num_blocks, scale, dtype, k_scale,
-                       v_scale);
+                       v_scale, 0);
+}
+
+/* Decode over FP8 (E4M3) pools, dequantised per KV head (see pao_write_fp8). */
+int pao_decode_fp8(double *out, const uint16_t *q, int64_t q_row_stride,
+                   const uint8_t *k_pool, const uint8_t *v_pool,
+                   const int32_t *block_table, int64_t bt_stride,
+                   int max_blocks_per_seq, const int32_t *context_lens,
+                   int num_seqs, int hq, int hkv, int d, int block_size,
+                   int64_t num_blocks, double scale, int dtype,
+                   const float *k_scale, const float *v_scale) {
+  if (!k_scale || !v_scale) return PAO_ERR_ARG;
+  return decode_common(out, q, q_row_stride, k_pool, v_pool, block_table,
+                       bt_stride, max_blocks_per_seq, context_lens, num_seqs,
+                       hq, hkv, d, block_size, num_blocks, scale, dtype, k_scale,
+                       v_scale, 1);
 }
 
 /* ---- prefill: packed variable-length queries --------------------------- */

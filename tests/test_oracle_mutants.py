@@ -55,6 +55,13 @@ MUTANTS = {
                                "k_pool + src * block_bytes,\n            (size_t)block_bytes / 2);"),
     "copy_blocks_stops_at_bad_pair": ("      status = PAO_ERR_BLOCK;\n      continue;",
                                       "      status = PAO_ERR_BLOCK;\n      break;"),
+    "fp8_exponent_bias": ("else v = ldexp(1.0 + m / 8.0, e - 7);",
+                          "else v = ldexp(1.0 + m / 8.0, e - 8);"),
+    "fp8_subnormal_scale": ("if (e == 0) v = ldexp(m / 8.0, -6);",
+                            "if (e == 0) v = ldexp(m / 8.0, -7);"),
+    "fp8_ties_away_from_zero": ("(err == best_err && (c & 1) == 0)", "(err == best_err)"),
+    "fp8_decode_reads_int8": ("= e4m3_value(k_pool[base + x]) * k_scale;",
+                              "= (double)(int8_t)k_pool[base + x] * k_scale;"),
     "decode_heads_strided": (
         "for (int h = g * group; h < (g + 1) * group; ++h) {\n      double *o = out + ((int64_t)b * hq + h) * d;",
         "for (int h = g; h < hq; h += hkv) {\n      double *o = out + ((int64_t)b * hq + h) * d;"),
@@ -318,10 +325,81 @@ def _pin_copy_on_write_decode(lib):
     return st == oracle.OK and np.array_equal(got, want)
 
 
+def _pin_fp8_codes(lib):
+    # the E4M3 table against torch's float8_e4m3fn (a library routine) and
+    # closed forms; the encoder against torch's round-to-nearest-even inside
+    # the range, ties to the even code, saturation at 448, NaN -> 0, -0 kept
+    codes = np.arange(256, dtype=np.uint8)
+    v = oracle.fp8_value(codes, lib=lib)
+    t = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(t)
+    if not (np.array_equal(np.isnan(v), nan) and np.array_equal(v[~nan], t[~nan])):
+        return False
+    if not (v[0x7E] == 448.0 and v[0x01] == 2.0 ** -9 and v[0x08] == 2.0 ** -6
+            and v[0x38] == 1.0 and v[0xB8] == -1.0):
+        return False
+    rng = np.random.default_rng(13)
+    for s in (1.0, 0.01, 37.0):
+        x = torch.from_numpy(rng.standard_normal(4096).astype(np.float32) * 40).to(torch.bfloat16)
+        y = x.float() / np.float32(s)
+        inside = (y.abs() < 448).numpy()
+        c = oracle.quantize_fp8(x, s, lib=lib)
+        want = y[torch.from_numpy(inside)].to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        if not np.array_equal(c[inside], want):
+            return False
+        if not (c[~inside] & 0x7F == 0x7E).all():
+            return False
+    ties = _bf16([1.0625, 1.1875, 2.0 ** -10, 3 * 2.0 ** -10, -1.0625, 500.0, -1e4,
+                  float("nan"), -0.0, float("inf")])
+    c, st = oracle.quantize_fp8(ties, 1.0, lib=lib, return_status=True)
+    if st != oracle.OK or c.tolist() != [0x38, 0x3A, 0x00, 0x02, 0xB8, 0x7E, 0xFE, 0x00, 0x80,
+                                         0x7E]:
+        return False
+    bad, st = oracle.quantize_fp8(ties, -1.0, lib=lib, return_status=True)
+    return st == oracle.ERR_SCALE and not bad.any()
+
+
+def _pin_fp8_write(lib):
+    # code = sign << 7 | exponent field << 3 | fraction, worked by hand
+    nb, bs, hkv, d = 4, 8, 2, 2
+    kp = np.zeros((nb, bs, hkv, d), np.uint8)
+    vp = np.zeros((nb, bs, hkv, d), np.uint8)
+    kn = _bf16([[[1.0, -2.0], [3.0, 4.0]]])   # / [0.5, 1.0] -> 2, -4 | 3, 4
+    vn = _bf16([[[0.5, 0.25], [-1.0, 8.0]]])  # / [0.25, 2.0] -> 2, 1 | -0.5, 4
+    st = oracle.write_fp8(kp, vp, kn, vn, np.array([2 * bs + 3]), bs, [0.5, 1.0],
+                          [0.25, 2.0], lib=lib)
+    return (st == oracle.OK and kp[2, 3].tolist() == [[0x40, 0xC8], [0x44, 0x48]]
+            and vp[2, 3].tolist() == [[0x40, 0x38], [0xB0, 0x48]]
+            and int(kp.astype(np.int64).sum()) == 0x40 + 0xC8 + 0x44 + 0x48)
+
+
+def _pin_fp8_decode(lib):
+    # FP8 pools whose dequantised values are exact in bf16 decode exactly
+    # like bf16 pools holding those values (the pinned 16-bit path)
+    x = W.make_inputs(_cfg("decode", 4, 2, 64, 16, 24, [1, 37, 90], "identity",
+                           dtype="bf16"), seed=48)
+    rng = np.random.default_rng(6)
+    shape = tuple(x.k_pool.shape)
+    finite = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
+    kc, vc = rng.choice(finite, shape), rng.choice(finite, shape)
+    ks = np.array([2.0 ** -3, 2.0 ** 2], np.float32)
+    vs = np.array([2.0 ** 1, 2.0 ** -5], np.float32)
+    kv = oracle.fp8_value(kc, lib=lib) * ks[None, None, :, None]
+    vv = oracle.fp8_value(vc, lib=lib) * vs[None, None, :, None]
+    kb = torch.from_numpy(kv).to(torch.bfloat16)
+    vb = torch.from_numpy(vv).to(torch.bfloat16)
+    if not (np.array_equal(kb.double().numpy(), kv) and np.array_equal(vb.double().numpy(), vv)):
+        return False
+    want = oracle.decode(x.q, kb, vb, x.block_table, x.context_lens, 2, 16, x.scale, lib=lib)
+    got = oracle.decode_fp8(x.q, kc, vc, x.block_table, x.context_lens, 2, 16, x.scale,
+                            ks, vs, lib=lib)
+    return np.array_equal(got, want)
+
+
 PINS = [_pin_decode_sdpa, _pin_prefill_sdpa, _pin_chunked_tail,
         _pin_decoders, _pin_write, _pin_saturated_softmax, _pin_int8_codes,
         _pin_int8_write, _pin_int8_decode, _pin_int8_nearest, _pin_copy_blocks,
-        _pin_copy_on_write_decode]
+        _pin_copy_on_write_decode, _pin_fp8_codes, _pin_fp8_write, _pin_fp8_decode]
 
 
 @pytest.fixture(scope="module")
