@@ -295,19 +295,21 @@ void pao_fp8_value(double *out, const uint8_t *codes, int64_t n) {
 
 /* The E4M3 code nearest to y (ties to the even code), saturating to the
  * largest finite value; the sign bit follows y's (so -0 and negative values
- * that round to zero give 0x80).  Found by trying every finite magnitude. */
+ * that round to zero give 0x80).  Finite magnitudes grow with the code
+ * (0x00 .. 0x7E), so bisection finds the two codes around |y| and the nearer
+ * one wins. */
 static uint8_t e4m3_nearest(float y) {
   const uint8_t sign = signbit(y) ? 0x80 : 0x00;
   const double a = fabs((double)y);
-  int best = 0;
-  double best_err = a;
-  for (int c = 1; c <= 0x7E; ++c) {
-    const double err = fabs(e4m3_value((uint8_t)c) - a);
-    if (err < best_err || (err == best_err && (c & 1) == 0)) {
-      best = c;
-      best_err = err;
-    }
+  if (!(a < 448.0)) return (uint8_t)(sign | 0x7E);
+  int lo = 0, hi = 0x7E; /* value(lo) <= a < value(hi) */
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) / 2;
+    if (e4m3_value((uint8_t)mid) <= a) lo = mid;
+    else hi = mid;
   }
+  const double dl = a - e4m3_value((uint8_t)lo), dh = e4m3_value((uint8_t)hi) - a;
+  const int best = dl < dh ? lo : (dh < dl ? hi : ((lo & 1) == 0 ? lo : hi));
   return (uint8_t)(sign | best);
 }
 
@@ -322,6 +324,7 @@ int pao_quantize_fp8(uint8_t *codes, const uint16_t *x, int64_t n, int dtype,
                      float scale) {
   if (!codes || (n > 0 && !x) || n < 0) return PAO_ERR_ARG;
   const int good = scale_ok(scale);
+#pragma omp parallel for schedule(static)
   for (int64_t i = 0; i < n; ++i)
     codes[i] = good ? quantize_fp8_1((float)decode16(x[i], dtype), scale) : 0;
   return good ? PAO_OK : PAO_ERR_SCALE;
@@ -371,13 +374,15 @@ static int gather_fp8(double *kc, double *vc, const uint8_t *k_pool,
                       const uint8_t *v_pool, const int32_t *bt_row, int len,
                       int g, int hkv, int d, int block_size, int64_t num_blocks,
                       double k_scale, double v_scale) {
+  double value[256]; /* every code's value, once per call */
+  for (int c = 0; c < 256; ++c) value[c] = e4m3_value((uint8_t)c);
   for (int j = 0; j < len; ++j) {
     int32_t block = bt_row[j / block_size];
     if (block < 0 || block >= num_blocks) return PAO_ERR_BLOCK;
     int64_t base = (((int64_t)block * block_size + j % block_size) * hkv + g) * d;
     for (int x = 0; x < d; ++x) {
-      kc[(int64_t)j * d + x] = e4m3_value(k_pool[base + x]) * k_scale;
-      vc[(int64_t)j * d + x] = e4m3_value(v_pool[base + x]) * v_scale;
+      kc[(int64_t)j * d + x] = value[k_pool[base + x]] * k_scale;
+      vc[(int64_t)j * d + x] = value[v_pool[base + x]] * v_scale;
     }
   }
   return PAO_OK;

@@ -59,8 +59,8 @@ MUTANTS = {
                           "else v = ldexp(1.0 + m / 8.0, e - 8);"),
     "fp8_subnormal_scale": ("if (e == 0) v = ldexp(m / 8.0, -6);",
                             "if (e == 0) v = ldexp(m / 8.0, -7);"),
-    "fp8_ties_away_from_zero": ("(err == best_err && (c & 1) == 0)", "(err == best_err)"),
-    "fp8_decode_reads_int8": ("= e4m3_value(k_pool[base + x]) * k_scale;",
+    "fp8_ties_away_from_zero": ("((lo & 1) == 0 ? lo : hi)", "(hi)"),
+    "fp8_decode_reads_int8": ("= value[k_pool[base + x]] * k_scale;",
                               "= (double)(int8_t)k_pool[base + x] * k_scale;"),
     "decode_heads_strided": (
         "for (int h = g * group; h < (g + 1) * group; ++h) {\n      double *o = out + ((int64_t)b * hq + h) * d;",
