@@ -7,11 +7,11 @@ slot_mapping, then paged decode over the whole context (split-KV plus the
 log-sum-exp merge) -- one pa_decode_write call, the public entry point for a
 decode step.  The headline value is the K/V bytes the step
 must read from HBM divided by the step's device time, with L2 flushed between
-timed steps.  The same line carries four secondary measurements (the
+timed steps.  The same line carries five secondary measurements (the
 packed-prefill workload in TFLOP/s, the long-context decode workload in GB/s,
-the headline decode over INT8 pools in GB/s and copy-on-write block copies in
-GB/s), the roofline of the dominant kernel, the oracle's CPU time, and an
-end-to-end figure through host buffers.
+the headline decode over INT8 and over FP8 pools in GB/s, and copy-on-write
+block copies in GB/s), the roofline of the dominant kernel, the oracle's CPU
+time, and an end-to-end figure through host buffers.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -235,40 +235,44 @@ def bench_decode(pa, W, name, steps, warmup, flush_buf, stream, seed=None):
     return x, out, ws, part, nparts, t_step, t_dec
 
 
-def bench_decode_int8(pa, W, name, steps, warmup, flush_buf, stream):
-    """The decode workload over INT8 pools.  The 16-bit pools are quantised
-    once, whole, by pa_reshape_and_cache_int8 under per-KV-head absmax / 127
-    scales; a step is pa_decode_write_int8 (this step's new tokens written
-    into the INT8 pools, then the decode, in one call).  Returns the inputs,
-    the step times and the times of the decode call alone."""
+def bench_decode_kv8(pa, W, name, steps, warmup, flush_buf, stream, fmt="int8"):
+    """The decode workload over 8-bit pools (fmt "int8" or "fp8").  The
+    16-bit pools are quantised once, whole, by the library's 8-bit write under
+    per-KV-head absmax / (largest code) scales; a step is the one-call 8-bit
+    step (this step's new tokens written, then the decode).  Returns the
+    inputs, the plan, the step times and the times of the decode call alone."""
     x = W.make_inputs(name, device="cuda")
     hkv, d = x.num_kv_heads, x.head_dim
+    top = 127.0 if fmt == "int8" else 448.0
+    write = pa.pa_reshape_and_cache_int8 if fmt == "int8" else pa.pa_reshape_and_cache_fp8
+    decode = pa.pa_decode_int8 if fmt == "int8" else pa.pa_decode_fp8
+    step_call = pa.pa_decode_write_int8 if fmt == "int8" else pa.pa_decode_write_fp8
 
     def absmax_scale(pool):
         # unwritten pool slots hold NaN: they quantise to 0 and set no scale
         a = pool.reshape(-1, hkv, d).float().nan_to_num(0.0, 0.0, 0.0).abs().amax(dim=(0, 2))
-        return (a / 127).clamp_min(1e-6).contiguous()
+        return (a / top).clamp_min(1e-6).contiguous()
     ks, vs = absmax_scale(x.k_pool), absmax_scale(x.v_pool)
-    kc = torch.empty(x.k_pool.shape, dtype=torch.int8, device="cuda")
+    code = torch.int8 if fmt == "int8" else torch.uint8
+    kc = torch.empty(x.k_pool.shape, dtype=code, device="cuda")
     vc = torch.empty_like(kc)
     slots = torch.arange(x.k_pool.shape[0] * x.block_size, dtype=torch.int64, device="cuda")
-    pa.pa_reshape_and_cache_int8(x.k_pool.reshape(-1, hkv, d), x.v_pool.reshape(-1, hkv, d),
-                                 kc, vc, slots, ks, vs, stream=stream)
+    write(x.k_pool.reshape(-1, hkv, d), x.v_pool.reshape(-1, hkv, d), kc, vc, slots, ks, vs,
+          stream=stream)
     x.k_pool = x.v_pool = None  # the 16-bit pools are not read again
     del slots
     out = torch.empty_like(x.q)
     ws, part, nparts = decode_workspace(pa, x)
 
     def dec():
-        pa.pa_decode_int8(out, x.q, kc, vc, x.block_table, x.context_lens, ks, vs,
-                          scale=x.scale, max_context_len=x.max_context_len,
-                          partition_size=x.partition_size, workspace=ws, stream=stream)
+        decode(out, x.q, kc, vc, x.block_table, x.context_lens, ks, vs, scale=x.scale,
+               max_context_len=x.max_context_len, partition_size=x.partition_size,
+               workspace=ws, stream=stream)
 
     def step():
-        pa.pa_decode_write_int8(out, x.q, x.k_new, x.v_new, kc, vc, x.slot_mapping,
-                                x.block_table, x.context_lens, ks, vs, scale=x.scale,
-                                max_context_len=x.max_context_len,
-                                partition_size=x.partition_size, workspace=ws, stream=stream)
+        step_call(out, x.q, x.k_new, x.v_new, kc, vc, x.slot_mapping, x.block_table,
+                  x.context_lens, ks, vs, scale=x.scale, max_context_len=x.max_context_len,
+                  partition_size=x.partition_size, workspace=ws, stream=stream)
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
@@ -504,12 +508,12 @@ def run_only(pa, W, args, flush_buf, stream):
         print(json.dumps({"only": "decode", "workload": HEADLINE, "ms": round(ms, 5),
                           "GBps": round(decode_bytes(x) / (ms * 1e-3) / 1e9, 1),
                           "partition_size": part, "partitions": nparts}))
-    elif args.only == "decode-int8":
-        x, part, nparts, _, t = bench_decode_int8(pa, W, HEADLINE, args.steps, args.warmup,
-                                                  flush_buf, stream)
+    elif args.only in ("decode-int8", "decode-fp8"):
+        x, part, nparts, _, t = bench_decode_kv8(pa, W, HEADLINE, args.steps, args.warmup,
+                                                 flush_buf, stream, args.only[7:])
         ms = statistics.fmean(t)
         kv8 = kv_read_bytes(x) // 2
-        print(json.dumps({"only": "decode-int8", "workload": HEADLINE, "ms": round(ms, 5),
+        print(json.dumps({"only": args.only, "workload": HEADLINE, "ms": round(ms, 5),
                           "GBps": round((kv8 + decode_bytes(x) - kv_read_bytes(x))
                                         / (ms * 1e-3) / 1e9, 1),
                           "partition_size": part, "partitions": nparts}))
@@ -532,10 +536,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-secondary", action="store_true",
-                    help="skip the packed-prefill, long-context, INT8 and copy-blocks measurements")
+                    help="skip the packed-prefill, long-context, 8-bit pool and copy-blocks "
+                         "measurements")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle time for the CPU baseline")
-    ap.add_argument("--only", choices=["decode", "decode-int8", "copy-blocks", "prefill"],
+    ap.add_argument("--only",
+                    choices=["decode", "decode-int8", "decode-fp8", "copy-blocks", "prefill"],
                     help="time one kernel's workload alone (a small profiling target)")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -652,22 +658,24 @@ def main():
                              "traffic": recorded_traffic("pa_decode", "long-context-decode",
                                                          dec_hash)}}
             del xl
-            xi, parti, npi, t_istep, t_idec = bench_decode_int8(
-                pa, W, HEADLINE, max(20, args.steps // 4), args.warmup, flush_buf, stream)
-            ms_i = statistics.fmean(t_idec)
-            kv8 = kv_read_bytes(xi) // 2  # one byte per element
-            gb8 = (kv8 + decode_bytes(xi) - kv_read_bytes(xi)) / (ms_i * 1e-3) / 1e9
-            sec["llama7b-decode-int8"] = {
-                "value": round(kv8 / (ms_i * 1e-3) / 1e9, 1), "unit": "GB/s",
-                "pools": "int8 codes, per-KV-head fp32 scales (absmax / 127)",
-                "ms_decode": round(ms_i, 5),
-                "ms_write_plus_decode": round(statistics.fmean(t_istep), 5),
-                "speedup_vs_16bit_decode": round(ms_dec / ms_i, 3),
-                "partition_size": parti, "partitions": npi,
-                "roofline": {"bound": "hbm", "achieved": round(gb8, 1), "peak": hbm_peak,
-                             "unit": "GB/s", "frac": round(gb8 / hbm_peak, 4),
-                             "traffic": None}}
-            del xi
+            for fmt, pools in (("int8", "int8 codes"), ("fp8", "FP8 E4M3 codes")):
+                xi, parti, npi, t_istep, t_idec = bench_decode_kv8(
+                    pa, W, HEADLINE, max(20, args.steps // 4), args.warmup, flush_buf, stream,
+                    fmt)
+                ms_i = statistics.fmean(t_idec)
+                kv8 = kv_read_bytes(xi) // 2  # one byte per element
+                gb8 = (kv8 + decode_bytes(xi) - kv_read_bytes(xi)) / (ms_i * 1e-3) / 1e9
+                sec[f"llama7b-decode-{fmt}"] = {
+                    "value": round(kv8 / (ms_i * 1e-3) / 1e9, 1), "unit": "GB/s",
+                    "pools": f"{pools}, per-KV-head fp32 scales (absmax / largest code)",
+                    "ms_decode": round(ms_i, 5),
+                    "ms_write_plus_decode": round(statistics.fmean(t_istep), 5),
+                    "speedup_vs_16bit_decode": round(ms_dec / ms_i, 3),
+                    "partition_size": parti, "partitions": npi,
+                    "roofline": {"bound": "hbm", "achieved": round(gb8, 1), "peak": hbm_peak,
+                                 "unit": "GB/s", "frac": round(gb8 / hbm_peak, 4),
+                                 "traffic": None}}
+                del xi
             moved, t_cp = bench_copy_blocks(pa, max(20, args.steps // 4), args.warmup,
                                             flush_buf, stream)
             ms_cp = statistics.fmean(t_cp)

@@ -14,8 +14,8 @@
  * decode, overlapped); pa_decode_plan sizes pa_decode's workspace;
  * pa_decode_static_ws is pa_decode without a caller-supplied workspace.
  * pa_reshape_and_cache_int8 / pa_decode_int8 / pa_decode_write_int8 are the
- * write, the decode and the step over INT8 pools; pa_copy_blocks copies
- * whole blocks (copy-on-write).
+ * write, the decode and the step over INT8 pools, the _fp8 calls the same
+ * over FP8 (E4M3) pools; pa_copy_blocks copies whole blocks (copy-on-write).
  *
  * Sources (web pages on paged KV caches, cited by page and section):
  *   [SKILL] cannbot-skills "model-infer-kvcache" skill page: §3.1 physical
@@ -411,6 +411,53 @@ pa_status pa_decode_write_int8(void *out, int64_t out_row_stride, const void *qu
                                int32_t max_context_len, int32_t partition_size,
                                void *workspace, size_t workspace_bytes, pa_dtype dtype,
                                int32_t *d_error, void *stream);
+
+/*
+ * FP8 KV pools.
+ *
+ * The same per-KV-head scales as the INT8 pools, with codes in the OCP FP8
+ * E4M3 format (1 sign, 4 exponent bits of bias 7, 3 fraction bits;
+ * exponent 0 subnormal; S.1111.111 NaN; no infinities, largest finite 448).
+ * A value x is stored as the E4M3 value nearest to x / scale (the division
+ * in fp32, ties to the even code, saturating at +-448; a NaN input is
+ * stored as 0) and read back as value(code) * scale.  Pools are
+ * [num_blocks, block_size, num_kv_heads, head_dim] bytes; the three calls
+ * below are the FP8 counterparts of the INT8 calls above, with the same
+ * arguments, requirements (head_dim 128 for the decode) and errors.  NaN
+ * codes never come from the write; rows past a sequence's context may hold
+ * any byte.
+ */
+pa_status pa_reshape_and_cache_fp8(const void *key, const void *value, int64_t kv_row_stride,
+                                   void *key_cache, void *value_cache,
+                                   const int64_t *slot_mapping, int32_t num_tokens,
+                                   int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                   int64_t num_blocks, const float *k_scale,
+                                   const float *v_scale, pa_dtype dtype, int32_t *d_error,
+                                   void *stream);
+
+pa_status pa_decode_fp8(void *out, int64_t out_row_stride, const void *query,
+                        int64_t q_row_stride, const void *key_cache, const void *value_cache,
+                        const int32_t *block_table, int64_t block_table_stride,
+                        int32_t max_blocks_per_seq, const int32_t *context_lens,
+                        int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                        int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                        const float *k_scale, const float *v_scale, float scale,
+                        int32_t max_context_len, int32_t partition_size, void *workspace,
+                        size_t workspace_bytes, pa_dtype dtype, int32_t *d_error,
+                        void *stream);
+
+pa_status pa_decode_write_fp8(void *out, int64_t out_row_stride, const void *query,
+                              int64_t q_row_stride, const void *key, const void *value,
+                              int64_t kv_row_stride, void *key_cache, void *value_cache,
+                              const int64_t *slot_mapping, int32_t num_new_tokens,
+                              const int32_t *block_table, int64_t block_table_stride,
+                              int32_t max_blocks_per_seq, const int32_t *context_lens,
+                              int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                              const float *k_scale, const float *v_scale, float scale,
+                              int32_t max_context_len, int32_t partition_size,
+                              void *workspace, size_t workspace_bytes, pa_dtype dtype,
+                              int32_t *d_error, void *stream);
 
 /*
  * pa_copy_blocks -- copy whole blocks of both pools (copy-on-write).

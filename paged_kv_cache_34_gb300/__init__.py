@@ -10,8 +10,8 @@ first call raises.
     pa_reshape_and_cache  new K/V rows -> pool rows given by slot_mapping
     pa_decode             one query per sequence, split-KV + LSE combine
     pa_prefill_varlen     causal attention for cu_seqlens-packed queries
-    pa_reshape_and_cache_int8, pa_decode_int8
-                          the write and the decode over INT8 pools
+    pa_reshape_and_cache_int8, pa_decode_int8, pa_decode_write_int8 (and _fp8)
+                          the write, decode and step over INT8 (FP8 E4M3) pools
     pa_copy_blocks        copy whole blocks of both pools (copy-on-write)
 
 Build the library with ``python -m paged_kv_cache_34_gb300.build``.
@@ -26,7 +26,8 @@ import torch
 
 __all__ = ["pa_reshape_and_cache", "pa_decode", "pa_decode_plan", "pa_decode_write",
            "pa_prefill_varlen", "pa_reshape_and_cache_int8", "pa_decode_int8",
-           "pa_decode_write_int8", "pa_copy_blocks", "PaError",
+           "pa_decode_write_int8", "pa_reshape_and_cache_fp8", "pa_decode_fp8",
+           "pa_decode_write_fp8", "pa_copy_blocks", "PaError",
            "library", "DEVERR_SLOT", "DEVERR_BLOCK_ID", "DEVERR_CU_SEQLENS",
            "DEVERR_CONTEXT", "DEVERR_TIMEOUT", "DEVERR_SCALE", "LIB_PATH"]
 
@@ -97,6 +98,12 @@ def library(path: str | None = None):
                                              I32, V, I32, I32, I32, I32, I32, I64, V, V, F, I32,
                                              I32, V, SZ, c.c_int, V, V]
         lib.pa_decode_write_int8.restype = c.c_int
+        lib.pa_reshape_and_cache_fp8.argtypes = lib.pa_reshape_and_cache_int8.argtypes
+        lib.pa_reshape_and_cache_fp8.restype = c.c_int
+        lib.pa_decode_fp8.argtypes = lib.pa_decode_int8.argtypes
+        lib.pa_decode_fp8.restype = c.c_int
+        lib.pa_decode_write_fp8.argtypes = lib.pa_decode_write_int8.argtypes
+        lib.pa_decode_write_fp8.restype = c.c_int
         if path is None:
             _lib = lib
         return lib
@@ -153,26 +160,49 @@ def _scales(t, hkv, what):
     return _ptr(t)
 
 
-def pa_reshape_and_cache_int8(key, value, key_cache, value_cache, slot_mapping, k_scale,
-                              v_scale, *, d_error=None, stream=None, lib=None):
-    """pa_reshape_and_cache into INT8 pools: caches int8 [NB, bs, Hkv, D];
-    k_scale / v_scale float32 [Hkv] (per-KV-head dequantisation scales)."""
+_POOL8 = {"int8": (torch.int8,), "fp8": (torch.uint8, torch.float8_e4m3fn)}
+
+
+def _check_pools8(fmt, key_cache, value_cache):
+    if key_cache.dtype not in _POOL8[fmt] or value_cache.dtype not in _POOL8[fmt]:
+        names = " or ".join(str(t).replace("torch.", "") for t in _POOL8[fmt])
+        raise ValueError(f"{fmt.upper()} caches must be {names}")
+    if not key_cache.is_contiguous() or not value_cache.is_contiguous():
+        raise ValueError("caches must be contiguous [num_blocks, block_size, Hkv, D]")
+
+
+def _write8(fmt, key, value, key_cache, value_cache, slot_mapping, k_scale, v_scale, d_error,
+            stream, lib):
     lib = lib or library()
     ks = _rows(key, "key")
     if _rows(value, "value") != ks:
         raise ValueError("key and value must share a row stride")
-    if key_cache.dtype != torch.int8 or value_cache.dtype != torch.int8:
-        raise ValueError("INT8 caches must be int8")
-    if not key_cache.is_contiguous() or not value_cache.is_contiguous():
-        raise ValueError("caches must be contiguous [num_blocks, block_size, Hkv, D]")
+    _check_pools8(fmt, key_cache, value_cache)
     if slot_mapping.dtype != torch.int64:
         raise ValueError("slot_mapping must be int64")
     nb, bs, hkv, d = key_cache.shape
-    st = lib.pa_reshape_and_cache_int8(
+    name = f"pa_reshape_and_cache_{fmt}"
+    st = getattr(lib, name)(
         _ptr(key), _ptr(value), ks, _ptr(key_cache), _ptr(value_cache), _ptr(slot_mapping),
         key.shape[0], hkv, d, bs, nb, _scales(k_scale, hkv, "k_scale"),
         _scales(v_scale, hkv, "v_scale"), _DTYPE[key.dtype], _ptr(d_error), _stream(stream))
-    _check(lib, st, "pa_reshape_and_cache_int8")
+    _check(lib, st, name)
+
+
+def pa_reshape_and_cache_int8(key, value, key_cache, value_cache, slot_mapping, k_scale,
+                              v_scale, *, d_error=None, stream=None, lib=None):
+    """pa_reshape_and_cache into INT8 pools: caches int8 [NB, bs, Hkv, D];
+    k_scale / v_scale float32 [Hkv] (per-KV-head dequantisation scales)."""
+    _write8("int8", key, value, key_cache, value_cache, slot_mapping, k_scale, v_scale,
+            d_error, stream, lib)
+
+
+def pa_reshape_and_cache_fp8(key, value, key_cache, value_cache, slot_mapping, k_scale,
+                             v_scale, *, d_error=None, stream=None, lib=None):
+    """pa_reshape_and_cache into FP8 pools: caches of E4M3 codes (uint8 or
+    float8_e4m3fn) [NB, bs, Hkv, D]; k_scale / v_scale float32 [Hkv]."""
+    _write8("fp8", key, value, key_cache, value_cache, slot_mapping, k_scale, v_scale,
+            d_error, stream, lib)
 
 
 def pa_copy_blocks(key_cache, value_cache, block_mapping, *, d_error=None, stream=None,
@@ -238,31 +268,47 @@ def pa_decode(out, query, key_cache, value_cache, block_table, context_lens, *, 
     return out
 
 
+def _decode8(fmt, out, query, key_cache, value_cache, block_table, context_lens, k_scale,
+             v_scale, scale, max_context_len, partition_size, workspace, d_error, stream, lib):
+    lib = lib or library()
+    s, hq, d = query.shape
+    nb, bs, hkv, _ = key_cache.shape
+    _check_pools8(fmt, key_cache, value_cache)
+    if block_table.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_table and context_lens must be int32")
+    P, need = pa_decode_plan(s, hq, hkv, d, max_context_len, partition_size, lib=lib)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    name = f"pa_decode_{fmt}"
+    st = getattr(lib, name)(
+        _ptr(out), _rows(out, "out"), _ptr(query), _rows(query, "query"), _ptr(key_cache),
+        _ptr(value_cache), _ptr(block_table), block_table.stride(0), block_table.shape[1],
+        _ptr(context_lens), s, hq, hkv, d, bs, nb, _scales(k_scale, hkv, "k_scale"),
+        _scales(v_scale, hkv, "v_scale"), float(scale), int(max_context_len), P,
+        _ptr(workspace), wbytes, _DTYPE[query.dtype], _ptr(d_error), _stream(stream))
+    _check(lib, st, name)
+    return out
+
+
 def pa_decode_int8(out, query, key_cache, value_cache, block_table, context_lens, k_scale,
                    v_scale, *, scale, max_context_len, partition_size=0, workspace=None,
                    d_error=None, stream=None, lib=None):
     """pa_decode over INT8 pools (int8 [NB, bs, Hkv, D], head_dim 128) with
     per-KV-head float32 scales k_scale / v_scale [Hkv]."""
-    lib = lib or library()
-    s, hq, d = query.shape
-    nb, bs, hkv, _ = key_cache.shape
-    if key_cache.dtype != torch.int8 or value_cache.dtype != torch.int8:
-        raise ValueError("INT8 caches must be int8")
-    P, need = pa_decode_plan(s, hq, hkv, d, max_context_len, partition_size, lib=lib)
-    if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
-    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    if block_table.dtype != torch.int32 or context_lens.dtype != torch.int32:
-        raise ValueError("block_table and context_lens must be int32")
-    st = lib.pa_decode_int8(_ptr(out), _rows(out, "out"), _ptr(query), _rows(query, "query"),
-                            _ptr(key_cache), _ptr(value_cache), _ptr(block_table),
-                            block_table.stride(0), block_table.shape[1], _ptr(context_lens), s,
-                            hq, hkv, d, bs, nb, _scales(k_scale, hkv, "k_scale"),
-                            _scales(v_scale, hkv, "v_scale"), float(scale),
-                            int(max_context_len), P, _ptr(workspace), wbytes,
-                            _DTYPE[query.dtype], _ptr(d_error), _stream(stream))
-    _check(lib, st, "pa_decode_int8")
-    return out
+    return _decode8("int8", out, query, key_cache, value_cache, block_table, context_lens,
+                    k_scale, v_scale, scale, max_context_len, partition_size, workspace,
+                    d_error, stream, lib)
+
+
+def pa_decode_fp8(out, query, key_cache, value_cache, block_table, context_lens, k_scale,
+                  v_scale, *, scale, max_context_len, partition_size=0, workspace=None,
+                  d_error=None, stream=None, lib=None):
+    """pa_decode over FP8 pools (E4M3 codes, uint8 or float8_e4m3fn
+    [NB, bs, Hkv, D], head_dim 128) with per-KV-head float32 scales."""
+    return _decode8("fp8", out, query, key_cache, value_cache, block_table, context_lens,
+                    k_scale, v_scale, scale, max_context_len, partition_size, workspace,
+                    d_error, stream, lib)
 
 
 def pa_decode_write(out, query, key, value, key_cache, value_cache, slot_mapping, block_table,
@@ -298,22 +344,16 @@ def pa_decode_write(out, query, key, value, key_cache, value_cache, slot_mapping
     return out
 
 
-def pa_decode_write_int8(out, query, key, value, key_cache, value_cache, slot_mapping,
-                         block_table, context_lens, k_scale, v_scale, *, scale, max_context_len,
-                         partition_size=0, workspace=None, d_error=None, stream=None, lib=None):
-    """One decode step over INT8 pools in one call: pa_reshape_and_cache_int8
-    then pa_decode_int8, the decode overlapping the write.  Arguments as for
-    those two functions."""
+def _decode_write8(fmt, out, query, key, value, key_cache, value_cache, slot_mapping,
+                   block_table, context_lens, k_scale, v_scale, scale, max_context_len,
+                   partition_size, workspace, d_error, stream, lib):
     lib = lib or library()
     s, hq, d = query.shape
     nb, bs, hkv, _ = key_cache.shape
     ks = _rows(key, "key")
     if _rows(value, "value") != ks:
         raise ValueError("key and value must share a row stride")
-    if key_cache.dtype != torch.int8 or value_cache.dtype != torch.int8:
-        raise ValueError("INT8 caches must be int8")
-    if not key_cache.is_contiguous() or not value_cache.is_contiguous():
-        raise ValueError("caches must be contiguous [num_blocks, block_size, Hkv, D]")
+    _check_pools8(fmt, key_cache, value_cache)
     if slot_mapping.dtype != torch.int64:
         raise ValueError("slot_mapping must be int64")
     if block_table.dtype != torch.int32 or context_lens.dtype != torch.int32:
@@ -322,15 +362,37 @@ def pa_decode_write_int8(out, query, key, value, key_cache, value_cache, slot_ma
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib.pa_decode_write_int8(
+    name = f"pa_decode_write_{fmt}"
+    st = getattr(lib, name)(
         _ptr(out), _rows(out, "out"), _ptr(query), _rows(query, "query"), _ptr(key),
         _ptr(value), ks, _ptr(key_cache), _ptr(value_cache), _ptr(slot_mapping), key.shape[0],
         _ptr(block_table), block_table.stride(0), block_table.shape[1], _ptr(context_lens), s,
         hq, hkv, d, bs, nb, _scales(k_scale, hkv, "k_scale"), _scales(v_scale, hkv, "v_scale"),
         float(scale), int(max_context_len), P, _ptr(workspace), wbytes, _DTYPE[query.dtype],
         _ptr(d_error), _stream(stream))
-    _check(lib, st, "pa_decode_write_int8")
+    _check(lib, st, name)
     return out
+
+
+def pa_decode_write_int8(out, query, key, value, key_cache, value_cache, slot_mapping,
+                         block_table, context_lens, k_scale, v_scale, *, scale, max_context_len,
+                         partition_size=0, workspace=None, d_error=None, stream=None, lib=None):
+    """One decode step over INT8 pools in one call: pa_reshape_and_cache_int8
+    then pa_decode_int8, the decode overlapping the write.  Arguments as for
+    those two functions."""
+    return _decode_write8("int8", out, query, key, value, key_cache, value_cache, slot_mapping,
+                          block_table, context_lens, k_scale, v_scale, scale, max_context_len,
+                          partition_size, workspace, d_error, stream, lib)
+
+
+def pa_decode_write_fp8(out, query, key, value, key_cache, value_cache, slot_mapping,
+                        block_table, context_lens, k_scale, v_scale, *, scale, max_context_len,
+                        partition_size=0, workspace=None, d_error=None, stream=None, lib=None):
+    """One decode step over FP8 pools in one call: pa_reshape_and_cache_fp8
+    then pa_decode_fp8.  Arguments as for those two functions."""
+    return _decode_write8("fp8", out, query, key, value, key_cache, value_cache, slot_mapping,
+                          block_table, context_lens, k_scale, v_scale, scale, max_context_len,
+                          partition_size, workspace, d_error, stream, lib)
 
 
 def pa_prefill_varlen(out, query, key_cache, value_cache, block_table, cu_seqlens_q,

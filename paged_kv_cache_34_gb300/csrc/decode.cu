@@ -265,30 +265,39 @@ __device__ __forceinline__ void load_q(uint32_t (&qf)[D / 16][2], const DecodePa
   }
 }
 
-// Widens int8 codes c (four per word) to fp16 pairs exactly: with the sign
-// bit flipped a code is the byte u = c + 128, the fp16 with bits 0x6400 | u
-// is 1024 + u, and subtracting 1152 leaves c.  lo gets bytes 0-1, hi 2-3.
+// Widens four 8-bit codes (one word) to two fp16 pairs exactly: lo gets
+// bytes 0-1, hi bytes 2-3 (the lower byte in the lower half).  INT8: with the
+// sign bit flipped a code is the byte u = c + 128, the fp16 with bits
+// 0x6400 | u is 1024 + u, and subtracting 1152 leaves c.  FP8 (E4M3): every
+// E4M3 value is an fp16 value; the hardware converts two per instruction.
+template <bool FP8>
 __device__ __forceinline__ void widen4(uint32_t w, uint32_t &lo, uint32_t &hi) {
-  const uint32_t u = w ^ 0x80808080u;
-  uint32_t a, b;
-  asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
-  asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(b) : "r"(u), "r"(0x64646464u));
-  const __half2 off = __floats2half2_rn(1152.0f, 1152.0f);
-  __half2 ha = __hsub2(*reinterpret_cast<__half2 *>(&a), off);
-  __half2 hb = __hsub2(*reinterpret_cast<__half2 *>(&b), off);
-  lo = *reinterpret_cast<uint32_t *>(&ha);
-  hi = *reinterpret_cast<uint32_t *>(&hb);
+  if constexpr (FP8) {
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"(static_cast<uint16_t>(w & 0xffffu)));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"(static_cast<uint16_t>(w >> 16)));
+  } else {
+    const uint32_t u = w ^ 0x80808080u;
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+    const __half2 off = __floats2half2_rn(1152.0f, 1152.0f);
+    __half2 ha = __hsub2(*reinterpret_cast<__half2 *>(&a), off);
+    __half2 hb = __hsub2(*reinterpret_cast<__half2 *>(&b), off);
+    lo = *reinterpret_cast<uint32_t *>(&ha);
+    hi = *reinterpret_cast<uint32_t *>(&hb);
+  }
 }
 
-// Two int8 words a, b holding the same four elements of two tokens -> the
+// Two code words a, b holding the same four elements of two tokens -> the
 // fp16 pairs (a.byte i, b.byte i): e0 for i = 0, e1 for 1, e2 for 2, e3 for 3.
+template <bool FP8>
 __device__ __forceinline__ void widen_tokens(uint32_t a, uint32_t b, uint32_t &e0,
                                              uint32_t &e1, uint32_t &e2, uint32_t &e3) {
   uint32_t x, y;
   asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(x) : "r"(a), "r"(b));
   asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(y) : "r"(a), "r"(b));
-  widen4(x, e0, e1);
-  widen4(y, e2, e3);
+  widen4<FP8>(x, e0, e1);
+  widen4<FP8>(y, e2, e3);
 }
 
 __device__ __forceinline__ void lds128(uint32_t addr, uint32_t (&w)[4]) {
@@ -297,10 +306,13 @@ __device__ __forceinline__ void lds128(uint32_t addr, uint32_t (&w)[4]) {
                : "r"(addr));
 }
 
-template <class E, int D, int BOXR, bool BAL, bool KV8>
+// KVF: the pool format -- 0 fp16/bf16 (as E), 1 INT8 codes, 2 FP8 (E4M3) codes.
+template <class E, int D, int BOXR, bool BAL, int KVF>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_persistent_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                              const __grid_constant__ CUtensorMap tmv) {
+  constexpr bool KV8 = KVF != 0;  // 8-bit codes, widened to fp16
+  constexpr bool FP8 = KVF == 2;
   using S = DecodeSmem<D, KV8>;
   using M = std::conditional_t<KV8, F16, E>;  // the tensor cores' operand type
   constexpr int NH = S::kHalves;
@@ -772,8 +784,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int u = 0; u < NT; ++u) {
             uint32_t a0, a1, a2, a3;
-            widen4(kw[u][0][ks >> 2][ks & 3], a0, a2);
-            widen4(kw[u][1][ks >> 2][ks & 3], a1, a3);
+            widen4<FP8>(kw[u][0][ks >> 2][ks & 3], a0, a2);
+            widen4<FP8>(kw[u][1][ks >> 2][ks & 3], a1, a3);
             mma_16816<false>(sc[u], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
           }
         // V's codes once K's are spent (fewer live registers); their loads
@@ -790,6 +802,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(empty + s));
         released = true;
+        if constexpr (FP8) {
+          // An E4M3 byte can be a NaN code: V rows past the context (stale or
+          // unwritten) become exact zeros.  K's are masked out of the scores.
+          if (j0 + ROWS > end) {
+#pragma unroll
+            for (int u = 0; u < NT; ++u)
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                if (j0 + 16 * u + v0 + (i & 1) + 8 * (i >> 1) >= end)
+                  vw[u][i][0] = vw[u][i][1] = vw[u][i][2] = vw[u][i][3] = 0u;
+          }
+        }
       } else {
         const uint32_t kb = smem_u32(kst);
         if (j0 + ROWS > end) {
@@ -876,8 +900,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int u = 0; u < NT; ++u) {
             uint32_t a0, a1, b0, b1, a2, a3, b2, b3;
-            widen_tokens(vw[u][0][w], vw[u][1][w], a0, a1, b0, b1);  // tokens 2t, 2t + 1
-            widen_tokens(vw[u][2][w], vw[u][3][w], a2, a3, b2, b3);  // tokens 2t + 8, + 9
+            widen_tokens<FP8>(vw[u][0][w], vw[u][1][w], a0, a1, b0, b1);  // tokens 2t, 2t + 1
+            widen_tokens<FP8>(vw[u][2][w], vw[u][3][w], a2, a3, b2, b3);  // tokens 2t + 8, + 9
             mma_16816<false>(o[2 * w], a0, a1, a2, a3, pb[u][0], pb[u][1]);
             mma_16816<false>(o[2 * w + 1], b0, b1, b2, b3, pb[u][0], pb[u][1]);
           }
@@ -1066,32 +1090,32 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
   }
 }
 
-template <class E, int D, int BOXR, bool BAL, bool KV8>
+template <class E, int D, int BOXR, bool BAL, int KVF>
 cudaError_t launch_kernel(const DecodeArgs &a, const DecodeParams &p, cudaStream_t stream) {
-  using S = DecodeSmem<D, KV8>;
+  using S = DecodeSmem<D, KVF != 0>;
   const int smem = S::bytes(a.num_seqs, p.max_ids);
-  auto kernel = decode_persistent_kernel<E, D, BOXR, BAL, KV8>;
-  cudaError_t e = allow_dynamic_smem<decode_persistent_kernel<E, D, BOXR, BAL, KV8>>();
+  auto kernel = decode_persistent_kernel<E, D, BOXR, BAL, KVF>;
+  cudaError_t e = allow_dynamic_smem<decode_persistent_kernel<E, D, BOXR, BAL, KVF>>();
   if (e != cudaSuccess) return e;
   return launch_pdl(kernel, dim3(static_cast<unsigned>(a.grid)), dim3(kThreads), smem, stream,
                     p, a.tm_k, a.tm_v);
 }
 
-template <class E, int D, int BOXR, bool KV8>
+template <class E, int D, int BOXR, int KVF>
 cudaError_t launch_typed(const DecodeArgs &a, const DecodeParams &p, cudaStream_t stream) {
-  const cudaError_t e = p.balanced ? launch_kernel<E, D, BOXR, true, KV8>(a, p, stream)
-                                   : launch_kernel<E, D, BOXR, false, KV8>(a, p, stream);
+  const cudaError_t e = p.balanced ? launch_kernel<E, D, BOXR, true, KVF>(a, p, stream)
+                                   : launch_kernel<E, D, BOXR, false, KVF>(a, p, stream);
   if (e != cudaSuccess || !a.merge) return e;
   const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.num_q_heads;
   return launch_pdl(decode_combine_kernel<E, D>, dim3(static_cast<unsigned>(rows)),
                     dim3(kCombineWarps * 32), 0, stream, p);
 }
 
-template <class E, int D, bool KV8 = false>
+template <class E, int D, int KVF = 0>
 cudaError_t launch_box(const DecodeArgs &a, const DecodeParams &p, cudaStream_t stream) {
   switch (a.box_rows) {
-    case 8: return launch_typed<E, D, 8, KV8>(a, p, stream);
-    case 16: return launch_typed<E, D, 16, KV8>(a, p, stream);
+    case 8: return launch_typed<E, D, 8, KVF>(a, p, stream);
+    case 16: return launch_typed<E, D, 16, KVF>(a, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1140,11 +1164,12 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
   p.v_scale = a.v_scale;
   p.err = a.d_error;
   const bool bf = a.dtype == PA_BF16;
+  if (a.head_dim == 128 && a.kv_int8 && a.kv_fp8)
+    return bf ? launch_box<BF16, 128, 2>(a, p, stream) : launch_box<F16, 128, 2>(a, p, stream);
+  if (a.head_dim == 128 && a.kv_int8)
+    return bf ? launch_box<BF16, 128, 1>(a, p, stream) : launch_box<F16, 128, 1>(a, p, stream);
   if (a.head_dim == 128)
-    return a.kv_int8
-               ? (bf ? launch_box<BF16, 128, true>(a, p, stream)
-                     : launch_box<F16, 128, true>(a, p, stream))
-               : (bf ? launch_box<BF16, 128>(a, p, stream) : launch_box<F16, 128>(a, p, stream));
+    return bf ? launch_box<BF16, 128>(a, p, stream) : launch_box<F16, 128>(a, p, stream);
   if (a.head_dim == 64)
     return bf ? launch_box<BF16, 64>(a, p, stream) : launch_box<F16, 64>(a, p, stream);
   return cudaErrorInvalidValue;

@@ -184,6 +184,36 @@ pa_status prepare_write(const void *key, const void *value, int64_t kv_row_strid
   return PA_OK;
 }
 
+// The write into 8-bit pools (INT8, or E4M3 with fp8).
+pa_status write_8bit(const void *key, const void *value, int64_t kv_row_stride, void *key_cache,
+                     void *value_cache, const int64_t *slot_mapping, int32_t num_tokens,
+                     int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                     int64_t num_blocks, const float *k_scale, const float *v_scale,
+                     pa_dtype dtype, int32_t *d_error, void *stream, bool fp8) {
+  pa::ReshapeArgs w;
+  bool empty = true;
+  const pa_status st = prepare_write(key, value, kv_row_stride, key_cache, value_cache,
+                                     slot_mapping, num_tokens, num_kv_heads, head_dim, block_size,
+                                     num_blocks, dtype, d_error, &w, &empty);
+  if (st != PA_OK) return st;
+  if (!k_scale || !v_scale) return PA_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(k_scale) | reinterpret_cast<uintptr_t>(v_scale)) & 3u)
+    return PA_ERR_ALIGN;
+  // int8 pool rows in 16-byte chunks, a chunk within one head
+  if (head_dim % 16 != 0) return PA_ERR_ALIGN;
+  if (empty) return PA_OK;
+  w.int8 = true;
+  w.fp8 = fp8;
+  w.dtype = dtype;
+  w.head_dim = head_dim;
+  w.k_scale = k_scale;
+  w.v_scale = v_scale;
+  cudaError_t e = current_num_sms(&w.num_sms);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = pa::launch_reshape_and_cache(w, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -237,27 +267,21 @@ pa_status pa_reshape_and_cache_int8(const void *key, const void *value, int64_t 
                                     int64_t num_blocks, const float *k_scale,
                                     const float *v_scale, pa_dtype dtype, int32_t *d_error,
                                     void *stream) {
-  pa::ReshapeArgs w;
-  bool empty = true;
-  const pa_status st = prepare_write(key, value, kv_row_stride, key_cache, value_cache,
-                                     slot_mapping, num_tokens, num_kv_heads, head_dim, block_size,
-                                     num_blocks, dtype, d_error, &w, &empty);
-  if (st != PA_OK) return st;
-  if (!k_scale || !v_scale) return PA_ERR_NULL;
-  if ((reinterpret_cast<uintptr_t>(k_scale) | reinterpret_cast<uintptr_t>(v_scale)) & 3u)
-    return PA_ERR_ALIGN;
-  // int8 pool rows in 16-byte chunks, a chunk within one head
-  if (head_dim % 16 != 0) return PA_ERR_ALIGN;
-  if (empty) return PA_OK;
-  w.int8 = true;
-  w.dtype = dtype;
-  w.head_dim = head_dim;
-  w.k_scale = k_scale;
-  w.v_scale = v_scale;
-  cudaError_t e = current_num_sms(&w.num_sms);
-  if (e != cudaSuccess) return cuda_fail(e);
-  e = pa::launch_reshape_and_cache(w, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+  return write_8bit(key, value, kv_row_stride, key_cache, value_cache, slot_mapping, num_tokens,
+                    num_kv_heads, head_dim, block_size, num_blocks, k_scale, v_scale, dtype,
+                    d_error, stream, false);
+}
+
+pa_status pa_reshape_and_cache_fp8(const void *key, const void *value, int64_t kv_row_stride,
+                                   void *key_cache, void *value_cache,
+                                   const int64_t *slot_mapping, int32_t num_tokens,
+                                   int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                   int64_t num_blocks, const float *k_scale,
+                                   const float *v_scale, pa_dtype dtype, int32_t *d_error,
+                                   void *stream) {
+  return write_8bit(key, value, kv_row_stride, key_cache, value_cache, slot_mapping, num_tokens,
+                    num_kv_heads, head_dim, block_size, num_blocks, k_scale, v_scale, dtype,
+                    d_error, stream, true);
 }
 
 pa_status pa_decode_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
@@ -308,7 +332,7 @@ pa_status decode_call(void *out, int64_t out_row_stride, const void *query, int6
                       int32_t partition_size, void *workspace, size_t workspace_bytes,
                       pa_dtype dtype, int32_t *d_error, void *stream,
                       const pa::ReshapeArgs *write, const float *k_scale = nullptr,
-                      const float *v_scale = nullptr) {
+                      const float *v_scale = nullptr, bool fp8 = false) {
   const bool int8 = k_scale != nullptr || v_scale != nullptr;
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq < 0 || max_context_len < 0 ||
@@ -415,6 +439,7 @@ pa_status decode_call(void *out, int64_t out_row_stride, const void *query, int6
                        a.box_rows, int8))
     return cuda_fail(cudaErrorInvalidValue);
   a.kv_int8 = int8;
+  a.kv_fp8 = int8 && fp8;
   a.k_scale = k_scale;
   a.v_scale = v_scale;
   a.after_write = false;
@@ -464,6 +489,24 @@ pa_status pa_decode_int8(void *out, int64_t out_row_stride, const void *query,
                      num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
                      max_context_len, partition_size, workspace, workspace_bytes, dtype, d_error,
                      stream, nullptr, k_scale, v_scale);
+}
+
+pa_status pa_decode_fp8(void *out, int64_t out_row_stride, const void *query,
+                        int64_t q_row_stride, const void *key_cache, const void *value_cache,
+                        const int32_t *block_table, int64_t block_table_stride,
+                        int32_t max_blocks_per_seq, const int32_t *context_lens,
+                        int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                        int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                        const float *k_scale, const float *v_scale, float scale,
+                        int32_t max_context_len, int32_t partition_size, void *workspace,
+                        size_t workspace_bytes, pa_dtype dtype, int32_t *d_error,
+                        void *stream) {
+  if (!k_scale || !v_scale) return PA_ERR_NULL;
+  return decode_call(out, out_row_stride, query, q_row_stride, key_cache, value_cache,
+                     block_table, block_table_stride, max_blocks_per_seq, context_lens, num_seqs,
+                     num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                     max_context_len, partition_size, workspace, workspace_bytes, dtype, d_error,
+                     stream, nullptr, k_scale, v_scale, true);
 }
 
 pa_status pa_decode_write(void *out, int64_t out_row_stride, const void *query,
@@ -519,6 +562,38 @@ pa_status pa_decode_write_int8(void *out, int64_t out_row_stride, const void *qu
                      num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
                      max_context_len, partition_size, workspace, workspace_bytes, dtype, d_error,
                      stream, empty ? nullptr : &w, k_scale, v_scale);
+}
+
+pa_status pa_decode_write_fp8(void *out, int64_t out_row_stride, const void *query,
+                              int64_t q_row_stride, const void *key, const void *value,
+                              int64_t kv_row_stride, void *key_cache, void *value_cache,
+                              const int64_t *slot_mapping, int32_t num_new_tokens,
+                              const int32_t *block_table, int64_t block_table_stride,
+                              int32_t max_blocks_per_seq, const int32_t *context_lens,
+                              int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                              const float *k_scale, const float *v_scale, float scale,
+                              int32_t max_context_len, int32_t partition_size,
+                              void *workspace, size_t workspace_bytes, pa_dtype dtype,
+                              int32_t *d_error, void *stream) {
+  if (!k_scale || !v_scale) return PA_ERR_NULL;
+  pa::ReshapeArgs w;
+  bool empty = true;
+  const pa_status st = prepare_write(key, value, kv_row_stride, key_cache, value_cache,
+                                     slot_mapping, num_new_tokens, num_kv_heads, head_dim,
+                                     block_size, num_blocks, dtype, d_error, &w, &empty);
+  if (st != PA_OK) return st;
+  w.int8 = true;
+  w.fp8 = true;
+  w.dtype = dtype;
+  w.head_dim = head_dim;
+  w.k_scale = k_scale;
+  w.v_scale = v_scale;
+  return decode_call(out, out_row_stride, query, q_row_stride, key_cache, value_cache,
+                     block_table, block_table_stride, max_blocks_per_seq, context_lens, num_seqs,
+                     num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                     max_context_len, partition_size, workspace, workspace_bytes, dtype, d_error,
+                     stream, empty ? nullptr : &w, k_scale, v_scale, true);
 }
 
 pa_status pa_prefill_varlen(void *out, int64_t out_row_stride, const void *query,

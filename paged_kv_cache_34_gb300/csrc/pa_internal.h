@@ -22,9 +22,11 @@ struct ReshapeArgs {
   int64_t num_slots;  // num_blocks * block_size
   int32_t *d_error;
   int num_sms;
-  // INT8 pools: the inputs are `dtype` (fp16/bf16), the pools int8 codes
-  // under the per-KV-head scales; row_bytes counts the 16-bit input row.
+  // 8-bit pools: the inputs are `dtype` (fp16/bf16), the pools INT8 codes
+  // (or, with fp8, E4M3 codes) under the per-KV-head scales; row_bytes
+  // counts the 16-bit input row.
   bool int8 = false;
+  bool fp8 = false;
   pa_dtype dtype = PA_F16;
   int32_t head_dim = 0;
   const float *k_scale = nullptr, *v_scale = nullptr;
@@ -98,7 +100,8 @@ struct DecodeArgs {
   CUtensorMap tm_k, tm_v;  // pool maps, box (64 | 128 for INT8, 1, box_rows), 128B swizzle
   int box_rows;
   int num_sms;
-  bool kv_int8 = false;  // INT8 pools (head_dim 128) with per-KV-head scales
+  bool kv_int8 = false;  // 8-bit pools (head_dim 128) with per-KV-head scales
+  bool kv_fp8 = false;   // ... holding E4M3 codes rather than INT8
   const float *k_scale = nullptr, *v_scale = nullptr;
 };
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);

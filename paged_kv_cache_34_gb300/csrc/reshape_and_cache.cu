@@ -74,21 +74,39 @@ __device__ __forceinline__ uint32_t code8(float x, float s) {
   return static_cast<uint32_t>(c) & 0xffu;
 }
 
+// FP8 pools: each value is stored as the nearest E4M3 value (ties to even,
+// saturating at +-448) to x / scale, the division in fp32; NaN -> 0 (the same
+// reading of the pages' quantised-KV scales, with the OCP E4M3 format).  Two
+// values per conversion: `lo` in the low byte.
+__device__ __forceinline__ uint32_t fp8_pair(float lo, float hi, float s) {
+  const float a = lo != lo ? 0.0f : __fdiv_rn(lo, s);
+  const float b = hi != hi ? 0.0f : __fdiv_rn(hi, s);
+  uint16_t r;
+  // the first source goes to the upper byte
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+  return r;
+}
+
 // 16 values (two 16-byte vectors of fp16/bf16 pairs) -> 16 codes.
-template <class E>
+template <class E, bool FP8>
 __device__ __forceinline__ uint4 quant16(const uint4 &a, const uint4 &b, float s) {
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
   uint32_t out[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const uint32_t w0 = w[2 * q], w1 = w[2 * q + 1];
-    out[q] = code8(E::lo(w0), s) | (code8(E::hi(w0), s) << 8) | (code8(E::lo(w1), s) << 16) |
-             (code8(E::hi(w1), s) << 24);
+    if constexpr (FP8) {
+      out[q] = fp8_pair(E::lo(w0), E::hi(w0), s) | (fp8_pair(E::lo(w1), E::hi(w1), s) << 16);
+    } else {
+      out[q] = code8(E::lo(w0), s) | (code8(E::hi(w0), s) << 8) |
+               (code8(E::lo(w1), s) << 16) | (code8(E::hi(w1), s) << 24);
+    }
   }
   return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
-template <class E>
+// The write into 8-bit pools (INT8 or, with FP8, E4M3 codes).
+template <class E, bool FP8>
 __global__ void __launch_bounds__(256) reshape_and_cache_int8_kernel(
     const uint4 *__restrict__ key, const uint4 *__restrict__ value, int64_t row_stride_vec,
     uint4 *__restrict__ key_cache, uint4 *__restrict__ value_cache,
@@ -118,8 +136,8 @@ __global__ void __launch_bounds__(256) reshape_and_cache_int8_kernel(
       const bool good = scale_ok(ksc) && scale_ok(vsc);
       if (!good) raise_error(err, PA_DEVERR_SCALE);
       const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-      kd[i] = good ? quant16<E>(k0, k1, ksc) : zero;
-      vd[i] = good ? quant16<E>(v0, v1, vsc) : zero;
+      kd[i] = good ? quant16<E, FP8>(k0, k1, ksc) : zero;
+      vd[i] = good ? quant16<E, FP8>(v0, v1, vsc) : zero;
     }
   }
 }
@@ -131,8 +149,10 @@ cudaError_t launch_reshape_and_cache(const ReshapeArgs &a, cudaStream_t stream) 
     if (row_vec8 < 256) threads = ((row_vec8 + 31) / 32) * 32;
     const int64_t max_ctas = static_cast<int64_t>(a.num_sms) * 16;
     const int grid = static_cast<int>(a.num_tokens < max_ctas ? a.num_tokens : max_ctas);
-    auto kernel = a.dtype == PA_BF16 ? reshape_and_cache_int8_kernel<BF16>
-                                     : reshape_and_cache_int8_kernel<F16>;
+    auto kernel = a.fp8 ? (a.dtype == PA_BF16 ? reshape_and_cache_int8_kernel<BF16, true>
+                                              : reshape_and_cache_int8_kernel<F16, true>)
+                        : (a.dtype == PA_BF16 ? reshape_and_cache_int8_kernel<BF16, false>
+                                              : reshape_and_cache_int8_kernel<F16, false>);
     return launch_pdl(kernel, dim3(grid), dim3(threads), 0, stream,
                       static_cast<const uint4 *>(a.key), static_cast<const uint4 *>(a.value),
                       static_cast<int64_t>(a.row_stride_bytes / 16),

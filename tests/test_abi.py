@@ -212,3 +212,21 @@ def test_decode_write_int8_host_validation(lib):
     assert call(kv_stride=100) == 2
     assert call(d=64, kv_stride=128) == 3  # INT8 decode: head_dim 128 only
     assert call(ks=ctypes.c_void_p(0x10002)) == 4
+
+
+def test_fp8_host_validation(lib):
+    # the FP8 calls share the INT8 calls' checks
+    w = lib.pa_reshape_and_cache_fp8
+    assert w(FAKE, FAKE, 256, FAKE, FAKE, FAKE, 0, 2, 128, 16, 8, FAKE, FAKE, 0, None, None) == 0
+    assert w(FAKE, FAKE, 256, FAKE, FAKE, FAKE, 3, 2, 128, 16, 8, None, FAKE, 0, None, None) == 1
+    assert w(FAKE, FAKE, 80, FAKE, FAKE, FAKE, 3, 2, 40, 16, 8, FAKE, FAKE, 0, None, None) == 4
+    d = lib.pa_decode_fp8
+    # out, out_stride, q, q_stride, kc, vc, bt, bt_stride, mbps, ctx, s, hq, hkv, d, bs, nb,
+    # k_scale, v_scale, scale, max_ctx, part, ws, ws_bytes, dtype, err, stream
+    assert d(FAKE, 1024, FAKE, 1024, FAKE, FAKE, FAKE, 16, 16, FAKE, 4, 8, 2, 128, 16, 64,
+             None, FAKE, 0.125, 100, 0, None, 0, 0, None, None) == 1
+    assert d(FAKE, 512, FAKE, 512, FAKE, FAKE, FAKE, 16, 16, FAKE, 4, 8, 2, 64, 16, 64,
+             FAKE, FAKE, 0.125, 100, 0, None, 0, 0, None, None) == 3
+    s = lib.pa_decode_write_fp8
+    assert s(FAKE, 1024, FAKE, 1024, FAKE, FAKE, 256, FAKE, FAKE, None, 4, FAKE, 16, 16, FAKE,
+             4, 8, 2, 128, 16, 64, FAKE, FAKE, 0.125, 100, 0, None, 0, 0, None, None) == 1

@@ -1,11 +1,12 @@
-"""INT8 KV pools on the GPU.
+"""8-bit KV pools (INT8 and FP8 E4M3) on the GPU.
 
-pa_reshape_and_cache_int8 must store the oracle's codes bit for bit, and
-pa_decode_int8 must match the oracle's decode over the same codes within the
-dtype's tolerance (cannbot-skills page App. A lists per-head dequantisation
-scales for key and value; the quantisation rule -- round-half-even(x / scale)
-in fp32, clamped to [-127, 127] -- is this library's reading, stated in
-include/pa.h and pinned in the oracle's tests)."""
+The writes must store the oracle's codes bit for bit, and the decodes must
+match the oracle's decode over the same codes within the dtype's tolerance
+(cannbot-skills page App. A lists per-head dequantisation scales for key and
+value; the quantisation rules -- INT8: round-half-even(x / scale) in fp32,
+clamped to +-127; FP8: the nearest E4M3 value to x / scale, ties to even,
+saturating at 448 -- are this library's readings, stated in include/pa.h and
+pinned in the oracle's tests).  Every test runs for both formats."""
 import numpy as np
 import pytest
 import torch
@@ -17,6 +18,18 @@ from gpu_util import (W, assert_close, cfg, gpu, new_err, oracle_pools_after_wri
 pytestmark = gpu
 
 TORCH16 = {oracle.BF16: torch.bfloat16, oracle.F16: torch.float16}
+FORMATS = ["int8", "fp8"]
+CODE_DTYPE = {"int8": np.int8, "fp8": np.uint8}
+CODE_MAX = {"int8": 127.0, "fp8": 448.0}
+# a byte the write never stores, placed where no decode may look: INT8 -128,
+# FP8 a NaN code
+POISON = {"int8": -128, "fp8": 0x7F}
+QUANTIZE = {"int8": oracle.quantize_int8, "fp8": oracle.quantize_fp8}
+ORACLE_WRITE = {"int8": oracle.write_int8, "fp8": oracle.write_fp8}
+ORACLE_DECODE = {"int8": oracle.decode_int8, "fp8": oracle.decode_fp8}
+GPU_WRITE = {"int8": pa.pa_reshape_and_cache_int8, "fp8": pa.pa_reshape_and_cache_fp8}
+GPU_DECODE = {"int8": pa.pa_decode_int8, "fp8": pa.pa_decode_fp8}
+GPU_STEP = {"int8": pa.pa_decode_write_int8, "fp8": pa.pa_decode_write_fp8}
 
 
 def used_blocks(x_host):
@@ -26,11 +39,11 @@ def used_blocks(x_host):
     return np.unique(np.concatenate(ids)) if ids else np.zeros(0, np.int64)
 
 
-def head_scales(pool, hkv):
-    """Per-KV-head absmax / 127 over the pool's finite values (fp32)."""
+def head_scales(pool, hkv, fmt):
+    """Per-KV-head absmax / (largest code) over the pool's finite values (fp32)."""
     a = pool.float().reshape(-1, hkv, pool.shape[-1])
     a = torch.where(torch.isfinite(a), a.abs(), torch.zeros_like(a))
-    return (a.amax(dim=(0, 2)) / 127).clamp_min(1e-6).to(torch.float32).contiguous()
+    return (a.amax(dim=(0, 2)) / CODE_MAX[fmt]).clamp_min(1e-6).to(torch.float32).contiguous()
 
 
 def as16(patterns, dtype_code):
@@ -38,102 +51,122 @@ def as16(patterns, dtype_code):
         TORCH16[dtype_code])
 
 
-def int8_pools(x_host):
+def poison_past_context(pool, x_host, fmt):
+    """Rows of the used blocks past each sequence's context get POISON."""
+    bt, bs = x_host.block_table.numpy(), x_host.block_size
+    flat = pool.reshape(-1, *pool.shape[2:])
+    for b, L in enumerate(x_host.context_lens.tolist()):
+        n = -(-int(L) // bs)
+        for j in range(int(L), n * bs):
+            flat[int(bt[b, j // bs]) * bs + j % bs] = POISON[fmt]
+
+
+def pools8(x_host, fmt):
     """The oracle's codes of the workload's pools after this step's write
-    (blocks the decode never reads stay 0)."""
+    (blocks the decode never reads stay 0, rows past a context hold POISON)."""
     code = oracle.dtype_code(x_host.dtype)
     kp, vp = oracle_pools_after_write(x_host)
     used = torch.from_numpy(used_blocks(x_host).astype(np.int64))
     k16, v16 = as16(kp, code)[used], as16(vp, code)[used]
     hkv = x_host.num_kv_heads
-    ks, vs = head_scales(k16, hkv), head_scales(v16, hkv)
-    kc = np.zeros(kp.shape, np.int8)
-    vc = np.zeros(vp.shape, np.int8)
+    ks, vs = head_scales(k16, hkv, fmt), head_scales(v16, hkv, fmt)
+    kc = np.zeros(kp.shape, CODE_DTYPE[fmt])
+    vc = np.zeros(vp.shape, CODE_DTYPE[fmt])
     u = used.numpy()
     for g in range(hkv):
-        kc[u, :, g] = oracle.quantize_int8(k16[:, :, g].contiguous(), float(ks[g]))
-        vc[u, :, g] = oracle.quantize_int8(v16[:, :, g].contiguous(), float(vs[g]))
+        kc[u, :, g] = QUANTIZE[fmt](k16[:, :, g].contiguous(), float(ks[g]))
+        vc[u, :, g] = QUANTIZE[fmt](v16[:, :, g].contiguous(), float(vs[g]))
+    poison_past_context(kc, x_host, fmt)
+    poison_past_context(vc, x_host, fmt)
     return kc, vc, ks, vs
 
 
-def gpu_decode_int8(x_host, kc, vc, ks, vs, partition_size, err):
+def gpu_decode8(fmt, x_host, kc, vc, ks, vs, partition_size, err):
     q = x_host.q.cuda()
     out = torch.full_like(q, float("nan"))
-    pa.pa_decode_int8(out, q, torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda(),
-                      x_host.block_table.cuda(), x_host.context_lens.cuda(), ks.cuda(),
-                      vs.cuda(), scale=x_host.scale, max_context_len=x_host.max_context_len,
-                      partition_size=partition_size, d_error=err)
+    GPU_DECODE[fmt](out, q, torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda(),
+                    x_host.block_table.cuda(), x_host.context_lens.cuda(), ks.cuda(), vs.cuda(),
+                    scale=x_host.scale, max_context_len=x_host.max_context_len,
+                    partition_size=partition_size, d_error=err)
     return out
 
 
-def oracle_decode_int8(x_host, kc, vc, ks, vs):
-    return oracle.decode_int8(x_host.q, kc, vc, x_host.block_table, x_host.context_lens,
+def oracle_decode8(fmt, x_host, kc, vc, ks, vs):
+    return ORACLE_DECODE[fmt](x_host.q, kc, vc, x_host.block_table, x_host.context_lens,
                               x_host.num_kv_heads, x_host.block_size, x_host.scale,
                               ks.numpy(), vs.numpy(), dtype=oracle.dtype_code(x_host.dtype))
 
 
-def check_decode(x_host, partition_size, what):
+def check_decode(fmt, x_host, partition_size, what):
     require_gpu()
-    kc, vc, ks, vs = int8_pools(x_host)
+    kc, vc, ks, vs = pools8(x_host, fmt)
     err = new_err()
-    got = gpu_decode_int8(x_host, kc, vc, ks, vs, partition_size, err)
+    got = gpu_decode8(fmt, x_host, kc, vc, ks, vs, partition_size, err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0, f"{what}: device error bits {int(err.item())}"
-    return assert_close(got, oracle_decode_int8(x_host, kc, vc, ks, vs), x_host.dtype,
-                        what=what)
+    return assert_close(got, oracle_decode8(fmt, x_host, kc, vc, ks, vs), x_host.dtype,
+                        what=f"{fmt} {what}")
 
 
+@pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("partition_size", [0, 64, 512])
-def test_llama7b_decode_int8(partition_size):
-    check_decode(W.make_inputs("llama7b-decode"), partition_size, f"llama7b P{partition_size}")
+def test_llama7b_decode(fmt, partition_size):
+    check_decode(fmt, W.make_inputs("llama7b-decode"), partition_size,
+                 f"llama7b P{partition_size}")
 
 
-def test_continuous_batching_int8():
-    check_decode(W.make_inputs("continuous-batching"), 0, "continuous-batching")
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_continuous_batching(fmt):
+    check_decode(fmt, W.make_inputs("continuous-batching"), 0, "continuous-batching")
 
 
-def test_long_context_int8_full_size():
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_long_context_full_size(fmt):
     x = W.make_inputs("long-context-decode")
-    check_decode(x, x.partition_size, "long-context")
+    check_decode(fmt, x, x.partition_size, "long-context")
 
 
+@pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("bs,hq,hkv,dtype", [(16, 8, 2, "f16"), (32, 32, 8, "bf16"),
                                              (128, 64, 8, "bf16"), (8, 4, 4, "f16")])
 @pytest.mark.parametrize("partition_size", [0, 64])
-def test_int8_grid(bs, hq, hkv, dtype, partition_size):
+def test_grid(fmt, bs, hq, hkv, dtype, partition_size):
     lengths = [0, 1, bs - 1, bs, bs + 1, 63, 200, 333]
     c = cfg(hq=hq, hkv=hkv, d=128, bs=bs, nb=sum(-(-n // bs) for n in lengths) + 8,
             dtype=dtype, lengths=lengths)
     x = W.make_inputs(c, seed=300 + bs + hq)
-    check_decode(x, partition_size, f"bs{bs} g{hq // hkv} {dtype} P{partition_size}")
+    check_decode(fmt, x, partition_size, f"bs{bs} g{hq // hkv} {dtype} P{partition_size}")
 
 
-def test_int8_decode_bad_scale_gives_zero_heads():
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_decode_bad_scale_gives_zero_heads(fmt):
     require_gpu()
     x = W.make_inputs(cfg(hq=8, hkv=2, d=128, bs=16, nb=64, dtype="bf16",
                           lengths=[40, 90, 17]), seed=8)
-    kc, vc, ks, vs = int8_pools(x)
+    kc, vc, ks, vs = pools8(x, fmt)
     bad = ks.clone()
     bad[0] = -1.0
     err = new_err()
-    got = gpu_decode_int8(x, kc, vc, bad, vs, 0, err)
+    got = gpu_decode8(fmt, x, kc, vc, bad, vs, 0, err)
     torch.cuda.synchronize()
     assert int(err.item()) & pa.DEVERR_SCALE
     g = got.double().cpu().numpy()
     assert (g[:, :4] == 0).all()  # the queries of KV head 0
-    want = oracle_decode_int8(x, kc, vc, ks, vs)
+    want = oracle_decode8(fmt, x, kc, vc, ks, vs)
     assert np.abs(g[:, 4:] - want[:, 4:]).max() <= 1e-2
 
 
+@pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-def test_write_int8_bit_exact(dtype):
+def test_write_bit_exact(fmt, dtype):
     require_gpu()
     c = cfg(hq=8, hkv=2, d=128, bs=16, nb=64, dtype=dtype, lengths=[30, 50, 17, 64],
             write_new_token=True)
     x = W.make_inputs(c, seed=21)
     kn, vn = x.k_new.clone(), x.v_new.clone()
-    kn[1] *= 100  # beyond the code range: clamped
+    kn[1] *= 100  # beyond the code range: clamped / saturated
     vn[2] *= -100
+    kn[0, 0, :4] = torch.tensor([float("nan"), -0.0, 1e-30, -1e-30])  # NaN, signed zeros
     slots = x.slot_mapping.clone()
     slots[3] = -1                                 # padding: nothing written
     n = slots.numel()
@@ -142,68 +175,86 @@ def test_write_int8_bit_exact(dtype):
     vn = torch.cat([vn, vn[:1]])
     shape = tuple(x.k_pool.shape)
     g = torch.Generator().manual_seed(4)
-    k0 = torch.randint(-127, 128, shape, generator=g, dtype=torch.int8)
-    v0 = torch.randint(-127, 128, shape, generator=g, dtype=torch.int8)
+    k0 = torch.randint(0, 256, shape, generator=g, dtype=torch.uint8).numpy().view(
+        CODE_DTYPE[fmt])
+    v0 = torch.randint(0, 256, shape, generator=g, dtype=torch.uint8).numpy().view(
+        CODE_DTYPE[fmt])
     ks = torch.tensor([0.021, 0.0137], dtype=torch.float32)
     vs = torch.tensor([0.0093, 0.05], dtype=torch.float32)
-    kd, vd, err = k0.cuda(), v0.cuda(), new_err()
-    pa.pa_reshape_and_cache_int8(kn.cuda(), vn.cuda(), kd, vd, slots.cuda(), ks.cuda(),
-                                 vs.cuda(), d_error=err)
+    kd, vd, err = torch.from_numpy(k0).cuda(), torch.from_numpy(v0).cuda(), new_err()
+    GPU_WRITE[fmt](kn.cuda(), vn.cuda(), kd, vd, slots.cuda(), ks.cuda(), vs.cuda(),
+                   d_error=err)
     torch.cuda.synchronize()
     assert int(err.item()) == pa.DEVERR_SLOT
-    kw, vw = k0.numpy().copy(), v0.numpy().copy()
-    st = oracle.write_int8(kw, vw, kn, vn, slots.numpy(), 16, ks.numpy(), vs.numpy())
+    kw, vw = k0.copy(), v0.copy()
+    st = ORACLE_WRITE[fmt](kw, vw, kn, vn, slots.numpy(), 16, ks.numpy(), vs.numpy())
     assert st == oracle.ERR_SLOT and n == 4
     assert np.array_equal(kd.cpu().numpy(), kw)
     assert np.array_equal(vd.cpu().numpy(), vw)
 
 
-def test_write_int8_bad_scale():
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_write_bad_scale(fmt):
     require_gpu()
     x = W.make_inputs(cfg(hq=4, hkv=2, d=128, bs=16, nb=16, dtype="bf16", lengths=[9, 20],
                           write_new_token=True), seed=6)
     shape = tuple(x.k_pool.shape)
-    kd = torch.full(shape, 7, dtype=torch.int8, device="cuda")
-    vd = torch.full(shape, 7, dtype=torch.int8, device="cuda")
+    kw = np.full(shape, 7, CODE_DTYPE[fmt])
+    vw = np.full(shape, 7, CODE_DTYPE[fmt])
+    kd, vd = torch.from_numpy(kw.copy()).cuda(), torch.from_numpy(vw.copy()).cuda()
     ks = torch.tensor([0.0, 0.02], dtype=torch.float32, device="cuda")
     vs = torch.tensor([0.01, 0.02], dtype=torch.float32, device="cuda")
     err = new_err()
-    pa.pa_reshape_and_cache_int8(x.k_new.cuda(), x.v_new.cuda(), kd, vd, x.slot_mapping.cuda(),
-                                 ks, vs, d_error=err)
+    GPU_WRITE[fmt](x.k_new.cuda(), x.v_new.cuda(), kd, vd, x.slot_mapping.cuda(), ks, vs,
+                   d_error=err)
     torch.cuda.synchronize()
     assert int(err.item()) & pa.DEVERR_SCALE
-    kw = np.full(shape, 7, np.int8)
-    vw = np.full(shape, 7, np.int8)
-    st = oracle.write_int8(kw, vw, x.k_new, x.v_new, x.slot_mapping.numpy(), 16,
+    st = ORACLE_WRITE[fmt](kw, vw, x.k_new, x.v_new, x.slot_mapping.numpy(), 16,
                            ks.cpu().numpy(), vs.cpu().numpy())
     assert st == oracle.ERR_SCALE
     assert np.array_equal(kd.cpu().numpy(), kw) and np.array_equal(vd.cpu().numpy(), vw)
 
 
-def test_decode_write_int8_step():
-    """pa_decode_write_int8 = the oracle's INT8 write of the step's new tokens,
-    then its INT8 decode over the updated pools (llama7b-decode, full size)."""
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_decode_write_step(fmt):
+    """The one-call step = the oracle's write of the step's new tokens, then
+    its decode over the updated pools (llama7b-decode, full size)."""
     require_gpu()
     x = W.make_inputs("llama7b-decode")
-    kc, vc, ks, vs = int8_pools(x)  # the codes after this step's write
+    kc, vc, ks, vs = pools8(x, fmt)  # the codes after this step's write
     hkv, d = x.num_kv_heads, x.head_dim
     slots = x.slot_mapping.numpy()
     k0, v0 = kc.copy(), vc.copy()
     k0.reshape(-1, hkv, d)[slots] = 0  # before the write
     v0.reshape(-1, hkv, d)[slots] = 0
     kw, vw = k0.copy(), v0.copy()
-    assert oracle.write_int8(kw, vw, x.k_new, x.v_new, slots, x.block_size, ks.numpy(),
+    assert ORACLE_WRITE[fmt](kw, vw, x.k_new, x.v_new, slots, x.block_size, ks.numpy(),
                              vs.numpy()) == oracle.OK
     assert np.array_equal(kw, kc) and np.array_equal(vw, vc)
 
     kd, vd, err = torch.from_numpy(k0).cuda(), torch.from_numpy(v0).cuda(), new_err()
     q = x.q.cuda()
     out = torch.full_like(q, float("nan"))
-    pa.pa_decode_write_int8(out, q, x.k_new.cuda(), x.v_new.cuda(), kd, vd,
-                            x.slot_mapping.cuda(), x.block_table.cuda(), x.context_lens.cuda(),
-                            ks.cuda(), vs.cuda(), scale=x.scale,
-                            max_context_len=x.max_context_len, d_error=err)
+    GPU_STEP[fmt](out, q, x.k_new.cuda(), x.v_new.cuda(), kd, vd, x.slot_mapping.cuda(),
+                  x.block_table.cuda(), x.context_lens.cuda(), ks.cuda(), vs.cuda(),
+                  scale=x.scale, max_context_len=x.max_context_len, d_error=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert np.array_equal(kd.cpu().numpy(), kc) and np.array_equal(vd.cpu().numpy(), vc)
-    assert_close(out, oracle_decode_int8(x, kc, vc, ks, vs), x.dtype, what="INT8 step")
+    assert_close(out, oracle_decode8(fmt, x, kc, vc, ks, vs), x.dtype, what=f"{fmt} step")
+
+
+def test_fp8_pool_as_float8_tensor():
+    """FP8 pools may be float8_e4m3fn tensors (the same bytes as uint8)."""
+    require_gpu()
+    x = W.make_inputs(cfg(hq=8, hkv=2, d=128, bs=16, nb=32, dtype="bf16", lengths=[50, 7]),
+                      seed=9)
+    kc, vc, ks, vs = pools8(x, "fp8")
+    q = x.q.cuda()
+    out = torch.empty_like(q)
+    kf = torch.from_numpy(kc).cuda().view(torch.float8_e4m3fn)
+    vf = torch.from_numpy(vc).cuda().view(torch.float8_e4m3fn)
+    pa.pa_decode_fp8(out, q, kf, vf, x.block_table.cuda(), x.context_lens.cuda(), ks.cuda(),
+                     vs.cuda(), scale=x.scale, max_context_len=x.max_context_len)
+    torch.cuda.synchronize()
+    assert_close(out, oracle_decode8("fp8", x, kc, vc, ks, vs), x.dtype, what="float8 pools")
