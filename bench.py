@@ -674,7 +674,8 @@ def main():
                     "partition_size": parti, "partitions": npi,
                     "roofline": {"bound": "hbm", "achieved": round(gb8, 1), "peak": hbm_peak,
                                  "unit": "GB/s", "frac": round(gb8 / hbm_peak, 4),
-                                 "traffic": None}}
+                                 "traffic": recorded_traffic(f"pa_decode_{fmt}", HEADLINE,
+                                                             dec_hash)}}
                 del xi
             moved, t_cp = bench_copy_blocks(pa, max(20, args.steps // 4), args.warmup,
                                             flush_buf, stream)
@@ -687,7 +688,9 @@ def main():
                             "copied in both pools",
                 "roofline": {"bound": "hbm", "achieved": round(gb_cp, 1), "peak": hbm_peak,
                              "unit": "GB/s", "frac": round(gb_cp / hbm_peak, 4),
-                             "traffic": None}}
+                             "traffic": recorded_traffic(
+                                 "pa_copy_blocks", "copy-blocks",
+                                 source_hash("copy_blocks.cu", "pa_device.cuh"))}}
             line["secondary"] = sec
 
         # ---- the oracle on the host cores -------------------------------
