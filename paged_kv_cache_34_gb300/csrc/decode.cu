@@ -308,7 +308,7 @@ __device__ __forceinline__ void lds128(uint32_t addr, uint32_t (&w)[4]) {
 
 // KVF: the pool format -- 0 fp16/bf16 (as E), 1 INT8 codes, 2 FP8 (E4M3) codes.
 template <class E, int D, int BOXR, bool BAL, int KVF>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm)
     decode_persistent_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                              const __grid_constant__ CUtensorMap tmv) {
   constexpr bool KV8 = KVF != 0;  // 8-bit codes, widened to fp16
@@ -494,8 +494,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       const unsigned live = __ballot_sync(0xffffffffu, feeder && act);
       const unsigned badmask = __ballot_sync(0xffffffffu, bad);
       int nbox = nb;
-      nbox += __shfl_xor_sync(0xffffffffu, nbox, 1);
-      nbox += __shfl_xor_sync(0xffffffffu, nbox, 2);  // lanes 0-3 hold all feeders
+#pragma unroll
+      for (int o = 1; o < kWorkers; o <<= 1)  // lane 0 sums the feeder lanes 0..kWorkers-1
+        nbox += __shfl_xor_sync(0xffffffffu, nbox, o);
       bool ok = true;
       if (lane == 0 && c >= NS)
         ok = mbar_wait_bounded(smem_u32(empty + s), ((c / NS) - 1) & 1);

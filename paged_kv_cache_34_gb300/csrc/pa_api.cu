@@ -105,8 +105,8 @@ bool use_balanced(int num_seqs, int num_kv_heads, int max_ctx, int partition_siz
   return t < (1LL << 30);
 }
 
-// Fixed split-KV plan.  Auto: every worker warp (four per CTA, two CTAs per SM)
-// should get about eight items of the largest possible batch, so the static
+// Fixed split-KV plan.  Auto: every worker warp (kDecodeWarps per CTA,
+// kDecodeCtasPerSm CTAs per SM) should get about eight items of the largest possible batch, so the static
 // item schedule balances; a partition is at least 64 tokens (128 when eight
 // query heads share a KV head) so the partial states stay a few percent of the
 // K/V bytes.
@@ -114,7 +114,8 @@ int plan_partition(int num_seqs, int num_q_heads, int num_kv_heads, int max_ctx,
                    int partition_size, int num_sms) {
   if (partition_size > 0) return partition_size;
   const long units = static_cast<long>(num_seqs > 0 ? num_seqs : 1) * num_kv_heads;
-  const long target_items = static_cast<long>(num_sms) * 2 * pa::kDecodeWarps * 8;
+  const long target_items =
+      static_cast<long>(num_sms) * pa::kDecodeCtasPerSm * pa::kDecodeWarps * 8;
   long P = (units * max_ctx + target_items - 1) / target_items;
   P = ((P + pa::kDecodeSub - 1) / pa::kDecodeSub) * pa::kDecodeSub;
   const long pmin = (num_q_heads / num_kv_heads) > 4 ? 128 : 64;
@@ -411,10 +412,12 @@ pa_status decode_call(void *out, int64_t out_row_stride, const void *query, int6
     w += align256(rows * 2 * sizeof(float));
     a.ws_pref = reinterpret_cast<int32_t *>(w);
   } else {
-    // Items are at most S * Hkv * partitions; two CTAs per SM, four workers each.
+    // Items are at most S * Hkv * partitions; kDecodeCtasPerSm CTAs per SM,
+    // kDecodeWarps workers each.
     const int64_t items = static_cast<int64_t>(num_seqs) * num_kv_heads * nparts;
     int64_t grid = (items + pa::kDecodeWarps - 1) / pa::kDecodeWarps;
-    if (grid > 2LL * a.num_sms) grid = 2LL * a.num_sms;
+    if (grid > static_cast<int64_t>(pa::kDecodeCtasPerSm) * a.num_sms)
+      grid = static_cast<int64_t>(pa::kDecodeCtasPerSm) * a.num_sms;
     if (grid < 1) grid = 1;
     a.grid = static_cast<int>(grid);
     a.merge = nparts > 1;

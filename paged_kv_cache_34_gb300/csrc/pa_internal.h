@@ -47,6 +47,7 @@ cudaError_t launch_copy_blocks(const CopyBlocksArgs &a, cudaStream_t stream);
 
 // Decode tiling shared by the planner and the kernels.
 constexpr int kDecodeWarps = 4;     // consumer warps (independent workers) per CTA
+constexpr int kDecodeCtasPerSm = 2;  // resident decode CTAs per SM
 constexpr int kDecodeSub = 16;      // tokens per worker per pipeline stage
 constexpr int kDecodeMaxGroup = 8;  // query heads per KV head
 constexpr int kDecodeChunkCap = 2048;  // balanced schedule: most tokens per chunk
@@ -62,7 +63,8 @@ inline DecodeBalance decode_balance(int num_seqs, int num_kv_heads, int max_ctx,
   DecodeBalance d;
   const int64_t t_max = static_cast<int64_t>(num_seqs) * num_kv_heads * ((max_ctx + 15) / 16) * 16;
   int64_t grid = (t_max / kDecodeSub + kDecodeWarps - 1) / kDecodeWarps;
-  if (grid > 2LL * num_sms) grid = 2LL * num_sms;
+  if (grid > static_cast<int64_t>(kDecodeCtasPerSm) * num_sms)
+    grid = static_cast<int64_t>(kDecodeCtasPerSm) * num_sms;
   if (grid < 1) grid = 1;
   d.grid = static_cast<int>(grid);
   d.workers = d.grid * kDecodeWarps;
