@@ -211,30 +211,6 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   return d;
 }
 
-// 2^x for a pair, on the FMA pipe (offloads the special-function unit).
-// Range reduction x = j + f with j = round(x) (the 1.5*2^23 shift puts j in
-// the low bits of t) and f in [-1/2, 1/2]; 2^f by a cubic whose coefficients
-// are a minimax fit of the relative error on that interval (max 7.5e-5);
-// 2^j by adding j to the exponent field (bits(t) << 23 == j << 23 mod 2^32).
-// Inputs below -126 are clamped there, so the result never leaves the
-// normal range; callers needing an exact 0 select it themselves.
-__device__ __forceinline__ uint64_t f2_exp2_poly(float x0, float x1) {
-  constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
-  const uint64_t x = f2_pack(fmaxf(x0, -126.f), fmaxf(x1, -126.f));
-  const uint64_t t = f2_add(x, f2_pack(kShift, kShift));
-  const uint64_t j = f2_add(t, f2_pack(-kShift, -kShift));
-  const uint64_t f = f2_fma(j, f2_pack(-1.f, -1.f), x);
-  uint64_t p = f2_fma(f2_pack(0.0551716685f, 0.0551716685f), f,
-                      f2_pack(0.2426111251f, 0.2426111251f));
-  p = f2_fma(p, f, f2_pack(0.6932609677f, 0.6932609677f));
-  p = f2_fma(p, f, f2_pack(0.9999280572f, 0.9999280572f));
-  float p0, p1, t0, t1;
-  f2_unpack(p, p0, p1);
-  f2_unpack(t, t0, t1);
-  return f2_pack(__int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23)),
-                 __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23)));
-}
-
 // ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor) loads into shared memory
 // ---------------------------------------------------------------------------
