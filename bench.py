@@ -446,20 +446,35 @@ def dist_setup(gpus):
     return None, 0, 1
 
 
-def reduce_max(dist, v: float) -> float:
+def _reduce(dist, v: float, op) -> float:
+    """All-reduce one number over the ranks (a CPU tensor under gloo)."""
     if dist is None:
         return v
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=op)
     return float(t.item())
+
+
+def reduce_max(dist, v: float) -> float:
+    return v if dist is None else _reduce(dist, v, dist.ReduceOp.MAX)
 
 
 def reduce_sum(dist, v: float) -> float:
-    if dist is None:
-        return v
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+    return v if dist is None else _reduce(dist, v, dist.ReduceOp.SUM)
+
+
+def rank_seed(W, rank: int) -> int:
+    """Each rank draws its own batch of the headline workload (weak scaling:
+    the work per GPU is fixed, the job grows with the ranks)."""
+    return W.default_seed(HEADLINE) + 7919 * rank
+
+
+def whole_job_gbs(dist, bytes_this_rank: int, ms_this_rank: float) -> tuple[float, float]:
+    """(GB/s of the whole job, slowest rank's ms): every rank's bytes over the
+    slowest rank's time."""
+    ms_max = reduce_max(dist, ms_this_rank)
+    return reduce_sum(dist, bytes_this_rank) / (ms_max * 1e-3) / 1e9, ms_max
 
 
 def run_reference(args):
@@ -563,7 +578,7 @@ def main():
         return
 
     # ---- headline: write + decode on the llama7b-decode workload ----------
-    seed = W.default_seed(HEADLINE) + 7919 * rank  # each rank its own batch
+    seed = rank_seed(W, rank)  # each rank its own batch
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -576,10 +591,8 @@ def main():
     if dist is not None:
         dist.barrier()
     ms_step = statistics.fmean(t_step)
-    ms_step_max = reduce_max(dist, ms_step)
     kv = kv_read_bytes(x)
-    total_kv = reduce_sum(dist, kv)  # every rank's own batch
-    value = total_kv / (ms_step_max * 1e-3) / 1e9
+    value, ms_step_max = whole_job_gbs(dist, kv, ms_step)  # every rank's own batch
     merge = nparts is None or nparts > 1  # the merge kernel runs
     launches_per_step = (1 if x.slot_mapping.numel() else 0) + 1 + (1 if merge else 0)
 
