@@ -258,3 +258,37 @@ def test_fp8_pool_as_float8_tensor():
                      vs.cuda(), scale=x.scale, max_context_len=x.max_context_len)
     torch.cuda.synchronize()
     assert_close(out, oracle_decode8("fp8", x, kc, vc, ks, vs), x.dtype, what="float8 pools")
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("partition_size", [0, 64])
+def test_device_errors_are_flagged(fmt, partition_size):
+    """A bad block id, then a context past the block table: flagged in
+    d_error, never a fault; the other sequences still match the oracle."""
+    require_gpu()
+    x = W.make_inputs(cfg(hq=8, hkv=2, d=128, bs=16, nb=64, dtype="bf16",
+                          lengths=[40, 100, 30, 70]), seed=43)
+    kc, vc, ks, vs = pools8(x, fmt)
+    want = oracle_decode8(fmt, x, kc, vc, ks, vs)
+    bt = x.block_table.clone()
+    bt[1, 2] = 10_000
+    cases = [(bt, x.context_lens, pa.DEVERR_BLOCK_ID, 1)]
+    cl = x.context_lens.clone()
+    cl[2] = x.block_table.shape[1] * x.block_size + 1  # past the block table's capacity
+    cases.append((x.block_table, cl, pa.DEVERR_CONTEXT, 2))
+    for bt_c, cl_c, bit, bad in cases:
+        q = x.q.cuda()
+        out = torch.full_like(q, float("nan"))
+        err = new_err()
+        GPU_DECODE[fmt](out, q, torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda(),
+                        bt_c.cuda(), cl_c.cuda(), ks.cuda(), vs.cuda(), scale=x.scale,
+                        max_context_len=int(cl_c.max()), partition_size=partition_size,
+                        d_error=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) & bit
+        g = out.double().cpu().numpy()
+        rows = [r for r in range(4) if r != bad]  # every other sequence is intact
+        assert np.isfinite(g[rows]).all()
+        assert np.abs(g[rows] - want[rows]).max() <= 1e-2
+        if bit == pa.DEVERR_CONTEXT:
+            assert (g[bad] == 0).all()
