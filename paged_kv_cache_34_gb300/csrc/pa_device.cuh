@@ -28,8 +28,6 @@ struct F16 {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
   }
-  // Sum of the two values packed in `w` (as the tensor core will see them).
-  static __device__ __forceinline__ float sum2(uint32_t w) { return lo(w) + hi(w); }
   // a += low half of w, b += high half, each widened exactly (mixed-precision
   // add.f32.f16: no separate unpacking instructions).
   static __device__ __forceinline__ void add_halves(uint32_t w, float &a, float &b) {
@@ -54,8 +52,6 @@ struct BF16 {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
   }
-  // Sum of the two values packed in `w` (as the tensor core will see them).
-  static __device__ __forceinline__ float sum2(uint32_t w) { return lo(w) + hi(w); }
   static __device__ __forceinline__ void add_halves(uint32_t w, float &a, float &b) {
     asm("{\n\t.reg .b16 l16, h16;\n\tmov.b32 {l16, h16}, %2;\n\t"
         "add.rn.f32.bf16 %0, l16, %0;\n\tadd.rn.f32.bf16 %1, h16, %1;\n\t}"
@@ -182,13 +178,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// max(a, b, c) in one instruction (three-input max.f32 of sm_100-family).
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
 // ---------------------------------------------------------------------------
 // Packed fp32 pairs (sm_100-family f32x2 arithmetic)
 // ---------------------------------------------------------------------------
@@ -203,11 +192,6 @@ __device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
 __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 
@@ -282,11 +266,6 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
   }
-}
-
-// Named barrier among `count` threads (a multiple of 32).
-__device__ __forceinline__ void named_barrier_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---------------------------------------------------------------------------
