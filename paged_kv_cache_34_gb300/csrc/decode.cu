@@ -144,18 +144,12 @@ __device__ __forceinline__ Item decode_item(int i, const int *pref, const int *l
   m.L = len[lo];
   const int np = m.L > 0 ? (m.L + P - 1) / P : 1;
   const int rem = i - pref[lo];
-#if PA_DECODE_PART_MAJOR
-  m.part = rem / hkv;
-  m.g = rem - m.part * hkv;
-#else
-  m.g = rem / np;
+  m.g = rem / np;  // numbered by KV head, then partition
   m.part = rem - m.g * np;
-#endif
   m.start = m.part * P;
   m.end = min(m.start + P, m.L);
   if (m.end < m.start) m.end = m.start;
   (void)hkv;
-  (void)np;
   return m;
 }
 

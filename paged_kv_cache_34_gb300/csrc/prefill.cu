@@ -60,20 +60,11 @@ constexpr int kEpiWarp0 = 8, kTmaWarp = 12, kMmaWarp = 13;
 // softmax holds a whole S row per thread, the epilogue a packed O row, the
 // producers little.  The split must fit in what the CTA is launched with
 // (checked on the host before the first launch).
-#ifndef PA_SOFTMAX_REGS
-#define PA_SOFTMAX_REGS 152
-#define PA_EPILOGUE_REGS 104
-#define PA_PRODUCER_REGS 104
-#endif
-constexpr int kSoftmaxRegs = PA_SOFTMAX_REGS, kEpilogueRegs = PA_EPILOGUE_REGS,
-              kProducerRegs = PA_PRODUCER_REGS;
+constexpr int kSoftmaxRegs = 152, kEpilogueRegs = 104, kProducerRegs = 104;
 constexpr int kRegPoolNeeded = 128 * (2 * kSoftmaxRegs + kEpilogueRegs + kProducerRegs);
 constexpr int kHalf = 128 * 128;    // 128 rows x 64 elements x 2 B
 constexpr int kTile = 2 * kHalf;    // 128 x 128 tile, two 64-wide halves
-#ifndef PA_PREFILL_K_BUFS
-#define PA_PREFILL_K_BUFS 2
-#endif
-constexpr int kKBufs = PA_PREFILL_K_BUFS;  // separate K and V rings (5 buffers)
+constexpr int kKBufs = 2;  // separate K and V rings (5 buffers)
 constexpr int kVBufs = 5 - kKBufs;
 constexpr int kKVBufs = kKBufs + kVBufs;
 constexpr int kQOff = 0;                           // Q_A, Q_B
