@@ -292,3 +292,51 @@ def test_device_errors_are_flagged(fmt, partition_size):
         assert np.abs(g[rows] - want[rows]).max() <= 1e-2
         if bit == pa.DEVERR_CONTEXT:
             assert (g[bad] == 0).all()
+
+
+def _decode_codes(fmt, x, kc, vc, ks, vs, bt, cl, partition_size=0):
+    q = x.q.cuda()
+    out = torch.empty_like(q)
+    GPU_DECODE[fmt](out, q, torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda(),
+                    bt.cuda(), cl.cuda(), ks.cuda(), vs.cuda(), scale=x.scale,
+                    max_context_len=int(cl.max()), partition_size=partition_size)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_block_permutation_invariance_bitwise(fmt):
+    """Moving the physical blocks (and the block table with them) changes
+    nothing in the output, bit for bit."""
+    require_gpu()
+    x = W.make_inputs(cfg(hq=8, hkv=2, d=128, bs=16, nb=64, dtype="bf16",
+                          lengths=[40, 100, 30, 70]), seed=51)
+    kc, vc, ks, vs = pools8(x, fmt)
+    perm = np.random.default_rng(5).permutation(kc.shape[0])
+    kp, vp = np.empty_like(kc), np.empty_like(vc)
+    kp[perm], vp[perm] = kc, vc
+    bt = x.block_table.clone()
+    ok = bt >= 0
+    bt[ok] = torch.from_numpy(perm).to(torch.int32)[bt[ok].long()]
+    a = _decode_codes(fmt, x, kc, vc, ks, vs, x.block_table, x.context_lens)
+    b = _decode_codes(fmt, x, kp, vp, ks, vs, bt, x.context_lens)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_shared_blocks_equal_private_copies(fmt):
+    """Two sequences whose tables name the same physical blocks (a shared
+    prefix) decode like two sequences with private copies of those blocks."""
+    require_gpu()
+    x = W.make_inputs(cfg(hq=8, hkv=2, d=128, bs=16, nb=64, dtype="bf16",
+                          lengths=[64, 64]), seed=52)
+    kc, vc, ks, vs = pools8(x, fmt)
+    shared = x.block_table.clone()
+    shared[1] = shared[0]  # sequence 1 reads sequence 0's blocks
+    kq, vq = kc.copy(), vc.copy()
+    for j in range(4):  # private copies: sequence 0's blocks copied into sequence 1's
+        kq[int(x.block_table[1, j])] = kc[int(x.block_table[0, j])]
+        vq[int(x.block_table[1, j])] = vc[int(x.block_table[0, j])]
+    a = _decode_codes(fmt, x, kc, vc, ks, vs, shared, x.context_lens)
+    b = _decode_codes(fmt, x, kq, vq, ks, vs, x.block_table, x.context_lens)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
