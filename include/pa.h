@@ -40,7 +40,9 @@
  *    default stream) and the call returns before it runs.
  *  - Strides are in ELEMENTS.  Element type is fp16 or bf16 (`dtype`); every
  *    K/V/Q/out pointer must be 16-byte aligned and every row stride a
- *    multiple of 8 elements.
+ *    multiple of 8 elements.  The 8-bit (INT8 / FP8) calls keep fp16/bf16
+ *    queries, outputs and new K/V rows; only their pools hold one-byte codes.
+ *    pa_copy_blocks copies bytes and takes no element type.
  *  - Cache layout ([SKILL] §3.1): key_cache and value_cache are separate,
  *    contiguous [num_blocks, block_size, num_kv_heads, head_dim] pools.  A
  *    physical slot s addresses row s of the pool viewed as
@@ -90,11 +92,12 @@ typedef enum pa_dtype { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
 
 /* Bits OR-ed into *d_error by the kernels. */
 #define PA_DEVERR_SLOT 1       /* slot_mapping entry >= num_blocks*block_size */
-#define PA_DEVERR_BLOCK_ID 2   /* block_table entry outside [0, num_blocks)   */
+#define PA_DEVERR_BLOCK_ID 2   /* block_table / block_mapping entry outside
+                                  [0, num_blocks)                            */
 #define PA_DEVERR_CU_SEQLENS 4 /* cu_seqlens not a prefix sum of the batch    */
 #define PA_DEVERR_CONTEXT 8    /* context_len < 0, > capacity or > host hint  */
 #define PA_DEVERR_TIMEOUT 16   /* a bounded pipeline wait gave up             */
-#define PA_DEVERR_SCALE 32     /* an INT8 scale not a positive finite number  */
+#define PA_DEVERR_SCALE 32     /* an 8-bit pool's scale not positive finite   */
 
 /* ABI version the library was built with (PA_ABI_VERSION). */
 int32_t pa_abi_version(void);
