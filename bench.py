@@ -516,11 +516,12 @@ def run_reference(args):
 
 def run_only(pa, W, args, flush_buf, stream):
     """One kernel's workload alone, without the e2e, secondary and CPU legs."""
-    if args.only == "decode":
-        x, _, _, part, nparts, _, t = bench_decode(pa, W, HEADLINE, args.steps, args.warmup,
+    if args.only in ("decode", "long-context"):
+        name = HEADLINE if args.only == "decode" else "long-context-decode"
+        x, _, _, part, nparts, _, t = bench_decode(pa, W, name, args.steps, args.warmup,
                                                    flush_buf, stream)
         ms = statistics.fmean(t)
-        print(json.dumps({"only": "decode", "workload": HEADLINE, "ms": round(ms, 5),
+        print(json.dumps({"only": args.only, "workload": name, "ms": round(ms, 5),
                           "GBps": round(decode_bytes(x) / (ms * 1e-3) / 1e9, 1),
                           "partition_size": part, "partitions": nparts}))
     elif args.only in ("decode-int8", "decode-fp8"):
@@ -556,7 +557,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--only",
-                    choices=["decode", "decode-int8", "decode-fp8", "copy-blocks", "prefill"],
+                    choices=["decode", "long-context", "decode-int8", "decode-fp8", "copy-blocks",
+                             "prefill"],
                     help="time one kernel's workload alone (a small profiling target)")
     args = ap.parse_args()
     if args.impl == "reference":
