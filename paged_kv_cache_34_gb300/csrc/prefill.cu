@@ -18,16 +18,16 @@
 //    HBM once and is then reused from L2) and runs the heaviest items of a
 //    sequence first (so the last items claimed, which set the finish time,
 //    are light).
-//  * Warp 8 (TMA): loads Q_A and Q_B once, then streams K and V tiles (128
+//  * Warp 12 (TMA): loads Q_A and Q_B once, then streams K and V tiles (128
 //    tokens each) through separate K (2 buffers) and V (3 buffers) rings,
 //    K running one tile ahead of V; a K/V
 //    tile is gathered block by block through block_table, one TMA box per
 //    block issued by its own lane, with the 128-byte swizzle the MMA
 //    descriptors expect.  The next tile's block ids are loaded while the
 //    current tile is issued.
-//  * Warp 9 (one thread): tcgen05.mma kind::f16, M = 128, N = 128, K = 16 x 8:
-//    S_t = Q_t K^T into TMEM and O_t += P_t V (V read MN-major straight from
-//    its TMA tile, P from TMEM).  The issue order S_A S_B | PV_A S_A' | PV_B
+//  * Warp 13 (MMA; one elected lane issues): tcgen05.mma kind::f16, M = 128,
+//    N = 128, K = 16 x 8: S_t = Q_t K^T into TMEM and O_t += P_t V (V read
+//    MN-major straight from its TMA tile, P from TMEM).  The issue order S_A S_B | PV_A S_A' | PV_B
 //    S_B' | ... keeps the tensor core busy with one tile while the other
 //    tile's softmax runs (ping-pong); the tensor core executes one thread's
 //    MMAs in order, so S_t' may overwrite the columns P_t was read from.
