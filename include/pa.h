@@ -228,7 +228,7 @@ pa_status pa_decode(void *out, int64_t out_row_stride, const void *query,
  * Device checks: a cu_seqlens_q that is not a non-decreasing prefix sum
  * ending at total_q, or a q_b above max_seqlen_q, sets
  * PA_DEVERR_CU_SEQLENS and the offending sequences are skipped.
- * Supported: head_dim 128; num_q_heads % num_kv_heads == 0; block_size 16,
+ * Supported: head_dim 64 or 128; num_q_heads % num_kv_heads == 0; block_size 16,
  * 32, 64 or 128.
  * Work is handed out to the CTAs through one of 256 counters kept in the
  * library's device memory, taken round robin per call; it needs no

@@ -617,7 +617,7 @@ pa_status pa_prefill_varlen(void *out, int64_t out_row_stride, const void *query
   if (block_table_stride < max_blocks_per_seq) return PA_ERR_SHAPE;
   if (!isfinite(scale)) return PA_ERR_SHAPE;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
-  if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (!(block_size == 16 || block_size == 32 || block_size == 64 || block_size == 128))
     return PA_ERR_UNSUPPORTED;
   if (num_blocks * block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;

@@ -261,7 +261,9 @@ __device__ PairItem item_at(const PrefillParams &p, int x, int lane, bool report
   return it;
 }
 
-template <class E>
+// D (head_dim) is 64 or 128: a Q, K or V tile row is D / 64 128-byte
+// halves; the shared-memory layout is the D = 128 one either way.
+template <class E, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq,
                    const __grid_constant__ CUtensorMap tmk,
@@ -274,6 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *misc = reinterpret_cast<volatile int *>(smem + kMiscOff);
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  constexpr int kHalves = D / 64;  // 128-byte halves per tile row
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   griddep_wait();  // inputs (e.g. this step's cache write) come from earlier kernels
   griddep_launch_dependents();
@@ -377,11 +381,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           const uint32_t qs = smem_u32(smem + kQOff);
           const int qtiles = it.nkv > 0 ? (it.has_b ? 2 : 1) : 0;
-          mbar_arrive_expect_tx(bar(kQFull), qtiles * kTile);
+          mbar_arrive_expect_tx(bar(kQFull), qtiles * kHalves * kHalf);
           for (int t = 0; t < qtiles; ++t) {
             tma_load_3d(qs + t * kTile, &tmq, bar(kQFull), 0, it.h, it.q_start + it.row0[t]);
-            tma_load_3d(qs + t * kTile + kHalf, &tmq, bar(kQFull), 64, it.h,
-                        it.q_start + it.row0[t]);
+            if (kHalves == 2)
+              tma_load_3d(qs + t * kTile + kHalf, &tmq, bar(kQFull), 64, it.h,
+                          it.q_start + it.row0[t]);
           }
         }
         ++nq;
@@ -415,13 +420,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (lane == 0)
               mbar_arrive_expect_tx(bar(kKVFull + slot),
-                                    static_cast<uint32_t>(__popc(vmask)) * bs * 128 * 2);
+                                    static_cast<uint32_t>(__popc(vmask)) * bs * D * 2);
             __syncwarp();
             if (valid) {
               const uint32_t dst = smem_u32(smem + kKVOff + slot * kTile) + lane * bs * 128;
               const CUtensorMap *map = which == 0 ? &tmk : &tmv;
               tma_load_3d(dst, map, bar(kKVFull + slot), 0, g, id * bs);
-              tma_load_3d(dst + kHalf, map, bar(kKVFull + slot), 64, g, id * bs);
+              if (kHalves == 2) tma_load_3d(dst + kHalf, map, bar(kKVFull + slot), 64, g, id * bs);
             }
             if (which == 0) ++nk;
             else ++nv;
@@ -443,8 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok) {
             uint8_t *vt = smem + kKVOff + v_slot(vn) * kTile;
             const int first = it.L - (it.nkv - 1) * 128;  // 1..127
-            for (int i = lane; i < (128 - first) * 16; i += 32) {
-              const int row = first + i / 16, c16 = i % 16;
+            for (int i = lane; i < (128 - first) * (D / 8); i += 32) {
+              const int row = first + i / (D / 8), c16 = i % (D / 8);
               *reinterpret_cast<uint4 *>(vt + (c16 >> 3) * kHalf + row * 128 + (c16 & 7) * 16) =
                   make_uint4(0, 0, 0, 0);
             }
@@ -475,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // by one elected lane (the same one every time: the warp is converged).
       constexpr bool kBF = E::kBF16;
       const uint32_t id_qk = idesc_f16(kBF, 128, 128, false);
-      const uint32_t id_pv = idesc_f16(kBF, 128, 128, true);
+      const uint32_t id_pv = idesc_f16(kBF, 128, D, true);
       const uint64_t q_desc[2] = {sdesc_sw128(smem_u32(smem + kQOff), 16, 1024),
                                   sdesc_sw128(smem_u32(smem + kQOff + kTile), 16, 1024)};
       int kbase = 0;            // ring position of this item's first K/V tile
@@ -495,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // K step k: 16 columns = 32 bytes into a 128-byte swizzled row,
           // the second 64 columns in the tile's second half
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
+          for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = ((k >> 2) * kHalf + (k & 3) * 32) >> 4;
             umma_f16_ss(tbase + t * 128, qd + off, kd + off, id_qk, k > 0 ? 1u : 0u);
           }
@@ -650,10 +655,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float l = l_buf[t * 128 + r];
         const float inv_l = (nkv_t > 0 && l > 0.f) ? 1.f / l : 0.f;
         const bool rows = it.row0[t] < it.q_len;
-        uint32_t w[64];  // the row of O / l, packed to the output type
+        uint32_t w[D / 2];  // the row of O / l, packed to the output type
         if (nkv_t > 0 && rows) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
             tmem_ld32(tbase + lane_addr + 256 + t * 128 + c * 32, o);
             tmem_wait_ld();
@@ -664,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 64; ++i) w[i] = 0u;
+          for (int i = 0; i < D / 2; ++i) w[i] = 0u;
         }
         tc_fence_before();
         __syncwarp();
@@ -672,9 +677,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t grow = static_cast<int64_t>(it.q_start) + it.row0[t] + r;
         if (rows && it.row0[t] + r < it.q_len && grow >= 0 && grow < p.total_q) {
           typename E::T *orow =
-              static_cast<typename E::T *>(p.out) + grow * p.out_row_stride + it.h * 128;
+              static_cast<typename E::T *>(p.out) + grow * p.out_row_stride + it.h * D;
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
+          for (int c = 0; c < D / 8; ++c)
             *reinterpret_cast<uint4 *>(orow + c * 8) =
                 make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
         }
@@ -767,7 +772,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // O holds exactly the sum through PV(kt-1): S(kt) being complete
           // means QK(kt) ran, and it was issued after PV(kt-1).  Rescale it.
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
             tmem_ld32(o_tm + c * 32, o);
             tmem_wait_ld();
@@ -832,6 +837,16 @@ cudaError_t check_register_pool() {
   return status;
 }
 
+template <auto Kernel>
+cudaError_t launch_variant(const PrefillParams &p, const PrefillArgs &a, int64_t grid,
+                           cudaStream_t stream) {
+  cudaError_t e = allow_dynamic_smem<Kernel>();
+  if (e == cudaSuccess) e = check_register_pool<Kernel>();
+  if (e != cudaSuccess) return e;
+  return launch_pdl(Kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, stream,
+                    p, a.tm_q, a.tm_k, a.tm_v);
+}
+
 // Launches so far in this process; picks each launch's schedule slot.
 std::atomic<uint32_t> g_prefill_launches{0};
 
@@ -866,21 +881,11 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
   p.num_items = static_cast<int32_t>(items);
   p.sched_slot = static_cast<int32_t>(g_prefill_launches.fetch_add(1) % kSchedSlots);
   const int64_t grid = items < a.num_sms ? items : a.num_sms;
-  cudaError_t e;
-  if (a.dtype == PA_BF16) {
-    e = allow_dynamic_smem<prefill_kernel<BF16>>();
-    if (e == cudaSuccess) e = check_register_pool<prefill_kernel<BF16>>();
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(prefill_kernel<BF16>, dim3(static_cast<unsigned>(grid)), dim3(kThreads),
-                   kSmemBytes, stream, p, a.tm_q, a.tm_k, a.tm_v);
-  } else {
-    e = allow_dynamic_smem<prefill_kernel<F16>>();
-    if (e == cudaSuccess) e = check_register_pool<prefill_kernel<F16>>();
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(prefill_kernel<F16>, dim3(static_cast<unsigned>(grid)), dim3(kThreads),
-                   kSmemBytes, stream, p, a.tm_q, a.tm_k, a.tm_v);
-  }
-  return e;
+  if (a.dtype == PA_BF16)
+    return a.head_dim == 64 ? launch_variant<prefill_kernel<BF16, 64>>(p, a, grid, stream)
+                            : launch_variant<prefill_kernel<BF16, 128>>(p, a, grid, stream);
+  return a.head_dim == 64 ? launch_variant<prefill_kernel<F16, 64>>(p, a, grid, stream)
+                          : launch_variant<prefill_kernel<F16, 128>>(p, a, grid, stream);
 }
 
 }  // namespace pa

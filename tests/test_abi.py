@@ -94,7 +94,7 @@ def prefill_call(lib, **kw):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(d=64), 3), (dict(bs=8), 3), (dict(hkv=5), 2), (dict(cu=None), 1),
+    (dict(d=96), 3), (dict(bs=8), 3), (dict(hkv=5), 2), (dict(cu=None), 1),
     (dict(out=MISALIGNED), 4), (dict(t=-1), 2), (dict(nb=0), 2),
 ])
 def test_prefill_host_validation(lib, kw, status):

@@ -56,6 +56,26 @@ def test_varlen_grid(bs, hq, hkv, dtype):
     _run(W.make_inputs(c, seed=200 + bs + hq), what=f"bs{bs} g{hq // hkv} {dtype}")
 
 
+@pytest.mark.parametrize("bs", [16, 128])
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 2)])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_varlen_grid_head_dim_64(bs, hq, hkv, dtype):
+    # head_dim 64: one 128-byte half per tile row, PV with N = 64.
+    lengths = [1, 5, 127, 128, 129, 300, 64]
+    c = cfg(kind="prefill", hq=hq, hkv=hkv, d=64, bs=bs,
+            nb=sum(-(-n // bs) for n in lengths) + 3, dtype=dtype, lengths=lengths)
+    _run(W.make_inputs(c, seed=260 + bs + hq), what=f"d64 bs{bs} g{hq // hkv} {dtype}")
+
+
+def test_chunked_prefill_head_dim_64():
+    lengths = [300, 129, 517, 64]
+    qlens = [44, 129, 200, 1]
+    c = cfg(kind="prefill", hq=8, hkv=4, d=64, bs=32, nb=60, dtype="bf16",
+            lengths=lengths)
+    x = W.make_inputs(c, seed=61, q_lens=qlens, new_lens=qlens)
+    _run(x, what="chunked d64")
+
+
 @pytest.mark.parametrize("causal", [True, False])
 def test_chunked_prefill_queries_shorter_than_context(causal):
     # q < L: the cache already holds a prefix; the step writes the new chunk
@@ -68,10 +88,11 @@ def test_chunked_prefill_queries_shorter_than_context(causal):
     _run(x, what=f"chunked causal={causal}")
 
 
-def test_packed_equals_each_sequence_alone_bitwise():
+@pytest.mark.parametrize("d", [128, 64])
+def test_packed_equals_each_sequence_alone_bitwise(d):
     require_gpu()
     lengths = [200, 33, 450, 128]
-    x = W.make_inputs(cfg(kind="prefill", hq=4, hkv=4, d=128, bs=64, nb=40,
+    x = W.make_inputs(cfg(kind="prefill", hq=4, hkv=4, d=d, bs=64, nb=40,
                           lengths=lengths), seed=53).to("cuda")
     gpu_write(x)
     packed = gpu_prefill(x)
