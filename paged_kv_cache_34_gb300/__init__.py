@@ -294,7 +294,7 @@ def _decode8(fmt, out, query, key_cache, value_cache, block_table, context_lens,
 def pa_decode_int8(out, query, key_cache, value_cache, block_table, context_lens, k_scale,
                    v_scale, *, scale, max_context_len, partition_size=0, workspace=None,
                    d_error=None, stream=None, lib=None):
-    """pa_decode over INT8 pools (int8 [NB, bs, Hkv, D], head_dim 128) with
+    """pa_decode over INT8 pools (int8 [NB, bs, Hkv, D], head_dim 64 or 128) with
     per-KV-head float32 scales k_scale / v_scale [Hkv]."""
     return _decode8("int8", out, query, key_cache, value_cache, block_table, context_lens,
                     k_scale, v_scale, scale, max_context_len, partition_size, workspace,
@@ -305,7 +305,7 @@ def pa_decode_fp8(out, query, key_cache, value_cache, block_table, context_lens,
                   v_scale, *, scale, max_context_len, partition_size=0, workspace=None,
                   d_error=None, stream=None, lib=None):
     """pa_decode over FP8 pools (E4M3 codes, uint8 or float8_e4m3fn
-    [NB, bs, Hkv, D], head_dim 128) with per-KV-head float32 scales."""
+    [NB, bs, Hkv, D], head_dim 64 or 128) with per-KV-head float32 scales."""
     return _decode8("fp8", out, query, key_cache, value_cache, block_table, context_lens,
                     k_scale, v_scale, scale, max_context_len, partition_size, workspace,
                     d_error, stream, lib)

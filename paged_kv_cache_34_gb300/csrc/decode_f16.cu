@@ -1,0 +1,10 @@
+// decode_f16.cu -- the paged decode over 16-bit pools, F16 elements.
+#include "decode_kernel.cuh"
+
+namespace pa {
+
+cudaError_t launch_decode_f16(const DecodeArgs &a, const dec::DecodeParams &p, cudaStream_t s) {
+  return dec::launch_family<F16, 0>(a, p, s);
+}
+
+}  // namespace pa

@@ -72,6 +72,8 @@ EncodeTiledFn encode_fn() {
 // A pool viewed as [rows, heads, head_dim] for TMA: boxes of 128 bytes of one
 // head's row (64 16-bit elements, or 128 int8 codes) by box_rows rows, with
 // the 128-byte swizzle the kernels' shared-memory reads expect.
+// One-byte pools: boxes of one head's whole row (head_dim codes), with the
+// 64-byte swizzle at head_dim 64.
 bool encode_rows_map(CUtensorMap *map, const void *base, pa_dtype dtype, int head_dim,
                      int heads, int64_t rows, int64_t row_stride, int box_rows,
                      bool int8 = false) {
@@ -82,13 +84,16 @@ bool encode_rows_map(CUtensorMap *map, const void *base, pa_dtype dtype, int hea
                               static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * eb,
                                  static_cast<cuuint64_t>(row_stride) * eb};
-  const cuuint32_t box[3] = {int8 ? 128u : 64u, 1, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t box[3] = {int8 ? static_cast<cuuint32_t>(head_dim) : 64u, 1,
+                             static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType dt = int8               ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                  : dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapSwizzle sw =
+      int8 && head_dim == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   CUresult r = enc(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -98,10 +103,11 @@ bool valid_block_size(int bs) { return bs == 8 || bs == 16 || bs == 32 || bs == 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // The automatic plan is the balanced split, as long as its positions fit in
-// int32 (else fixed partitions sized by plan_partition).
-bool use_balanced(int num_seqs, int num_kv_heads, int max_ctx, int partition_size) {
+// int32 (else fixed partitions sized by plan_partition); `units` = decode
+// units (KV-head slices) per sequence.
+bool use_balanced(int num_seqs, int units, int max_ctx, int partition_size) {
   if (partition_size != 0 || max_ctx <= 0) return false;
-  const int64_t t = static_cast<int64_t>(num_seqs) * num_kv_heads * ((max_ctx + 15) / 16) * 16;
+  const int64_t t = static_cast<int64_t>(num_seqs) * units * ((max_ctx + 15) / 16) * 16;
   return t < (1LL << 30);
 }
 
@@ -113,7 +119,8 @@ bool use_balanced(int num_seqs, int num_kv_heads, int max_ctx, int partition_siz
 int plan_partition(int num_seqs, int num_q_heads, int num_kv_heads, int max_ctx,
                    int partition_size, int num_sms) {
   if (partition_size > 0) return partition_size;
-  const long units = static_cast<long>(num_seqs > 0 ? num_seqs : 1) * num_kv_heads;
+  const long units = static_cast<long>(num_seqs > 0 ? num_seqs : 1) * num_kv_heads *
+                     pa::decode_slices(num_q_heads / num_kv_heads).nc;
   const long target_items =
       static_cast<long>(num_sms) * pa::kDecodeCtasPerSm * pa::kDecodeWarps * 8;
   long P = (units * max_ctx + target_items - 1) / target_items;
@@ -297,11 +304,14 @@ pa_status pa_decode_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_h
   if (e != cudaSuccess) return cuda_fail(e);
   size_t ws = 0;
   int P = 0;
-  if (use_balanced(num_seqs, num_kv_heads, max_context_len, partition_size)) {
-    // Balanced split (P reported as 0): pieces x G rows of partial state,
-    // plus the per-sequence prefix sums for the merge kernel.
-    const pa::DecodeBalance d = pa::decode_balance(num_seqs, num_kv_heads, max_context_len, sms);
-    const size_t rows = static_cast<size_t>(d.pieces) * (num_q_heads / num_kv_heads);
+  if (num_q_heads % num_kv_heads != 0) return PA_ERR_SHAPE;
+  const pa::DecodeSlices sl = pa::decode_slices(num_q_heads / num_kv_heads);
+  if (use_balanced(num_seqs, num_kv_heads * sl.nc, max_context_len, partition_size)) {
+    // Balanced split (P reported as 0): pieces x (heads per slice) rows of
+    // partial state, plus the per-sequence prefix sums for the merge kernel.
+    const pa::DecodeBalance d =
+        pa::decode_balance(num_seqs, num_kv_heads * sl.nc, max_context_len, sms);
+    const size_t rows = static_cast<size_t>(d.pieces) * sl.hs;
     ws = align256(rows * head_dim * sizeof(float)) + align256(rows * 2 * sizeof(float)) +
          align256((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t));
   } else {
@@ -344,9 +354,7 @@ pa_status decode_call(void *out, int64_t out_row_stride, const void *query, int6
   if (!isfinite(scale)) return PA_ERR_SHAPE;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
-  if (num_q_heads / num_kv_heads > pa::kDecodeMaxGroup) return PA_ERR_UNSUPPORTED;
   if (!valid_block_size(block_size)) return PA_ERR_UNSUPPORTED;
-  if (int8 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (num_blocks * block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
   if (partition_size % pa::kDecodeSub != 0) return PA_ERR_SHAPE;
   if (num_seqs == 0) return PA_OK;
@@ -397,14 +405,15 @@ pa_status decode_call(void *out, int64_t out_row_stride, const void *query, int6
   a.ws_o = nullptr;
   a.ws_ml = nullptr;
   a.ws_pref = nullptr;
+  a.slices = pa::decode_slices(num_q_heads / num_kv_heads);
+  const int units = num_kv_heads * a.slices.nc;  // decode units per sequence
   cudaError_t e = current_num_sms(&a.num_sms);
   if (e != cudaSuccess) return cuda_fail(e);
   if (balanced) {
-    const pa::DecodeBalance d =
-        pa::decode_balance(num_seqs, num_kv_heads, max_context_len, a.num_sms);
+    const pa::DecodeBalance d = pa::decode_balance(num_seqs, units, max_context_len, a.num_sms);
     a.grid = d.grid;
     a.merge = true;
-    const size_t rows = static_cast<size_t>(d.pieces) * (num_q_heads / num_kv_heads);
+    const size_t rows = static_cast<size_t>(d.pieces) * a.slices.hs;
     char *w = static_cast<char *>(workspace);
     a.ws_o = reinterpret_cast<float *>(w);
     w += align256(rows * head_dim * sizeof(float));
@@ -412,9 +421,9 @@ pa_status decode_call(void *out, int64_t out_row_stride, const void *query, int6
     w += align256(rows * 2 * sizeof(float));
     a.ws_pref = reinterpret_cast<int32_t *>(w);
   } else {
-    // Items are at most S * Hkv * partitions; kDecodeCtasPerSm CTAs per SM,
+    // Items are at most S * units * partitions; kDecodeCtasPerSm CTAs per SM,
     // kDecodeWarps workers each.
-    const int64_t items = static_cast<int64_t>(num_seqs) * num_kv_heads * nparts;
+    const int64_t items = static_cast<int64_t>(num_seqs) * units * nparts;
     int64_t grid = (items + pa::kDecodeWarps - 1) / pa::kDecodeWarps;
     if (grid > static_cast<int64_t>(pa::kDecodeCtasPerSm) * a.num_sms)
       grid = static_cast<int64_t>(pa::kDecodeCtasPerSm) * a.num_sms;
@@ -452,6 +461,18 @@ pa_status decode_call(void *out, int64_t out_row_stride, const void *query, int6
     e = pa::launch_reshape_and_cache(w, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     a.after_write = true;
+    // One new token per sequence (token b of sequence b, the pages' decode
+    // step): the decode takes each sequence's newest row from the step's
+    // input and does not wait for the write.
+    if (w.num_tokens == num_seqs) {
+      a.fused = true;
+      a.new_k = w.key;
+      a.new_v = w.value;
+      a.new_stride = w.row_stride_bytes / 2;
+      a.slot_mapping = w.slot_mapping;
+      a.k_pool = key_cache;
+      a.v_pool = value_cache;
+    }
   }
   e = pa::launch_decode(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);

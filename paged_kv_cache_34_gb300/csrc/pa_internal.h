@@ -49,19 +49,37 @@ cudaError_t launch_copy_blocks(const CopyBlocksArgs &a, cudaStream_t stream);
 constexpr int kDecodeWarps = 4;     // consumer warps (independent workers) per CTA
 constexpr int kDecodeCtasPerSm = 2;  // resident decode CTAs per SM
 constexpr int kDecodeSub = 16;      // tokens per worker per pipeline stage
-constexpr int kDecodeMaxGroup = 8;  // query heads per KV head
 constexpr int kDecodeChunkCap = 2048;  // balanced schedule: most tokens per chunk
+constexpr int kDecodeSliceHeads = 16;  // most query heads one K/V read serves
+
+// The query heads of one KV head (the GQA group, G of them) are served in
+// slices of at most kDecodeSliceHeads heads: one K/V read serves a whole
+// slice (one or two 8-head column groups of the score tile), and a KV head
+// with more query heads is read once per slice.  A decode unit is one
+// (sequence, slice); a sequence has num_kv_heads * nc units.
+struct DecodeSlices {
+  int ng;  // 8-head column groups per slice (1 or 2)
+  int hs;  // query heads per slice (the last slice may hold fewer)
+  int nc;  // slices per KV head
+};
+inline DecodeSlices decode_slices(int group) {
+  DecodeSlices s;
+  s.hs = group < kDecodeSliceHeads ? group : kDecodeSliceHeads;
+  s.ng = s.hs > 8 ? 2 : 1;
+  s.nc = (group + s.hs - 1) / s.hs;
+  return s;
+}
 
 // Balanced decode schedule sizes, shared by the planner and the launcher:
-// the grid (CTAs) and the most pieces (workspace rows per query head) the
-// split can produce for max_context_len.
+// the grid (CTAs) and the most pieces (workspace rows per slice head) the
+// split can produce for max_context_len; `units` = decode units per sequence.
 struct DecodeBalance {
   int grid, workers;
   int64_t pieces;  // units + chunks
 };
-inline DecodeBalance decode_balance(int num_seqs, int num_kv_heads, int max_ctx, int num_sms) {
+inline DecodeBalance decode_balance(int num_seqs, int units, int max_ctx, int num_sms) {
   DecodeBalance d;
-  const int64_t t_max = static_cast<int64_t>(num_seqs) * num_kv_heads * ((max_ctx + 15) / 16) * 16;
+  const int64_t t_max = static_cast<int64_t>(num_seqs) * units * ((max_ctx + 15) / 16) * 16;
   int64_t grid = (t_max / kDecodeSub + kDecodeWarps - 1) / kDecodeWarps;
   if (grid > static_cast<int64_t>(kDecodeCtasPerSm) * num_sms)
     grid = static_cast<int64_t>(kDecodeCtasPerSm) * num_sms;
@@ -71,7 +89,7 @@ inline DecodeBalance decode_balance(int num_seqs, int num_kv_heads, int max_ctx,
   const int64_t per = static_cast<int64_t>(d.workers) * kDecodeChunkCap;
   const int64_t k = t_max > 0 ? (t_max + per - 1) / per : 1;
   const int64_t chunks = k * d.workers;
-  d.pieces = static_cast<int64_t>(num_seqs) * num_kv_heads + chunks;
+  d.pieces = static_cast<int64_t>(num_seqs) * units + chunks;
   return d;
 }
 
@@ -97,12 +115,22 @@ struct DecodeArgs {
   // writes only K/V pool rows: the decode kernel may read everything else
   // before waiting for it.
   bool after_write;
+  // ... and that write's token b is sequence b's newest row (num_new_tokens
+  // == num_seqs): the decode takes that row from new_k / new_v when
+  // slot_mapping[b] is its slot, and does not wait for the write.
+  bool fused = false;
+  const void *new_k = nullptr, *new_v = nullptr;
+  int64_t new_stride = 0;  // elements between tokens of new_k / new_v
+  const int64_t *slot_mapping = nullptr;
+  const void *k_pool = nullptr, *v_pool = nullptr;
+  DecodeSlices slices;
   int32_t *d_error;
   pa_dtype dtype;
-  CUtensorMap tm_k, tm_v;  // pool maps, box (64 | 128 for INT8, 1, box_rows), 128B swizzle
+  // pool maps: box (64 elements | head_dim codes, 1, box_rows), swizzled
+  CUtensorMap tm_k, tm_v;
   int box_rows;
   int num_sms;
-  bool kv_int8 = false;  // 8-bit pools (head_dim 128) with per-KV-head scales
+  bool kv_int8 = false;  // one-byte pools with per-KV-head scales
   bool kv_fp8 = false;   // ... holding E4M3 codes rather than INT8
   const float *k_scale = nullptr, *v_scale = nullptr;
 };

@@ -60,51 +60,6 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
   }
 }
 
-// INT8 pools: each KV head's values are stored as round-half-even(x /
-// scale) clamped to [-127, 127] (NaN -> 0), the division and the rounding in
-// fp32 (cannbot-skills page, App. A quantised-KV scales; the formula is this
-// library's reading).  A scale that is not a positive finite number stores 0
-// and reports PA_DEVERR_SCALE.
-__device__ __forceinline__ bool scale_ok(float s) { return s > 0.0f && s <= 3.4028234663852886e38f; }
-
-__device__ __forceinline__ uint32_t code8(float x, float s) {
-  if (x != x) return 0u;
-  int c = __float2int_rn(__fdiv_rn(x, s));
-  c = c > 127 ? 127 : (c < -127 ? -127 : c);
-  return static_cast<uint32_t>(c) & 0xffu;
-}
-
-// FP8 pools: each value is stored as the nearest E4M3 value (ties to even,
-// saturating at +-448) to x / scale, the division in fp32; NaN -> 0 (the same
-// reading of the pages' quantised-KV scales, with the OCP E4M3 format).  Two
-// values per conversion: `lo` in the low byte.
-__device__ __forceinline__ uint32_t fp8_pair(float lo, float hi, float s) {
-  const float a = lo != lo ? 0.0f : __fdiv_rn(lo, s);
-  const float b = hi != hi ? 0.0f : __fdiv_rn(hi, s);
-  uint16_t r;
-  // the first source goes to the upper byte
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
-  return r;
-}
-
-// 16 values (two 16-byte vectors of fp16/bf16 pairs) -> 16 codes.
-template <class E, bool FP8>
-__device__ __forceinline__ uint4 quant16(const uint4 &a, const uint4 &b, float s) {
-  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-  uint32_t out[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint32_t w0 = w[2 * q], w1 = w[2 * q + 1];
-    if constexpr (FP8) {
-      out[q] = fp8_pair(E::lo(w0), E::hi(w0), s) | (fp8_pair(E::lo(w1), E::hi(w1), s) << 16);
-    } else {
-      out[q] = code8(E::lo(w0), s) | (code8(E::hi(w0), s) << 8) |
-               (code8(E::lo(w1), s) << 16) | (code8(E::hi(w1), s) << 24);
-    }
-  }
-  return make_uint4(out[0], out[1], out[2], out[3]);
-}
-
 // The write into 8-bit pools (INT8 or, with FP8, E4M3 codes).
 template <class E, bool FP8>
 __global__ void __launch_bounds__(256) reshape_and_cache_int8_kernel(

@@ -60,7 +60,7 @@ def decode_call(lib, **kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(hkv=3), 2),                       # Hq % Hkv != 0
-    (dict(hq=32, hkv=2), 3),                # group 16 > 8
+    (dict(hq=8, hkv=16), 2),                # more KV heads than query heads
     (dict(d=96), 3),                        # head_dim not built
     (dict(bs=24), 3),                       # block size not built
     (dict(bt_stride=8), 2),                 # stride < max_blocks_per_seq
@@ -163,7 +163,7 @@ def decode_int8_call(lib, **kw):
     (dict(ks=None), 1),                     # the per-head scales are required
     (dict(vs=None), 1),
     (dict(ks=ctypes.c_void_p(0x10002)), 4),  # scales are fp32: 4-byte aligned
-    (dict(d=64), 3),                        # INT8 pools: head_dim 128 only
+    (dict(d=96), 3),                        # head_dim not built
     (dict(hkv=3), 2),                       # Hq % Hkv != 0
     (dict(kc=MISALIGNED), 4),
     (dict(q=None), 1),
@@ -210,7 +210,7 @@ def test_decode_write_int8_host_validation(lib):
     assert call(vs=None) == 1
     assert call(slots=None) == 1          # the write half is checked first
     assert call(kv_stride=100) == 2
-    assert call(d=64, kv_stride=128) == 3  # INT8 decode: head_dim 128 only
+    assert call(d=96, kv_stride=192) == 3  # head_dim not built
     assert call(ks=ctypes.c_void_p(0x10002)) == 4
 
 
@@ -225,7 +225,7 @@ def test_fp8_host_validation(lib):
     # k_scale, v_scale, scale, max_ctx, part, ws, ws_bytes, dtype, err, stream
     assert d(FAKE, 1024, FAKE, 1024, FAKE, FAKE, FAKE, 16, 16, FAKE, 4, 8, 2, 128, 16, 64,
              None, FAKE, 0.125, 100, 0, None, 0, 0, None, None) == 1
-    assert d(FAKE, 512, FAKE, 512, FAKE, FAKE, FAKE, 16, 16, FAKE, 4, 8, 2, 64, 16, 64,
+    assert d(FAKE, 768, FAKE, 768, FAKE, FAKE, FAKE, 16, 16, FAKE, 4, 8, 2, 96, 16, 64,
              FAKE, FAKE, 0.125, 100, 0, None, 0, 0, None, None) == 3
     s = lib.pa_decode_write_fp8
     assert s(FAKE, 1024, FAKE, 1024, FAKE, FAKE, 256, FAKE, FAKE, None, 4, FAKE, 16, 16, FAKE,

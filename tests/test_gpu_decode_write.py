@@ -57,15 +57,37 @@ def test_llama7b_step_matches_separate_calls_and_oracle(partition_size):
     check(W.make_inputs("llama7b-decode"), partition_size, f"llama7b P{partition_size}")
 
 
-@pytest.mark.parametrize("bs,hq,hkv,dtype", [(16, 8, 2, "f16"), (32, 32, 8, "bf16"),
-                                             (128, 64, 8, "bf16"), (8, 4, 4, "f16")])
-def test_gqa_and_block_sizes(bs, hq, hkv, dtype):
+@pytest.mark.parametrize("bs,hq,hkv,dtype,d", [(16, 8, 2, "f16", 128), (32, 32, 8, "bf16", 128),
+                                               (128, 64, 8, "bf16", 128), (8, 4, 4, "f16", 128),
+                                               (16, 64, 4, "bf16", 128), (32, 64, 2, "f16", 64),
+                                               (16, 8, 1, "bf16", 64)])
+def test_gqa_and_block_sizes(bs, hq, hkv, dtype, d):
     lengths = [1, bs - 1, bs, bs + 1, 63, 200, 333]
-    c = cfg(hq=hq, hkv=hkv, d=128, bs=bs, nb=sum(-(-n // bs) for n in lengths) + 8,
+    c = cfg(hq=hq, hkv=hkv, d=d, bs=bs, nb=sum(-(-n // bs) for n in lengths) + 8,
             dtype=dtype, lengths=lengths, write_new_token=True)
     x = W.make_inputs(c, seed=7 + bs + hq)
     for part in (0, 64):
-        check(x, part, f"bs{bs} g{hq // hkv} {dtype} P{part}")
+        check(x, part, f"bs{bs} g{hq // hkv} d{d} {dtype} P{part}")
+
+
+def test_step_rows_not_the_newest():
+    # One new token per sequence, but slot_mapping does not send every token
+    # to its own sequence's newest position: sequence 1 writes nothing this
+    # step (slot -1, and its context excludes the token), and tokens 2 and 3
+    # are sent to each other's newest slot.  The step must still equal the
+    # write followed by the decode (the decode reads those newest rows from
+    # the pool once the write has finished).
+    c = cfg(hq=8, hkv=2, d=128, bs=16, nb=64, dtype="bf16", lengths=[40, 90, 17, 33, 64],
+            write_new_token=True)
+    x = W.make_inputs(c, seed=13)
+    sm = x.slot_mapping.clone()
+    sm[1] = -1
+    sm[2], sm[3] = x.slot_mapping[3].item(), x.slot_mapping[2].item()
+    x.slot_mapping = sm
+    x.context_lens = x.context_lens.clone()
+    x.context_lens[1] -= 1
+    for part in (0, 64):
+        check(x, part, f"crossed slots P{part}")
 
 
 def test_padding_slots_and_empty_sequences():

@@ -340,3 +340,73 @@ def test_shared_blocks_equal_private_copies(fmt):
     a = _decode_codes(fmt, x, kc, vc, ks, vs, shared, x.context_lens)
     b = _decode_codes(fmt, x, kq, vq, ks, vs, x.block_table, x.context_lens)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 2), (16, 2), (32, 2), (24, 2)])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_head_dim_64_and_wide_groups(fmt, hq, hkv, dtype):
+    # head_dim 64 pools (64-byte code rows) and GQA groups of 1 to 16 query
+    # heads per KV head (24: one full and one partly filled 16-head slice).
+    lengths = [0, 1, 15, 17, 33, 200, 333]
+    for d, bs in ((64, 16), (64, 128), (128, 32)):
+        c = cfg(hq=hq, hkv=hkv, d=d, bs=bs, nb=sum(-(-n // bs) for n in lengths) + 8,
+                dtype=dtype, lengths=lengths)
+        x = W.make_inputs(c, seed=700 + hq + hkv + d + bs)
+        for part in (0, 64):
+            check_decode(fmt, x, part, f"d{d} bs{bs} g{hq // hkv} {dtype} P{part}")
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_llama7b_shape_at_head_dim_64(fmt):
+    # llama7b-decode's batch, lengths and pool with 64-wide heads.
+    x = W.make_inputs("llama7b-decode", head_dim=64)
+    check_decode(fmt, x, 0, "llama7b d64")
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_bf16_queries_outside_fp16_range(fmt):
+    # bf16 queries keep their own range: heads 0-3 beyond fp16's largest
+    # finite value (65504), heads 4-7 below its smallest normal (2^-14).
+    # One-byte codes widen exactly to bf16, so the query is never rounded.
+    require_gpu()
+    x = W.make_inputs(cfg(hq=8, hkv=2, d=128, bs=16, nb=64, dtype="bf16",
+                          lengths=[40, 90, 17, 128]), seed=77)
+    q = x.q.float()
+    q[:, :4] *= 3.0e5
+    q[:, 4:] *= 1.0e-7
+    x.q = q.to(torch.bfloat16)
+    assert (x.q[:, :4].float().abs().max() > 65504) and (x.q[:, 4:].float().abs().max() < 2**-14)
+    check_decode(fmt, x, 0, "bf16 query range")
+    check_decode(fmt, x, 64, "bf16 query range P64")
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("d,hq,hkv", [(64, 8, 2), (128, 32, 2)])
+def test_decode_write_step_shapes(fmt, d, hq, hkv):
+    """The one-call 8-bit step at head_dim 64 and with 16 query heads per KV
+    head: pools equal to the oracle's write, output within tolerance of the
+    oracle's decode over those codes."""
+    require_gpu()
+    c = cfg(hq=hq, hkv=hkv, d=d, bs=16, nb=200, dtype="bf16", lengths=[1, 40, 300, 17, 1000],
+            write_new_token=True)
+    x = W.make_inputs(c, seed=88 + d + hq)
+    kc, vc, ks, vs = pools8(x, fmt)  # the codes after this step's write
+    slots = x.slot_mapping.numpy()
+    k0, v0 = kc.copy(), vc.copy()
+    k0.reshape(-1, hkv, d)[slots] = 0  # before the write
+    v0.reshape(-1, hkv, d)[slots] = 0
+    for part in (0, 64):
+        kd, vd, err = torch.from_numpy(k0.copy()).cuda(), torch.from_numpy(v0.copy()).cuda(), \
+            new_err()
+        q = x.q.cuda()
+        out = torch.full_like(q, float("nan"))
+        GPU_STEP[fmt](out, q, x.k_new.cuda(), x.v_new.cuda(), kd, vd, x.slot_mapping.cuda(),
+                      x.block_table.cuda(), x.context_lens.cuda(), ks.cuda(), vs.cuda(),
+                      scale=x.scale, max_context_len=x.max_context_len, partition_size=part,
+                      d_error=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert np.array_equal(kd.cpu().numpy(), kc) and np.array_equal(vd.cpu().numpy(), vc)
+        assert_close(out, oracle_decode8(fmt, x, kc, vc, ks, vs), x.dtype,
+                     what=f"{fmt} step d{d} g{hq // hkv} P{part}")
