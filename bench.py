@@ -43,6 +43,7 @@ import torch  # noqa: E402
 HEADLINE = "llama7b-decode"
 METRIC = "paged-decode KV-read GB/s (% of HBM peak); varlen prefill TFLOP/s"
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
+HOST_LEAD_CYCLES = 200_000  # ~0.1 ms of device spin ahead of each timed step
 
 
 # ---------------------------------------------------------------------------
@@ -145,13 +146,29 @@ def flush_l2(buf):
     buf[1].sum()
 
 
+def settle(step, seconds: float = 0.25):
+    """Untimed back-to-back steps for a fixed wall time after the warm-up
+    steps, so the timed region does not start while the GPU's clocks are
+    still ramping up from idle."""
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
+
+
 def time_steps(step, k, flush_buf, stream):
     """Per-step device time (ms) with CUDA events on the launching stream, L2
     flushed (untimed) before each step."""
+    settle(step)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
     for i in range(k):
         flush_l2(flush_buf)
+        # a short device-side spin before the start event, so the host has
+        # enqueued the step by the time the GPU reaches it: the interval then
+        # holds the step's device time, not the host's launch latency
+        torch.cuda._sleep(HOST_LEAD_CYCLES)
         starts[i].record(stream)
         step()
         ends[i].record(stream)
@@ -217,8 +234,8 @@ def decode_workspace(pa, x):
     return ws, part, nparts
 
 
-def bench_decode(pa, W, name, steps, warmup, flush_buf, stream, seed=None):
-    x = W.make_inputs(name, seed=seed, device="cuda")
+def bench_decode(pa, W, name, steps, warmup, flush_buf, stream, seed=None, overrides=None):
+    x = W.make_inputs(name, seed=seed, device="cuda", **(overrides or {}))
     out = torch.empty_like(x.q)
     ws, part, nparts = decode_workspace(pa, x)
     step = decode_step_fn(pa, x, out, ws, stream)
@@ -306,8 +323,10 @@ def bench_copy_blocks(pa, steps, warmup, flush_buf, stream):
     return moved, t
 
 
-def bench_prefill(pa, W, steps, warmup, flush_buf, stream):
-    x = W.make_inputs("packed-prefill", device="cuda")
+def bench_prefill(pa, W, steps, warmup, flush_buf, stream, name="packed-prefill"):
+    """A prefill step (this step's K/V rows written, then causal attention of
+    the packed queries against the paged cache), and the prefill call alone."""
+    x = W.make_inputs(name, device="cuda")
     out = torch.empty_like(x.q)
 
     def pre():
@@ -401,15 +420,35 @@ def e2e_decode(pa, W, name, steps, warmup, stream):
 # ---------------------------------------------------------------------------
 # CPU baseline: the oracle on the host cores
 # ---------------------------------------------------------------------------
-def oracle_decode_rate(x_dev, budget_s: float, max_calls: int | None = None):
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def oracle_decode_rate(x_dev, budget_s: float, max_calls: int | None = None,
+                       threads: int | None = None):
     """The oracle's write + decode over sequences of the workload, repeated
-    until ~budget_s of CPU time; returns (GB/s of K/V read, sample text,
-    threads, calls, seconds)."""
+    until ~budget_s of CPU time (on `threads` OpenMP threads, default all);
+    returns (GB/s of K/V read, calls, threads, seconds)."""
     import oracle
     x = x_dev.to("cpu")
     kp = oracle._u16(x.k_pool)
     vp = oracle._u16(x.v_pool)
     lib = oracle.load()
+    oracle.set_threads(threads or os.cpu_count() or 1, lib=lib)
     threads = oracle.max_threads(lib)
     kv_per_seq = (x.context_lens.long() * x.num_kv_heads * x.head_dim * 4).tolist()
     # one call = one sequence's write + decode (all heads); cycle through them
@@ -431,6 +470,49 @@ def oracle_decode_rate(x_dev, budget_s: float, max_calls: int | None = None):
         if el >= budget_s or (max_calls and calls >= max_calls):
             break
     return nbytes / el / 1e9, calls, threads, el
+
+
+def oracle_prefill_rate(x_dev, budget_s: float, rows_per_seq: int = 8):
+    """The oracle's prefill on a sample of query rows (the last rows_per_seq
+    of every sequence: the rows with the most visible keys), repeated until
+    ~budget_s; returns (TFLOP/s of visible pairs, calls, threads, seconds)."""
+    import oracle
+    x = x_dev.to("cpu")
+    lib = oracle.load()
+    oracle.set_threads(os.cpu_count() or 1, lib=lib)
+    threads = oracle.max_threads(lib)
+    kp, vp = oracle._u16(x.k_pool), oracle._u16(x.v_pool)
+    # the step's write first (the sample then reads this step's rows too)
+    oracle.write(kp, vp, x.k_new, x.v_new, x.slot_mapping, x.block_size, lib=lib)
+    cu, q, L = x.cu_seqlens_q.tolist(), x.q_lens.tolist(), x.context_lens.tolist()
+    rows, pairs = [], 0
+    for b in range(x.num_seqs):
+        for i in range(max(0, q[b] - rows_per_seq), q[b]):
+            rows.append(cu[b] + i)
+            pairs += L[b] - q[b] + i + 1
+    rows = np.asarray(rows, dtype=np.int64)
+    flops = 4 * x.num_q_heads * x.head_dim * pairs
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        oracle.prefill(x.q, kp, vp, x.block_table, x.cu_seqlens_q, x.context_lens,
+                       x.num_kv_heads, x.block_size, x.scale, causal=x.causal, rows=rows,
+                       lib=lib)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return flops * calls / el / 1e12, calls, threads, el
+
+
+def headline_config(x, world: int) -> dict:
+    """The headline workload's description, the same in both arms."""
+    return {"workload": HEADLINE, "sequences_per_gpu": x.num_seqs, "context": "U[512,2048]",
+            "heads": f"{x.num_q_heads}/{x.num_kv_heads}", "head_dim": x.head_dim,
+            "block_size": x.block_size, "pool_blocks": x.num_blocks,
+            "step": "one decode step: cache write of each sequence's new token, then "
+                    "attention over its whole context",
+            "l2": "flushed before every timed GPU step (512 MB write, then 512 MB read)",
+            "parallelism": f"replica x{world}" if world > 1 else "single GPU"}
 
 
 # ---------------------------------------------------------------------------
@@ -502,10 +584,9 @@ def run_reference(args):
         "ms_per_step": round(secs * 1e3 / max(1, args.steps), 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": HEADLINE, "sequences": 8, "context": "U[512,2048]",
-                   "heads": "32/32", "head_dim": 128, "block_size": 16, "pool_blocks": 8192},
+        "config": headline_config(x, args.gpus),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
-                         "kind": "oracle",
+                         "kind": "oracle", "cpu_model": cpu_model(),
                          "sample": f"{calls_total} single-sequence write+decode oracle calls "
                                    f"(~{per_step:.2f} s per step) cycling the 8 sequences"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -596,11 +677,14 @@ def main():
     kv = kv_read_bytes(x)
     value, ms_step_max = whole_job_gbs(dist, kv, ms_step)  # every rank's own batch
     merge = nparts is None or nparts > 1  # the merge kernel runs
-    launches_per_step = (1 if x.slot_mapping.numel() else 0) + 1 + (1 if merge else 0)
+    # 16-bit pools with the balanced split write inside the decode launch;
+    # otherwise the write is a launch of its own
+    separate_write = x.slot_mapping.numel() > 0 and part != 0
+    launches_per_step = (1 if separate_write else 0) + 1 + (1 if merge else 0)
 
     ms_dec = statistics.fmean(t_dec)
     dec_achieved = decode_bytes(x) / (ms_dec * 1e-3) / 1e9
-    dec_hash = source_hash("decode.cu", "pa_device.cuh")
+    dec_hash = source_hash("decode_kernel.cuh", "decode.cu", "pa_device.cuh")
     traffic = recorded_traffic("pa_decode", HEADLINE, dec_hash)
 
     line = {
@@ -608,17 +692,13 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step_max, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": HEADLINE, "sequences_per_gpu": x.num_seqs,
-                   "context": "U[512,2048]", "heads": "32/32", "head_dim": 128,
-                   "block_size": 16, "pool_blocks": 8192,
-                   "step": "pa_decode_write: cache write of the 8 new tokens + decode",
-                   "split_kv": "balanced across workers" if part == 0 else
-                               f"fixed partitions of {part} tokens ({nparts} for the longest)",
-                   "kv_bytes_per_step": kv,
-                   "l2": "flushed before every timed step (512 MB write, then 512 MB read)",
-                   "parallelism": f"replica x{world}" if world > 1 else "single GPU",
-                   "wall_s_timed_region": round(wall, 3),
-                   "pct_of_hbm_peak": round(100 * value / world / hbm_peak, 2)},
+        "config": headline_config(x, world),
+        "step_detail": {"call": "pa_decode_write (the cache write inside the decode launch)"
+                                if not separate_write else "pa_decode_write",
+                        "split_kv": "balanced across workers" if part == 0 else
+                                    f"fixed partitions of {part} tokens ({nparts} for the longest)",
+                        "kv_bytes_per_step": kv, "wall_s_timed_region": round(wall, 3),
+                        "pct_of_hbm_peak": round(100 * value / world / hbm_peak, 2)},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
         "roofline": {"kernel": "pa_decode (split-KV decode + merge launches)", "bound": "hbm",
@@ -640,39 +720,77 @@ def main():
                                  "pa_decode_write, one D2H copy of the output], host wall "
                                  "clock, L2 flushed before each step"}
 
+        ob = max(1.0, args.cpu_budget / 6)  # oracle seconds per secondary workload
         if not args.no_secondary:
             sec = {}
-            xp, t_pstep, t_pre = bench_prefill(pa, W, max(10, args.steps // 10), args.warmup,
-                                               flush_buf, stream)
-            fl = prefill_flops(xp)
-            ms_pre = statistics.fmean(t_pre)
-            tf = fl / (ms_pre * 1e-3) / 1e12
-            sec["packed-prefill"] = {
-                "value": round(tf, 2), "unit": "TFLOP/s", "flops": fl,
-                "ms_prefill": round(ms_pre, 5),
-                "ms_write_plus_prefill": round(statistics.fmean(t_pstep), 5),
-                "write_GBps": round(write_bytes(xp) / ((statistics.fmean(t_pstep) - ms_pre)
-                                                      * 1e-3) / 1e9, 1),
-                "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": tf_peak,
-                             "peak_kind": f"{peak_kind} bf16 burst", "unit": "TFLOP/s",
-                             "frac": round(tf / tf_peak, 4),
-                             "traffic": recorded_traffic(
-                                 "pa_prefill_varlen", "packed-prefill",
-                                 source_hash("prefill.cu", "pa_tcgen05.cuh", "pa_device.cuh"))}}
-            del xp
-            xl, _, _, partl, npl, t_lstep, t_ldec = bench_decode(
-                pa, W, "long-context-decode", max(10, args.steps // 10), args.warmup,
-                flush_buf, stream)
-            ms_l = statistics.fmean(t_ldec)
-            gb = decode_bytes(xl) / (ms_l * 1e-3) / 1e9
-            sec["long-context-decode"] = {
-                "value": round(kv_read_bytes(xl) / (ms_l * 1e-3) / 1e9, 1), "unit": "GB/s",
-                "ms_decode": round(ms_l, 5), "partition_size": partl, "partitions": npl,
-                "roofline": {"bound": "hbm", "achieved": round(gb, 1), "peak": hbm_peak,
-                             "unit": "GB/s", "frac": round(gb / hbm_peak, 4),
-                             "traffic": recorded_traffic("pa_decode", "long-context-decode",
-                                                         dec_hash)}}
-            del xl
+            pre_hash = source_hash("prefill.cu", "pa_tcgen05.cuh", "pa_device.cuh")
+            # ---- prefill: packed (q = L) and chunked / multi-token (q < L)
+            for pname in ("packed-prefill", "chunked-prefill"):
+                xp, t_pstep, t_pre = bench_prefill(pa, W, max(10, args.steps // 10), args.warmup,
+                                                   flush_buf, stream, pname)
+                fl = prefill_flops(xp)
+                ms_pre = statistics.fmean(t_pre)
+                tf = fl / (ms_pre * 1e-3) / 1e12
+                kvb = kv_read_bytes(xp)
+                entry = {
+                    "value": round(tf, 2), "unit": "TFLOP/s", "flops": fl,
+                    "kv_bytes": kvb, "ms_prefill": round(ms_pre, 5),
+                    "ms_write_plus_prefill": round(statistics.fmean(t_pstep), 5),
+                    "q_lens": "q = L" if pname == "packed-prefill" else "1, 4, 64 cycling"}
+                if pname == "packed-prefill":
+                    entry["write_GBps"] = round(write_bytes(xp) / ((statistics.fmean(t_pstep)
+                                                                    - ms_pre) * 1e-3) / 1e9, 1)
+                    entry["roofline"] = {
+                        "bound": "tensor", "achieved": round(tf, 1), "peak": tf_peak,
+                        "peak_kind": f"{peak_kind} bf16 burst", "unit": "TFLOP/s",
+                        "frac": round(tf / tf_peak, 4),
+                        "traffic": recorded_traffic("pa_prefill_varlen", pname, pre_hash)}
+                else:
+                    # a few queries per sequence against long contexts: the
+                    # K/V bytes, not the flops, set the bound
+                    gbp = kvb / (ms_pre * 1e-3) / 1e9
+                    entry["roofline"] = {
+                        "bound": "hbm", "achieved": round(gbp, 1), "peak": hbm_peak,
+                        "unit": "GB/s", "frac": round(gbp / hbm_peak, 4),
+                        "traffic": recorded_traffic("pa_prefill_varlen", pname, pre_hash)}
+                r, calls, th, el = oracle_prefill_rate(xp, ob)
+                entry["cpu_baseline"] = {"value": round(r, 6), "unit": "TFLOP/s", "cores": th,
+                                         "kind": "oracle",
+                                         "sample": f"{calls} oracle prefill calls on the last "
+                                                   f"8 query rows of each sequence ({el:.1f} s)"}
+                sec[pname] = entry
+                del xp
+            # ---- 16-bit decodes: the other decode workloads (and a 16-query-
+            # head group over the continuous-batching batch)
+            for dname, over, note in (
+                    ("tiny-decode", {}, "launch-bound (132 KB of K/V): no roofline claim"),
+                    ("continuous-batching", {}, None),
+                    ("continuous-batching", {"num_q_heads": 128},
+                     "128 query heads over 8 KV heads (16 per KV head, one K/V read)"),
+                    ("long-context-decode", {}, None)):
+                key = dname if not over else f"{dname}-g{over['num_q_heads'] // 8}"
+                xd, _, _, partd, npd, _, t_d = bench_decode(
+                    pa, W, dname, max(10, args.steps // 10), args.warmup, flush_buf, stream,
+                    overrides=over)
+                ms_d = statistics.fmean(t_d)
+                gbd = decode_bytes(xd) / (ms_d * 1e-3) / 1e9
+                entry = {"value": round(kv_read_bytes(xd) / (ms_d * 1e-3) / 1e9, 1),
+                         "unit": "GB/s", "ms_decode": round(ms_d, 5),
+                         "heads": f"{xd.num_q_heads}/{xd.num_kv_heads}",
+                         "partition_size": partd, "partitions": npd}
+                if note:
+                    entry["note"] = note
+                entry["roofline"] = None if dname == "tiny-decode" else {
+                    "bound": "hbm", "achieved": round(gbd, 1), "peak": hbm_peak,
+                    "unit": "GB/s", "frac": round(gbd / hbm_peak, 4),
+                    "traffic": recorded_traffic("pa_decode", key, dec_hash)}
+                r, calls, th, el = oracle_decode_rate(xd, ob)
+                entry["cpu_baseline"] = {"value": round(r, 4), "unit": "GB/s", "cores": th,
+                                         "kind": "oracle",
+                                         "sample": f"{calls} single-sequence oracle decode "
+                                                   f"calls ({el:.1f} s)"}
+                sec[key] = entry
+                del xd
             for fmt, pools in (("int8", "int8 codes"), ("fp8", "FP8 E4M3 codes")):
                 xi, parti, npi, t_istep, t_idec = bench_decode_kv8(
                     pa, W, HEADLINE, max(20, args.steps // 4), args.warmup, flush_buf, stream,
@@ -708,12 +826,16 @@ def main():
                                  source_hash("copy_blocks.cu", "pa_device.cuh"))}}
             line["secondary"] = sec
 
-        # ---- the oracle on the host cores -------------------------------
+        # ---- the oracle on the host cores: all of them, then one --------
         r, calls, threads, el = oracle_decode_rate(x, args.cpu_budget)
+        r1, calls1, _, el1 = oracle_decode_rate(x, max(1.0, args.cpu_budget / 3), threads=1)
         line["cpu_baseline"] = {"value": round(r, 4), "unit": "GB/s", "cores": threads,
-                                "kind": "oracle",
+                                "kind": "oracle", "cpu_model": cpu_model(),
+                                "value_single_thread": round(r1, 4),
                                 "sample": f"{calls} single-sequence write+decode oracle calls "
-                                          f"({el:.1f} s) cycling the workload's 8 sequences"}
+                                          f"({el:.1f} s) cycling the workload's 8 sequences on "
+                                          f"{threads} threads; {calls1} calls ({el1:.1f} s) on "
+                                          "one thread"}
         print(json.dumps(line))
     if dist is not None:
         dist.barrier()

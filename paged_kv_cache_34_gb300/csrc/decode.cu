@@ -48,14 +48,15 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
   p.ws_o = a.ws_o;
   p.ws_ml = a.ws_ml;
   p.ws_pref = a.ws_pref;
+  p.nw = a.num_new;
   p.after_write = a.after_write ? 1 : 0;
-  p.fused = a.fused ? 1 : 0;
   p.new_k = a.new_k;
   p.new_v = a.new_v;
   p.new_stride = a.new_stride;
   p.slot_mapping = a.slot_mapping;
   p.k_pool = a.k_pool;
   p.v_pool = a.v_pool;
+  p.num_slots = a.num_blocks * a.block_size;
   p.k_scale = a.k_scale;
   p.v_scale = a.v_scale;
   p.err = a.d_error;

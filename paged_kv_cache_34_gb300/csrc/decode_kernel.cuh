@@ -49,10 +49,11 @@
 //    fragments (warp-shuffle max over tokens), P^T is formed with movmatrix,
 //    and O^T[D x 8] += V^T[D x 16] P^T[16 x 8] reads V through ldmatrix.trans
 //    (16-bit pools) or widens one-byte codes into fragments in registers.
-//  * The one-call decode step: when the step's cache write runs just before
-//    this kernel and new token b is sequence b's newest position, the
-//    worker holding that position takes its K/V row from the step's input
-//    instead of the pool, so the decode never waits for the write.
+//  * The one-call decode step: the same launch also writes the step's new
+//    K/V rows into the pool (workers copy them before their first stage
+//    lands), and the worker holding a sequence's newest row takes it from
+//    the token that slot_mapping sends there, straight from the step's
+//    input, so no read waits for the write.
 //  * Exponentials are base 2 with the scale pre-multiplied by log2(e).
 #pragma once
 
@@ -68,6 +69,11 @@ namespace dec {
 
 constexpr int kWorkers = kDecodeWarps;
 constexpr int kThreads = (kWorkers + 1) * 32;  // + producer warp
+// The one-call step adds a writer warp; at most three warps per SM
+// sub-partition either way (two CTAs per SM), so the register budget is the
+// same.
+constexpr int threads_for(bool wr) { return (kWorkers + (wr ? 2 : 1)) * 32; }
+constexpr int kWriterWarp = kWorkers + 1;
 constexpr uint32_t kTerminate = 0x100u;        // stage header: no more data
 
 // A stage holds, per K and V, `kRegions` regions of kWorkers x kRows rows:
@@ -86,9 +92,11 @@ struct DecodeSmem {
   static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kHdrOffset = kBarOffset + 2 * kStages * 8;
   static constexpr int kAbortOffset = kHdrOffset + 32;  // after kStages (<= 8) headers
-  // per worker: the step's input K and V rows of its piece's newest token
+  // per worker (one-call step, 16-bit pools): the step's input K and V rows
+  // of its piece's newest token, then that row's block id and token b's slot
   static constexpr int kNewOffset = kAbortOffset + 128;
-  static constexpr int kNewBytes = 2 * D * 2;
+  static constexpr int kNewMeta = KV8 ? 0 : 2 * D * 2;
+  static constexpr int kNewBytes = KV8 ? 0 : kNewMeta + 16;
   static constexpr int kVarOffset = kNewOffset + kWorkers * kNewBytes;  // pref[S+1], len[S], ids
   static int bytes(int num_seqs, int max_ids) {
     return 1024 + kVarOffset + 4 * (2 * num_seqs + 1) + 4 * kWorkers * 2 * max_ids;
@@ -114,17 +122,20 @@ struct DecodeParams {
   float *ws_o, *ws_ml;
   int32_t *ws_pref;  // balanced: the prefix sums, for the merge kernel
   const float *k_scale, *v_scale;  // one-byte pools: per-KV-head dequantisation scales
-  // Launched directly after this step's cache write: only K/V pool rows can
-  // be that kernel's output, so everything else is read at once.
+  // The one-call step: nw new tokens (new_k / new_v [nw, Hkv, D] rows at
+  // new_stride elements) are written to pool rows slot_mapping[t] (of
+  // num_slots) in the same launch; a sequence's newest row is taken from
+  // the token written to it.  nw = 0: a plain decode.
+  int32_t nw;
+  // Launched right after this step's cache write as its own kernel (the
+  // two-launch step): only K/V pool rows can be that kernel's output, so
+  // everything else is read at once and only the first K/V load waits.
   int32_t after_write;
-  // ... and new token b is sequence b's newest row: that row is taken from
-  // new_k / new_v ([S, Hkv, D] at new_stride elements) when slot_mapping[b]
-  // is its slot, so the decode does not wait for the write.
-  int32_t fused;
   const void *new_k, *new_v;
   int64_t new_stride;
   const int64_t *slot_mapping;
-  const void *k_pool, *v_pool;  // the pools, for a newest row whose slot differs
+  void *k_pool, *v_pool;
+  int64_t num_slots;
   int32_t *err;
 };
 
@@ -286,47 +297,17 @@ __device__ __forceinline__ void load_q(uint32_t (&qf)[NG][D / 16][2], const Deco
   }
 }
 
-// Widens four one-byte codes (one word) to two pairs of the operand type
-// exactly: lo gets bytes 0-1, hi bytes 2-3 (the lower byte in the lower
-// half).  Every INT8 code and every E4M3 value is exactly representable in
-// both fp16 and bf16.
-//  INT8 -> fp16: with the sign bit flipped a code c is the byte u = c + 128;
-//    the fp16 with bits 0x6400 | u is 1024 + u, and subtracting 1152 leaves c.
-//  INT8 -> bf16: the bf16 0x4300 | (c & 0x7f) is 128 + (c & 0x7f), and
-//    0x4300 | (c & 0x80) is 128 or 256 by the sign bit; their difference is
-//    the two's-complement value c.
-//  E4M3 -> fp16: the hardware converts two values per instruction.
-//  E4M3 -> bf16: through fp16; an fp16 normal (every nonzero E4M3 value is
-//    one) with its exponent-and-mantissa field shifted right by 3 is the bf16
-//    with the same fraction and the exponent field reinterpreted under bias
-//    127, i.e. the value times 2^-112, which one exact multiply undoes.
-template <bool FP8, bool BF>
+// Widens four one-byte codes (one word) to two fp16 pairs exactly: lo gets
+// bytes 0-1, hi bytes 2-3 (the lower byte in the lower half).  Every INT8
+// code and every E4M3 value is an fp16 value.
+//  INT8: with the sign bit flipped a code c is the byte u = c + 128; the
+//    fp16 with bits 0x6400 | u is 1024 + u, and subtracting 1152 leaves c.
+//  E4M3: the hardware converts two values per instruction.
+template <bool FP8>
 __device__ __forceinline__ void widen4(uint32_t w, uint32_t &lo, uint32_t &hi) {
   if constexpr (FP8) {
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"(static_cast<uint16_t>(w & 0xffffu)));
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"(static_cast<uint16_t>(w >> 16)));
-    if constexpr (BF) {
-      const __nv_bfloat162 two112 = __halves2bfloat162(__ushort_as_bfloat16(0x7780),
-                                                       __ushort_as_bfloat16(0x7780));
-      uint32_t a = ((lo >> 3) & 0x0fff0fffu) | (lo & 0x80008000u);
-      uint32_t b = ((hi >> 3) & 0x0fff0fffu) | (hi & 0x80008000u);
-      __nv_bfloat162 ha = __hmul2(*reinterpret_cast<__nv_bfloat162 *>(&a), two112);
-      __nv_bfloat162 hb = __hmul2(*reinterpret_cast<__nv_bfloat162 *>(&b), two112);
-      lo = *reinterpret_cast<uint32_t *>(&ha);
-      hi = *reinterpret_cast<uint32_t *>(&hb);
-    }
-  } else if constexpr (BF) {
-    uint32_t a, b;
-    asm("prmt.b32 %0, %1, 0, 0x4140;" : "=r"(a) : "r"(w));  // bytes 0, 1 -> low bytes of halves
-    asm("prmt.b32 %0, %1, 0, 0x4342;" : "=r"(b) : "r"(w));  // bytes 2, 3
-    const uint32_t ax = (a & 0x007f007fu) | 0x43004300u, ay = (a & 0x00800080u) | 0x43004300u;
-    const uint32_t bx = (b & 0x007f007fu) | 0x43004300u, by = (b & 0x00800080u) | 0x43004300u;
-    __nv_bfloat162 ha = __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&ax),
-                                *reinterpret_cast<const __nv_bfloat162 *>(&ay));
-    __nv_bfloat162 hb = __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&bx),
-                                *reinterpret_cast<const __nv_bfloat162 *>(&by));
-    lo = *reinterpret_cast<uint32_t *>(&ha);
-    hi = *reinterpret_cast<uint32_t *>(&hb);
   } else {
     const uint32_t u = w ^ 0x80808080u;
     uint32_t a, b;
@@ -341,15 +322,50 @@ __device__ __forceinline__ void widen4(uint32_t w, uint32_t &lo, uint32_t &hi) {
 }
 
 // Two code words a, b holding the same four elements of two tokens -> the
-// operand pairs (a.byte i, b.byte i): e0 for i = 0, e1 for 1, e2 for 2, e3 for 3.
-template <bool FP8, bool BF>
+// fp16 pairs (a.byte i, b.byte i): e0 for i = 0, e1 for 1, e2 for 2, e3 for 3.
+template <bool FP8>
 __device__ __forceinline__ void widen_tokens(uint32_t a, uint32_t b, uint32_t &e0,
                                              uint32_t &e1, uint32_t &e2, uint32_t &e3) {
   uint32_t x, y;
   asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(x) : "r"(a), "r"(b));
   asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(y) : "r"(a), "r"(b));
-  widen4<FP8, BF>(x, e0, e1);
-  widen4<FP8, BF>(y, e2, e3);
+  widen4<FP8>(x, e0, e1);
+  widen4<FP8>(y, e2, e3);
+}
+
+// bf16 queries over one-byte pools run on the fp16 tensor-core path: each
+// head's query is multiplied by the power of two 2^e that brings its largest
+// magnitude into [2^14, 2^15) and rounded to fp16 -- exact for every element
+// within 2^28 of that largest one (bf16 has 8 significant bits, fp16 11) --
+// and the head's scores are multiplied back by 2^-e, so no query value
+// leaves fp16's range.  Lane (head column, t) holds the pairs of load_q;
+// qsc[n] receives 2^-e of the lane's head in column group n.
+template <int D, int NG>
+__device__ __forceinline__ void q_bf16_to_f16(uint32_t (&qf)[NG][D / 16][2],
+                                              float (&qsc)[NG]) {
+#pragma unroll
+  for (int n = 0; n < NG; ++n) {
+    float mx = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks)
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        mx = fmaxf(mx, fmaxf(fabsf(BF16::lo(qf[n][ks][j])), fabsf(BF16::hi(qf[n][ks][j]))));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));  // the head's four lanes
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    int e = 0;
+    if (mx > 0.f) {
+      const int ex = static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 127;  // floor(log2)
+      e = min(126, max(-126, 14 - ex));
+    }
+    const float f = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks)
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        qf[n][ks][j] = F16::pack2(BF16::lo(qf[n][ks][j]) * f, BF16::hi(qf[n][ks][j]) * f);
+    qsc[n] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+  }
 }
 
 __device__ __forceinline__ void lds128(uint32_t addr, uint32_t (&w)[4]) {
@@ -371,14 +387,19 @@ __device__ __forceinline__ uint32_t chunk_off(int r, int c) {
 }
 
 // KVF: the pool format -- 0 fp16/bf16 (as E), 1 INT8 codes, 2 FP8 (E4M3)
-// codes.  NG: 8-head column groups per slice (1 or 2).
-template <class E, int D, bool BAL, int KVF, int NG>
-__global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm)
+// codes.  NG: 8-head column groups per slice (1 or 2).  WR: the one-call
+// step (the launch also writes the step's new rows); the plain decode is
+// built without that code, which would otherwise cost it registers.
+template <class E, int D, bool BAL, int KVF, int NG, bool WR>
+__global__ void __launch_bounds__(threads_for(WR), kDecodeCtasPerSm)
     decode_persistent_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                              const __grid_constant__ CUtensorMap tmv) {
-  constexpr bool KV8 = KVF != 0;  // one-byte codes, widened to the query's type
+  constexpr bool KV8 = KVF != 0;  // one-byte codes, widened to fp16
   constexpr bool FP8 = KVF == 2;
-  constexpr bool BF = E::kBF16;
+  using M = std::conditional_t<KV8, F16, E>;  // the tensor cores' operand type
+  constexpr bool BF = M::kBF16;
+  constexpr bool QS = KV8 && E::kBF16;  // bf16 queries rescaled per head into fp16
+  static_assert(!(WR && KV8), "the one-call step is built for 16-bit pools");
   using S = DecodeSmem<D, KV8>;
   constexpr int NH = S::kHalves;
   constexpr int NR = S::kRegions;
@@ -405,11 +426,8 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int P = p.partition_size;
   const int nseq = p.num_seqs;
-  // Inputs come from earlier kernels.  Launched right after this step's
-  // cache write (`after_write`), only the K/V rows can be the write's
-  // output: the kernel then reads context_lens, block_table and q at once
-  // and waits, if at all, only before its first K/V load (in the producer
-  // below).
+  // Inputs come from earlier kernels (after a separate cache write, only its
+  // K/V rows do: see after_write).
   if (!p.after_write) griddep_wait();
   griddep_launch_dependents();
   if (tid == 0) {
@@ -468,6 +486,44 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm)
   if (sc.balanced && blockIdx.x == 0 && p.ws_pref)
     for (int i = tid; i <= nseq; i += blockDim.x) p.ws_pref[i] = s_pref[i];
   const int bs = p.block_size;
+
+  // The one-call step's cache write (16-bit pools), done by each CTA's
+  // writer warp while the producer and the workers run: lane-global index i
+  // covers 16-byte chunk i % C of token i / C's K and V rows (C chunks per
+  // row, all KV heads), so each lane copies at most a chunk or two.  Slots
+  // < 0 write nothing; slots past the pool are reported and skipped.
+  auto write_new = [&]() {
+    const int C = p.hkv * D / 8;
+    const int64_t total = static_cast<int64_t>(p.nw) * C;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * 32;
+#pragma unroll 1
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * 32 + lane; i < total; i += stride) {
+      const int t = static_cast<int>(i / C), c = static_cast<int>(i - static_cast<int64_t>(t) * C);
+      // the row's loads are issued with the slot's (their addresses do not
+      // depend on it)
+      const uint4 k = __ldg(reinterpret_cast<const uint4 *>(
+                                static_cast<const typename E::T *>(p.new_k) + t * p.new_stride) +
+                            c);
+      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(
+                                static_cast<const typename E::T *>(p.new_v) + t * p.new_stride) +
+                            c);
+      const int64_t slot = __ldg(p.slot_mapping + t);
+      if (slot < 0) continue;
+      if (slot >= p.num_slots) {
+        if (c == 0) raise_error(p.err, PA_DEVERR_SLOT);
+        continue;
+      }
+      static_cast<uint4 *>(p.k_pool)[slot * C + c] = k;
+      static_cast<uint4 *>(p.v_pool)[slot * C + c] = v;
+    }
+  };
+
+  if constexpr (WR) {
+    if (warp == kWriterWarp) {
+      write_new();
+      return;
+    }
+  }
 
   // ------------------------------------------------------------ producer --
   if (warp == kWorkers) {
@@ -562,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm)
           cur += ROWS;
         }
       }
-      if (c == 0 && p.after_write && !p.fused) griddep_wait();  // the cache write has landed
+      if (c == 0 && p.after_write) griddep_wait();  // the cache write has landed
       const unsigned live = __ballot_sync(0xffffffffu, feeder && act);
       const unsigned badmask = __ballot_sync(0xffffffffu, bad);
       int nbox = nb;
@@ -582,7 +638,6 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm)
             mbar_wait_bounded(smem_u32(full + (k % NS)), (k / NS) & 1);
         }
         cp_async_wait_all();
-        if (p.fused) griddep_wait();  // this grid ends after the cache write
         return;
       }
       if (live == 0) {
@@ -591,7 +646,6 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm)
           mbar_arrive(smem_u32(full + s));
         }
         cp_async_wait_all();
-        if (p.fused) griddep_wait();  // this grid ends after the cache write
         return;
       }
       const uint32_t bar = smem_u32(full + s);
@@ -622,6 +676,7 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm)
   // ----------------------------------------------------- consumer = worker --
   float sl = p.scale_log2;  // one-byte pools: times the piece's K scale
   float vsc = 1.f;          // one-byte pools: the piece's V scale
+  float slh[QS ? NG : 1][2];  // bf16 queries over one-byte pools: sl times each head's 2^-e
   const int r0 = warp * ROWS;  // this worker's rows in a stage
   const int mj = lane >> 3, mr = lane & 7;
   const int g8 = lane >> 2, t4 = lane & 3;
@@ -640,9 +695,8 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm)
   // this worker's shared buffer, with the row's block id and the token's
   // slot_mapping entry (see put_newest).
   bool nw_on = false;
-  int nw_id = 0;
-  int64_t nw_sm = 0;
   uint8_t *s_new = smem + S::kNewOffset + warp * S::kNewBytes;
+  int64_t *s_nw = reinterpret_cast<int64_t *>(s_new + S::kNewMeta);  // [block id, token b's slot]
   if (sc.balanced) {
     // Empty sequences have no pieces: their (zero) outputs are written here.
     for (int b = blockIdx.x * kWorkers + warp; b < nseq; b += sc.NW) {
@@ -819,18 +873,35 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm)
             if (lane == 0) raise_error(p.err, PA_DEVERR_SCALE);
           }
         }
-        // The one-call step: the newest row's block id, the token's slot
-        // and its input rows (copied into this worker's buffer: 16 bytes per
-        // lane, K then V), all used at the row's stage.
-        nw_on = p.fused && m.end == m.L;
+        if constexpr (QS) {
+          float qsc[NG];
+          q_bf16_to_f16<D, NG>(qf, qsc);
+#pragma unroll
+          for (int n = 0; n < NG; ++n) {  // heads 8n + 2t, +1 sit in head columns 2t, 2t + 1
+            slh[n][0] = sl * __shfl_sync(0xffffffffu, qsc[n], 8 * t4);
+            slh[n][1] = sl * __shfl_sync(0xffffffffu, qsc[n], 8 * t4 + 4);
+          }
+        }
+        // The one-call step: the newest row's block id and, for the usual
+        // step (token b is sequence b's new token), token b's slot and its
+        // input rows (copied into this worker's buffer: 16 bytes per lane,
+        // K then V), all used at the row's stage.
+        nw_on = WR && m.end == m.L;
         if (nw_on) {
-          nw_id = __ldg(p.block_table + static_cast<int64_t>(m.b) * p.bt_stride + (m.L - 1) / bs);
-          nw_sm = __ldg(p.slot_mapping + m.b);
-          if (lane < D / 4) {
-            const typename E::T *src = static_cast<const typename E::T *>(
-                                           lane < D / 8 ? p.new_k : p.new_v) +
-                                       m.b * p.new_stride + kvh * D + 8 * (lane % (D / 8));
-            cp_async_16(smem_u32(s_new + lane * 16), src);
+          // copied asynchronously (no register waits on them here)
+          if (lane == 0) {  // the block id lands in the low word
+            cp_async_4(smem_u32(s_nw),
+                       p.block_table + static_cast<int64_t>(m.b) * p.bt_stride + (m.L - 1) / bs);
+            if (m.b < p.nw) cp_async_8(smem_u32(s_nw + 1), p.slot_mapping + m.b);
+            else s_nw[1] = -2;
+          }
+          if (m.b < p.nw) {
+            if (lane < D / 4) {
+              const typename E::T *src = static_cast<const typename E::T *>(
+                                             lane < D / 8 ? p.new_k : p.new_v) +
+                                         m.b * p.new_stride + kvh * D + 8 * (lane % (D / 8));
+              cp_async_16(smem_u32(s_new + lane * 16), src);
+            }
           }
           cp_async_commit();
         }
@@ -872,56 +943,50 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm)
     }
     return false;
   };
-  // Puts the piece's newest row (stage row rr of this worker) in place.
-  // When slot_mapping sends the step's token to that row's slot, the row is
-  // the step's input (from the worker's buffer; one-byte pools take the
-  // write's quantiser, so the codes are the ones the write stores);
-  // otherwise the row is whatever the pool holds once the cache write has
-  // finished.  A bad block id leaves the stage as loaded: the piece is
-  // flagged by the producer and contributes nothing.
-  auto put_newest = [&](uint8_t *kst, int rr) {
+  // Puts the piece's newest row (stage row rr of this worker) in place: the
+  // pool row as the TMA loaded it may or may not already hold this step's
+  // write, so when a new token is written to that row's slot the row is
+  // taken from the token's input instead (one-byte pools take the write's
+  // quantiser, so the codes are the ones the write stores).  The token is
+  // token b when slot_mapping[b] is the row's slot (the usual step), else the
+  // last token sent there; with none, the pool's row stands.  A bad block
+  // id leaves the stage as loaded: the piece is flagged by the producer and
+  // contributes nothing.
+  auto put_newest = [&](uint8_t *kst, int rr) -> bool {
     cp_async_wait_all();
     __syncwarp();
-    const int64_t slot =
-        static_cast<int64_t>(nw_id) * bs + (cur_item.L - 1) % bs;
-    if (nw_id < 0 || nw_id >= p.num_blocks) return;
-    const bool from_input = nw_sm == slot;
-    if (!from_input) griddep_wait();  // every lane: the write's memory is visible after it
+    const int64_t nw_id = *reinterpret_cast<const int32_t *>(s_nw), nw_sm = s_nw[1];
+    if (nw_id < 0 || nw_id >= p.num_blocks) return false;
+    const int64_t slot = nw_id * bs + (cur_item.L - 1) % bs;
     const int kvh = p.nc == 1 ? cur_item.g : cur_item.g / p.nc;
+    if (nw_sm != slot) {
+      int t = -1;
+      for (int base = 0; base < p.nw; base += 32) {
+        const int tt = base + lane;
+        const unsigned hit =
+            __ballot_sync(0xffffffffu, tt < p.nw && __ldg(p.slot_mapping + tt) == slot);
+        if (hit) t = base + 31 - __clz(hit);
+      }
+      if (t < 0) return false;  // no token of this step is written to the row
+      if (lane < D / 4)
+        *reinterpret_cast<uint4 *>(s_new + lane * 16) = __ldg(reinterpret_cast<const uint4 *>(
+            static_cast<const typename E::T *>(lane < D / 8 ? p.new_k : p.new_v) +
+            t * p.new_stride + kvh * D + 8 * (lane % (D / 8))));
+      __syncwarp();
+    }
     const int row = r0 + rr;
-    constexpr int C = KV8 ? D / 16 : D / 8;  // 16-byte chunks of a stage row, per tensor
+    constexpr int C = D / 8;  // 16-byte chunks of a stage row, per tensor
     if (lane < 2 * C) {
-      const int which = lane / C, c = lane % C;
-      uint4 v;
-      if (from_input) {
-        if constexpr (KV8) {
-          // input chunks 2c, 2c + 1 of this tensor (elements 16c .. 16c + 15)
-          const uint4 *in = reinterpret_cast<const uint4 *>(s_new + which * D * 2) + 2 * c;
-          const float s = __ldg((which ? p.v_scale : p.k_scale) + kvh);
-          v = scale_ok(s) ? quant16<E, FP8>(in[0], in[1], s) : make_uint4(0u, 0u, 0u, 0u);
-        } else {
-          v = *(reinterpret_cast<const uint4 *>(s_new) + lane);
-        }
-      } else {
-        const int64_t rowb = (slot * p.hkv + kvh) * D * (KV8 ? 1 : 2);
-        v = __ldcg(reinterpret_cast<const uint4 *>(
-                       static_cast<const uint8_t *>(which ? p.v_pool : p.k_pool) + rowb) +
-                   c);
-      }
-      if constexpr (KV8) {
-        *reinterpret_cast<uint4 *>(kst + which * RB + chunk_off<RP>(row, c)) = v;
-      } else {
-        const int h = c >> 3;  // 64-element half
-        *reinterpret_cast<uint4 *>(kst + which * NH * RB + h * RB + chunk_off<128>(row, c & 7)) =
-            v;
-      }
+      const int which = lane / C, c = lane % C, h = c >> 3;  // h: 64-element half
+      *reinterpret_cast<uint4 *>(kst + which * NH * RB + h * RB + chunk_off<128>(row, c & 7)) =
+          *(reinterpret_cast<const uint4 *>(s_new) + lane);
     }
     __syncwarp();
+    return true;
   };
   // The next piece starts at the top of the loop, before its first stage is
   // waited for (its query loads overlap the wait).
   bool active = false, need_piece = true;
-
   for (int c = 0;; ++c) {
     const int s = c % NS;
     if (need_piece) {
@@ -941,10 +1006,9 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm)
       const int j0 = cur;
       uint8_t *kst = smem + s * S::kStageBytes;
       bool touched = false;  // generic-proxy writes into the stage
-      if (nw_on && end - 1 < j0 + ROWS) {
-        put_newest(kst, end - 1 - j0);
-        touched = true;
-      }
+      // the piece's newest row (one-call step): this worker's stage row
+      // end - 1 - j0
+      if (WR && nw_on && end - 1 < j0 + ROWS) touched = put_newest(kst, end - 1 - j0);
       if constexpr (!KV8) {
         if (j0 + ROWS > end) {
           // Rows past the context may hold anything (even NaN); their weight
@@ -965,7 +1029,7 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm)
       constexpr int PASSES = (KV8 && NG == 2) ? 2 : 1;
       constexpr int NTP = NT / PASSES;       // score tiles per pass
       constexpr int VWW = KV8 ? D / 32 : 1;  // code words per V token row per lane
-#pragma unroll 1
+#pragma unroll
       for (int ps = 0; ps < PASSES; ++ps) {
         float sc2[NG][NTP][4];
 #pragma unroll
@@ -991,21 +1055,30 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm)
           const uint32_t kr = smem_u32(kst) + r0 * RP;
           const uint32_t vr = smem_u32(kst) + RB + r0 * RP;
           constexpr int KC = D / 64;  // 16-byte K chunks per lane per row
+          // K codes: every tile's loads issued before the first widening
+          // (one column group), or a chunk at a time (two: fewer registers).
+          constexpr int KL = NG == 1 ? KC : 1;  // chunks loaded per batch
 #pragma unroll
-          for (int uu = 0; uu < NTP; ++uu) {
-            const int u = ps * NTP + uu;
+          for (int cb = 0; cb < KC; cb += KL) {
+            uint32_t kw[NTP][2][KL][4];  // [tile][row g | g + 8][chunk][word]
 #pragma unroll
-            for (int cc = 0; cc < KC; ++cc) {
-              uint32_t kw[2][4];  // [row g | g + 8][word] of chunk KC t + cc
+            for (int uu = 0; uu < NTP; ++uu)
 #pragma unroll
               for (int r = 0; r < 2; ++r)
-                lds128(kr + chunk_off<RP>(16 * u + g8 + 8 * r, KC * t4 + cc), kw[r]);
 #pragma unroll
-              for (int kq = 0; kq < 4; ++kq) {
-                const int ks = 4 * cc + kq;
+                for (int cc = 0; cc < KL; ++cc)
+                  lds128(kr + chunk_off<RP>(16 * (ps * NTP + uu) + g8 + 8 * r,
+                                            KC * t4 + cb + cc),
+                         kw[uu][r][cc]);
+
+#pragma unroll
+            for (int kq = 0; kq < 4 * KL; ++kq) {
+              const int ks = 4 * cb + kq;
+#pragma unroll
+              for (int uu = 0; uu < NTP; ++uu) {
                 uint32_t a0, a1, a2, a3;
-                widen4<FP8, BF>(kw[0][kq], a0, a2);
-                widen4<FP8, BF>(kw[1][kq], a1, a3);
+                widen4<FP8>(kw[uu][0][kq >> 2][kq & 3], a0, a2);
+                widen4<FP8>(kw[uu][1][kq >> 2][kq & 3], a1, a3);
 #pragma unroll
                 for (int n = 0; n < NG; ++n)
                   mma_16816<BF>(sc2[n][uu], a0, a1, a2, a3, qf[n][ks][0], qf[n][ks][1]);
@@ -1074,13 +1147,18 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm)
         for (int n = 0; n < NG; ++n) {
           float sv[NTP][4];
           float mx0 = -INFINITY, mx1 = -INFINITY;
+          float slA = sl, slB = sl;  // the score factors of this lane's two heads
+          if constexpr (QS) {
+            slA = slh[n][0];
+            slB = slh[n][1];
+          }
 #pragma unroll
           for (int uu = 0; uu < NTP; ++uu) {
             const int t0 = j0 + 16 * (ps * NTP + uu) + g8, t1 = t0 + 8;
-            sv[uu][0] = t0 < end ? sc2[n][uu][0] * sl : -INFINITY;
-            sv[uu][1] = t0 < end ? sc2[n][uu][1] * sl : -INFINITY;
-            sv[uu][2] = t1 < end ? sc2[n][uu][2] * sl : -INFINITY;
-            sv[uu][3] = t1 < end ? sc2[n][uu][3] * sl : -INFINITY;
+            sv[uu][0] = t0 < end ? sc2[n][uu][0] * slA : -INFINITY;
+            sv[uu][1] = t0 < end ? sc2[n][uu][1] * slB : -INFINITY;
+            sv[uu][2] = t1 < end ? sc2[n][uu][2] * slA : -INFINITY;
+            sv[uu][3] = t1 < end ? sc2[n][uu][3] * slB : -INFINITY;
             mx0 = fmaxf(mx0, fmaxf(sv[uu][0], sv[uu][2]));
             mx1 = fmaxf(mx1, fmaxf(sv[uu][1], sv[uu][3]));
           }
@@ -1099,10 +1177,10 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm)
           float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
           for (int uu = 0; uu < NTP; ++uu) {
-            const uint32_t w0 = E::pack2(exp2f(sv[uu][0] - mn0), exp2f(sv[uu][1] - mn1));  // t0
-            const uint32_t w1 = E::pack2(exp2f(sv[uu][2] - mn0), exp2f(sv[uu][3] - mn1));  // t1
-            ls0 += E::lo(w0) + E::lo(w1);
-            ls1 += E::hi(w0) + E::hi(w1);
+            const uint32_t w0 = M::pack2(exp2f(sv[uu][0] - mn0), exp2f(sv[uu][1] - mn1));  // t0
+            const uint32_t w1 = M::pack2(exp2f(sv[uu][2] - mn0), exp2f(sv[uu][3] - mn1));  // t1
+            ls0 += M::lo(w0) + M::lo(w1);
+            ls1 += M::hi(w0) + M::hi(w1);
             // P^T fragments (tokens x heads) from the S^T accumulator layout.
             pb[n][uu][0] = movmatrix_trans(w0);
             pb[n][uu][1] = movmatrix_trans(w1);
@@ -1125,8 +1203,8 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm)
 #pragma unroll
             for (int uu = 0; uu < NTP; ++uu) {
               uint32_t a0, a1, b0, b1, a2, a3, b2, b3;
-              widen_tokens<FP8, BF>(vw[uu][0][w], vw[uu][1][w], a0, a1, b0, b1);  // tokens 2t, +1
-              widen_tokens<FP8, BF>(vw[uu][2][w], vw[uu][3][w], a2, a3, b2, b3);  // 2t + 8, + 9
+              widen_tokens<FP8>(vw[uu][0][w], vw[uu][1][w], a0, a1, b0, b1);  // tokens 2t, +1
+              widen_tokens<FP8>(vw[uu][2][w], vw[uu][3][w], a2, a3, b2, b3);  // 2t + 8, + 9
 #pragma unroll
               for (int n = 0; n < NG; ++n) {
                 mma_16816<BF>(o[n][2 * w], a0, a1, a2, a3, pb[n][uu][0], pb[n][uu][1]);
@@ -1323,24 +1401,37 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
   }
 }
 
-template <class E, int D, bool BAL, int KVF, int NG>
+template <class E, int D, bool BAL, int KVF, int NG, bool WR = false>
 cudaError_t launch_kernel(const DecodeArgs &a, const DecodeParams &p, cudaStream_t stream) {
   using S = DecodeSmem<D, KVF != 0>;
   const int smem = S::bytes(a.num_seqs, p.max_ids);
-  auto kernel = decode_persistent_kernel<E, D, BAL, KVF, NG>;
-  cudaError_t e = allow_dynamic_smem<decode_persistent_kernel<E, D, BAL, KVF, NG>>();
+  auto kernel = decode_persistent_kernel<E, D, BAL, KVF, NG, WR>;
+  cudaError_t e = allow_dynamic_smem<decode_persistent_kernel<E, D, BAL, KVF, NG, WR>>();
   if (e != cudaSuccess) return e;
-  return launch_pdl(kernel, dim3(static_cast<unsigned>(a.grid)), dim3(kThreads), smem, stream,
+  return launch_pdl(kernel, dim3(static_cast<unsigned>(a.grid)), dim3(threads_for(WR)), smem,
+                    stream,
                     p, a.tm_k, a.tm_v);
 }
 
 // The decode kernel of the schedule, head-group width and head dim in `p`,
-// then (when pieces need combining) the merge kernel.
+// then (when pieces need combining) the merge kernel.  The one-call step
+// (p.nw > 0) is built for 16-bit pools and the balanced schedule; the
+// launcher sends every other step through a separate write launch.
 template <class E, int KVF>
 cudaError_t launch_family(const DecodeArgs &a, const DecodeParams &p, cudaStream_t stream) {
   cudaError_t e;
   const bool bal = p.balanced != 0, wide = p.hs > 8;
-  if (a.head_dim == 128) {
+  if (p.nw > 0) {
+    if constexpr (KVF != 0) {
+      return cudaErrorInvalidValue;
+    } else {
+      if (!bal) return cudaErrorInvalidValue;
+      e = a.head_dim == 128 ? (wide ? launch_kernel<E, 128, true, KVF, 2, true>(a, p, stream)
+                                    : launch_kernel<E, 128, true, KVF, 1, true>(a, p, stream))
+                            : (wide ? launch_kernel<E, 64, true, KVF, 2, true>(a, p, stream)
+                                    : launch_kernel<E, 64, true, KVF, 1, true>(a, p, stream));
+    }
+  } else if (a.head_dim == 128) {
     e = bal ? (wide ? launch_kernel<E, 128, true, KVF, 2>(a, p, stream)
                     : launch_kernel<E, 128, true, KVF, 1>(a, p, stream))
             : (wide ? launch_kernel<E, 128, false, KVF, 2>(a, p, stream)

@@ -357,7 +357,13 @@ pa_status decode_call(void *out, int64_t out_row_stride, const void *query, int6
   if (!valid_block_size(block_size)) return PA_ERR_UNSUPPORTED;
   if (num_blocks * block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
   if (partition_size % pa::kDecodeSub != 0) return PA_ERR_SHAPE;
-  if (num_seqs == 0) return PA_OK;
+  if (num_seqs == 0) {  // nothing to attend: only the step's write, if any
+    if (!write) return PA_OK;
+    pa::ReshapeArgs w = *write;
+    cudaError_t e = current_num_sms(&w.num_sms);
+    if (e == cudaSuccess) e = pa::launch_reshape_and_cache(w, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+  }
   if (!out || !query || !key_cache || !value_cache || !block_table || !context_lens)
     return PA_ERR_NULL;
   const int64_t qrow = static_cast<int64_t>(num_q_heads) * head_dim;
@@ -454,25 +460,26 @@ pa_status decode_call(void *out, int64_t out_row_stride, const void *query, int6
   a.kv_fp8 = int8 && fp8;
   a.k_scale = k_scale;
   a.v_scale = v_scale;
-  a.after_write = false;
-  if (write) {
+  if (write && (!balanced || int8)) {
+    // Fixed partitions or one-byte pools: the write is its own launch; the
+    // decode kernel reads context_lens, block_table and the query at once
+    // and waits for the write (programmatic dependent launch) only before
+    // its first K/V load.
     pa::ReshapeArgs w = *write;
     w.num_sms = a.num_sms;
     e = pa::launch_reshape_and_cache(w, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     a.after_write = true;
-    // One new token per sequence (token b of sequence b, the pages' decode
-    // step): the decode takes each sequence's newest row from the step's
-    // input and does not wait for the write.
-    if (w.num_tokens == num_seqs) {
-      a.fused = true;
-      a.new_k = w.key;
-      a.new_v = w.value;
-      a.new_stride = w.row_stride_bytes / 2;
-      a.slot_mapping = w.slot_mapping;
-      a.k_pool = key_cache;
-      a.v_pool = value_cache;
-    }
+  } else if (write) {
+    // 16-bit pools, balanced schedule: the step's cache write runs inside
+    // the decode launch.
+    a.num_new = write->num_tokens;
+    a.new_k = write->key;
+    a.new_v = write->value;
+    a.new_stride = write->row_stride_bytes / 2;
+    a.slot_mapping = write->slot_mapping;
+    a.k_pool = write->key_cache;
+    a.v_pool = write->value_cache;
   }
   e = pa::launch_decode(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);

@@ -114,9 +114,26 @@ __device__ __forceinline__ int checked_context_len(int len, int capacity, int hi
 // and reports PA_DEVERR_SCALE.
 __device__ __forceinline__ bool scale_ok(float s) { return s > 0.0f && s <= 3.4028234663852886e38f; }
 
-__device__ __forceinline__ uint32_t code8(float x, float s) {
+// x / s rounded to nearest (ties to even) in fp32, for a positive finite s
+// and its correctly rounded reciprocal r = RN(1/s): q0 = RN(x r) is within
+// an ulp of x / s, the remainder x - q0 s is exact with one fused
+// multiply-add, and RN(q0 + remainder * r) is then the correctly rounded
+// quotient (Markstein's division theorem; P. Markstein, IBM J. Res. Dev.
+// 34(1), 1990).  It holds while the quotient is a normal number; below that
+// the result is still within the subnormal range, and an infinite first
+// product is returned as is -- either way the codes built from it below are
+// those of the exactly rounded quotient.  The result takes x's sign (s > 0),
+// which a zero remainder step would otherwise lose for x = -0.
+__device__ __forceinline__ float div_rn_recip(float x, float s, float r) {
+  const float q0 = __fmul_rn(x, r);
+  if (isinf(q0)) return q0;
+  const float e = __fmaf_rn(-q0, s, x);
+  return copysignf(__fmaf_rn(e, r, q0), x);
+}
+
+__device__ __forceinline__ uint32_t code8(float x, float s, float r) {
   if (x != x) return 0u;
-  int c = __float2int_rn(__fdiv_rn(x, s));
+  int c = __float2int_rn(div_rn_recip(x, s, r));
   c = c > 127 ? 127 : (c < -127 ? -127 : c);
   return static_cast<uint32_t>(c) & 0xffu;
 }
@@ -125,28 +142,62 @@ __device__ __forceinline__ uint32_t code8(float x, float s) {
 // saturating at +-448) to x / scale, the division in fp32; NaN -> 0 (the same
 // reading of the pages' quantised-KV scales, with the OCP E4M3 format).  Two
 // values per conversion: `lo` in the low byte.
-__device__ __forceinline__ uint32_t fp8_pair(float lo, float hi, float s) {
-  const float a = lo != lo ? 0.0f : __fdiv_rn(lo, s);
-  const float b = hi != hi ? 0.0f : __fdiv_rn(hi, s);
-  uint16_t r;
+__device__ __forceinline__ uint32_t fp8_pair(float lo, float hi, float s, float r) {
+  const float a = lo != lo ? 0.0f : div_rn_recip(lo, s, r);
+  const float b = hi != hi ? 0.0f : div_rn_recip(hi, s, r);
+  uint16_t pair;
   // the first source goes to the upper byte
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
-  return r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(b), "f"(a));
+  return pair;
+}
+
+// 16 values with the plain division, for a subnormal scale (outside the
+// conditions of the reciprocal route above): kept out of line, it is never
+// the common path.
+template <class E, bool FP8>
+__device__ __noinline__ uint4 quant16_div(uint4 a, uint4 b, float s) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float v[4] = {E::lo(w[2 * q]), E::hi(w[2 * q]), E::lo(w[2 * q + 1]), E::hi(w[2 * q + 1])};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = v[k] != v[k] ? 0.0f : __fdiv_rn(v[k], s);
+    if constexpr (FP8) {
+      uint16_t lo, hi;
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(v[1]), "f"(v[0]));
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(v[3]), "f"(v[2]));
+      out[q] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    } else {
+      uint32_t c4 = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        int c = __float2int_rn(v[k]);
+        c = c > 127 ? 127 : (c < -127 ? -127 : c);
+        c4 |= (static_cast<uint32_t>(c) & 0xffu) << (8 * k);
+      }
+      out[q] = c4;
+    }
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
 // 16 values (two 16-byte vectors of fp16/bf16 pairs) -> 16 codes.
 template <class E, bool FP8>
 __device__ __forceinline__ uint4 quant16(const uint4 &a, const uint4 &b, float s) {
+  if (!(s >= 1.17549435e-38f)) return quant16_div<E, FP8>(a, b, s);  // subnormal scale
+  const float r = __frcp_rn(s);
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
   uint32_t out[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const uint32_t w0 = w[2 * q], w1 = w[2 * q + 1];
     if constexpr (FP8) {
-      out[q] = fp8_pair(E::lo(w0), E::hi(w0), s) | (fp8_pair(E::lo(w1), E::hi(w1), s) << 16);
+      out[q] = fp8_pair(E::lo(w0), E::hi(w0), s, r) |
+               (fp8_pair(E::lo(w1), E::hi(w1), s, r) << 16);
     } else {
-      out[q] = code8(E::lo(w0), s) | (code8(E::hi(w0), s) << 8) |
-               (code8(E::lo(w1), s) << 16) | (code8(E::hi(w1), s) << 24);
+      out[q] = code8(E::lo(w0), s, r) | (code8(E::hi(w0), s, r) << 8) |
+               (code8(E::lo(w1), s, r) << 16) | (code8(E::hi(w1), s, r) << 24);
     }
   }
   return make_uint4(out[0], out[1], out[2], out[3]);
@@ -264,6 +315,9 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
 // 4-byte asynchronous global -> shared copies (no register staging).
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_8(uint32_t dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
 }
 // 16-byte asynchronous global -> shared copy through L2 only.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {

@@ -114,15 +114,16 @@ struct DecodeArgs {
   // The previous kernel in the stream is this library's cache write, which
   // writes only K/V pool rows: the decode kernel may read everything else
   // before waiting for it.
-  bool after_write;
-  // ... and that write's token b is sequence b's newest row (num_new_tokens
-  // == num_seqs): the decode takes that row from new_k / new_v when
-  // slot_mapping[b] is its slot, and does not wait for the write.
-  bool fused = false;
+  bool after_write = false;
+  // The one-call step: the decode launch also writes num_new tokens' K/V
+  // rows (new_k / new_v, new_stride elements apart) into the pools at
+  // slot_mapping, and takes each sequence's newest row from the token
+  // written to it.
+  int32_t num_new = 0;
   const void *new_k = nullptr, *new_v = nullptr;
-  int64_t new_stride = 0;  // elements between tokens of new_k / new_v
+  int64_t new_stride = 0;
   const int64_t *slot_mapping = nullptr;
-  const void *k_pool = nullptr, *v_pool = nullptr;
+  void *k_pool = nullptr, *v_pool = nullptr;
   DecodeSlices slices;
   int32_t *d_error;
   pa_dtype dtype;

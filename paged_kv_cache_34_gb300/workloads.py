@@ -22,6 +22,14 @@ measured on (named by what they are):
                        bs 128, 4096-block pool, bf16, split-KV partitions of
                        512 tokens
 
+and one more shape for the chunked-prefill / multi-token-decode use of the
+prefill (q < L, bottom-right causal):
+
+  chunked-prefill      16 seqs, L ~ U[2048,8192], q cycling 1, 4, 64 (the
+                       newest q tokens of each context are the queries and
+                       this step's writes), causal, 32/8 heads, D 128,
+                       bs 128, 1024-block pool, bf16
+
 Values are N(0,1) drawn in fp32 by numpy's PCG64 and rounded to the config
 dtype (round-to-nearest-even, by torch's conversion).  Pool rows no sequence
 uses hold NaN, so a stray read of an unused slot poisons the output.
@@ -65,11 +73,16 @@ CONFIGS = {
         num_q_heads=64, num_kv_heads=8, head_dim=128, block_size=128,
         num_blocks=4096, placement="permutation", dtype="bf16",
         write_new_token=False, partition_size=512),
+    "chunked-prefill": dict(
+        kind="prefill", num_seqs=16, lengths=("uniform", 2048, 8192),
+        q_lens=("cycle", [1, 4, 64]), num_q_heads=32, num_kv_heads=8,
+        head_dim=128, block_size=128, num_blocks=1024,
+        placement="permutation", dtype="bf16", causal=True),
 }
 
-# Config order as the five workloads are listed; the seed is 1000 + index.
+# Config order as the workloads are listed; the seed is 1000 + index.
 ORDER = ["tiny-decode", "llama7b-decode", "continuous-batching",
-         "packed-prefill", "long-context-decode"]
+         "packed-prefill", "long-context-decode", "chunked-prefill"]
 
 TORCH_DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16}
 
@@ -203,7 +216,13 @@ def make_inputs(name_or_cfg, seed: int | None = None, *, lengths=None,
         else:
             nl = np.asarray(new_lens, np.int32)
     else:
-        ql = ctx.copy() if q_lens is None else np.asarray(q_lens, np.int32)
+        if q_lens is not None:
+            ql = np.asarray(q_lens, np.int32)
+        elif cfg.get("q_lens"):  # ("cycle", [a, b, ...]): sequence b gets entry b % len
+            vals = cfg["q_lens"][1]
+            ql = np.minimum(np.array([vals[b % len(vals)] for b in range(s)], np.int32), ctx)
+        else:
+            ql = ctx.copy()
         nl = ql.copy() if new_lens is None else np.asarray(new_lens, np.int32)
     assert np.all(nl <= ctx)
 

@@ -410,3 +410,36 @@ def test_decode_write_step_shapes(fmt, d, hq, hkv):
         assert np.array_equal(kd.cpu().numpy(), kc) and np.array_equal(vd.cpu().numpy(), vc)
         assert_close(out, oracle_decode8(fmt, x, kc, vc, ks, vs), x.dtype,
                      what=f"{fmt} step d{d} g{hq // hkv} P{part}")
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_quantiser_every_input_pattern(fmt, dtype):
+    """The write's quantiser over every 16-bit input pattern (NaN, infinities,
+    signed zeros and subnormals included) and scales from 2^-130 to 2^20,
+    odd mantissas among them: codes bit-identical to the oracle's, whose
+    quotient is the IEEE fp32 division x / scale."""
+    require_gpu()
+    pats = np.arange(65536, dtype=np.uint16)
+    t16 = TORCH16[oracle.F16 if dtype == "f16" else oracle.BF16]
+    x = torch.from_numpy(pats.view(np.int16)).view(t16)
+    hkv, d = 4, 128
+    rows = x.reshape(-1, hkv, d)                      # 128 tokens of 4 heads
+    n = rows.shape[0]
+    scales = [2.0 ** -130, 1.0e-38, 3.0e-12, 0.0123, 0.0078125, 1.0 / 3.0, 1.7, 1024.5,
+              2.0 ** 20]
+    for s in scales:
+        sc = torch.full((hkv,), s, dtype=torch.float32)
+        kd = torch.zeros((n, 1, hkv, d), dtype=torch.int8 if fmt == "int8" else torch.uint8,
+                         device="cuda")
+        vd = torch.zeros_like(kd)
+        slots = torch.arange(n, dtype=torch.int64, device="cuda")
+        GPU_WRITE[fmt](rows.cuda(), rows.flip(0).contiguous().cuda(), kd, vd, slots, sc.cuda(),
+                       sc.cuda())
+        torch.cuda.synchronize()
+        want = QUANTIZE[fmt](x, float(np.float32(s))).reshape(n, 1, hkv, d)
+        got = kd.cpu().numpy()
+        bad = np.flatnonzero(got.reshape(-1) != want.reshape(-1))
+        assert bad.size == 0, (f"{fmt} {dtype} scale {s}: {bad.size} codes differ, first input "
+                               f"pattern {int(pats[bad[0]]):#06x}")
+        assert np.array_equal(vd.cpu().numpy(), want[::-1])
