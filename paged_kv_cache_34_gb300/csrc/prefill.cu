@@ -262,8 +262,9 @@ __device__ PairItem item_at(const PrefillParams &p, int x, int lane, bool report
 }
 
 // D (head_dim) is 64 or 128: a Q, K or V tile row is D / 64 128-byte
-// halves; the shared-memory layout is the D = 128 one either way.
-template <class E, int D>
+// halves; the shared-memory layout is the D = 128 one either way.  SPEC:
+// the softmax for launches whose query tiles come one per item (see below).
+template <class E, int D, bool SPEC>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq,
                    const __grid_constant__ CUtensorMap tmk,
@@ -731,41 +732,91 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 128; ++c)
             if (c > bound) v[c] = __float_as_uint(-INFINITY);
         }
-        // Row max of the raw scores (scale > 0 keeps the order), as a tree.
-        float mx[8];
+        // P = 2^(s * scale*log2(e) - mu) for the row, rounded to the input
+        // type for the tensor core and packed two per word into pw; returns
+        // the row sum of the same rounded values (exactly widened), so O / l
+        // is an exact weighted mean of V under the rounded weights, and the
+        // row's largest scaled score in *tmax.
+        // With `store`, each 16 words go to TMEM as soon as they are made
+        // (the max is already known); otherwise all of them stay in pw.
+        // P overlays the first 64 columns of this tile's S in TMEM, two
+        // 16-bit values per column (the A operand of O += P V).  S(kt) being
+        // complete means PV(kt-1) has read P(kt-1): the tensor core runs one
+        // thread's MMAs in order.
+        uint32_t pw[64];
+        auto p_row = [&](float mu, float *tmax, bool store) -> float {
+          const uint64_t sl2 = f2_pack(sl, sl), nmu2 = f2_pack(-mu, -mu);
+          float rs[4] = {0.f, 0.f, 0.f, 0.f};
+          float mx[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(v[i]);
+          for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
 #pragma unroll
-        for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(v[c]));
-        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl;
-        const bool raise_max = mt > m_ref + kRescaleThreshold;
-        const float m_new = raise_max ? mt : m_ref;
-        const float corr = raise_max ? fast_exp2(m_ref - m_new) : 1.f;
-        const float mu = m_new == -INFINITY ? 0.f : m_new;
-        // p = 2^(s * scale*log2(e) - max), rounded to the input type for the
-        // tensor core; the row sum adds the same rounded values (exactly
-        // widened), so O / l is an exact weighted mean of V under the
-        // rounded weights.  S(kt) being complete means PV(kt-1) has read
-        // P(kt-1): the tensor core runs one thread's MMAs in order.
-        const uint64_t sl2 = f2_pack(sl, sl), nmu2 = f2_pack(-mu, -mu);
-        float rs[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int hf = 0; hf < 4; ++hf) {  // 32 columns -> 16 packed words
-          uint32_t pw[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const int i = hf * 16 + k;  // column pair
+          for (int i = 0; i < 64; ++i) {  // column pair
+            const float s0 = __uint_as_float(v[2 * i]), s1 = __uint_as_float(v[2 * i + 1]);
+            if (!store) mx[i & 3] = fmaxf(mx[i & 3], fmaxf(s0, s1));
             float x0f, x1f;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
-                             sl2, nmu2),
-                      x0f, x1f);
-            pw[k] = E::pack2(fast_exp2(x0f), fast_exp2(x1f));  // 2^-inf = 0 when masked
-            E::add_halves(pw[k], rs[(k & 1) * 2], rs[(k & 1) * 2 + 1]);
+            f2_unpack(f2_fma(f2_pack(s0, s1), sl2, nmu2), x0f, x1f);
+            pw[i] = E::pack2(fast_exp2(x0f), fast_exp2(x1f));  // 2^-inf = 0 when masked
+            E::add_halves(pw[i], rs[(i & 1) * 2], rs[(i & 1) * 2 + 1]);
+            if (store && (i & 15) == 15)
+              tmem_st16(s_tm + (i >> 4) * 16, *reinterpret_cast<uint32_t(*)[16]>(pw + i - 15));
           }
-          // P overlays the first 64 columns of this tile's S in TMEM, two
-          // 16-bit values per column (the A operand of O += P V).
-          tmem_st16(s_tm + hf * 16, pw);
+          *tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl;
+          return (rs[0] + rs[1]) + (rs[2] + rs[3]);
+        };
+        // The running max m_ref is only raised -- and O rescaled -- when the
+        // tile's max exceeds it by more than kRescaleThreshold (log2 units).
+        // SPEC (launches whose queries fit one 128-row tile per sequence:
+        // nothing else for the tensor core while this softmax runs): once a
+        // row has a finite running max, its exponentials start from it at
+        // once, the tile's max being found alongside them; the rare row whose
+        // max does jump reloads its scores (still in TMEM: P is stored only
+        // after this) and redoes them from the new max.  Otherwise (two query
+        // tiles, whose softmaxes alternate with each other's MMAs, or the
+        // row's first visible tile) the max comes first.  Measured, the early
+        // start only pays where the softmax is the whole critical path, and
+        // its code costs the other path when both are built in one kernel.
+        auto row_max = [&]() {
+          float mx[8];  // raw scores (scale > 0 keeps the order), as a tree
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(v[i]);
+#pragma unroll
+          for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(v[c]));
+          return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl;
+        };
+        bool raise_max;
+        float m_new, corr, rsum, mt;
+        // Both branches hold warp-collective TMEM loads and stores, so each
+        // is taken by the whole warp (a row for which the other branch would
+        // do gets the same result from this one).
+        if (!SPEC || __any_sync(0xffffffffu, m_ref == -INFINITY)) {
+          mt = row_max();
+          raise_max = mt > m_ref + kRescaleThreshold;  // false only for a fully masked row
+          m_new = raise_max ? mt : m_ref;
+          corr = raise_max ? fast_exp2(m_ref - m_new) : 1.f;
+          rsum = p_row(m_new == -INFINITY ? 0.f : m_new, &mt, true);
+        } else {
+          rsum = p_row(m_ref, &mt, false);
+          raise_max = mt > m_ref + kRescaleThreshold;
+          m_new = raise_max ? mt : m_ref;
+          corr = raise_max ? fast_exp2(m_ref - m_new) : 1.f;
+          if (__any_sync(0xffffffffu, raise_max)) {  // rows that keep m_ref redo the same P
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              tmem_ld32(s_tm + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
+            tmem_wait_ld();
+            if (edge) {
+#pragma unroll
+              for (int c = 0; c < 128; ++c)
+                if (c > bound) v[c] = __float_as_uint(-INFINITY);
+            }
+            rsum = p_row(m_new, &mt, true);
+          } else {
+#pragma unroll
+            for (int hf = 0; hf < 4; ++hf)
+              tmem_st16(s_tm + hf * 16, *reinterpret_cast<uint32_t(*)[16]>(pw + hf * 16));
+          }
         }
         tmem_wait_st();
         if (kt >= 1 && __any_sync(0xffffffffu, raise_max)) {
@@ -782,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
         }
-        l = l * corr + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+        l = l * corr + rsum;
         m_ref = m_new;
         tc_fence_before();
         __syncwarp();
@@ -881,11 +932,21 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
   p.num_items = static_cast<int32_t>(items);
   p.sched_slot = static_cast<int32_t>(g_prefill_launches.fetch_add(1) % kSchedSlots);
   const int64_t grid = items < a.num_sms ? items : a.num_sms;
+  // No sequence has more than one 128-row query tile (chunked prefill, a few
+  // new tokens per sequence): every item is a single tile.
+  if (a.max_seqlen_q <= 128) {
+    if (a.dtype == PA_BF16)
+      return a.head_dim == 64
+                 ? launch_variant<prefill_kernel<BF16, 64, true>>(p, a, grid, stream)
+                 : launch_variant<prefill_kernel<BF16, 128, true>>(p, a, grid, stream);
+    return a.head_dim == 64 ? launch_variant<prefill_kernel<F16, 64, true>>(p, a, grid, stream)
+                            : launch_variant<prefill_kernel<F16, 128, true>>(p, a, grid, stream);
+  }
   if (a.dtype == PA_BF16)
-    return a.head_dim == 64 ? launch_variant<prefill_kernel<BF16, 64>>(p, a, grid, stream)
-                            : launch_variant<prefill_kernel<BF16, 128>>(p, a, grid, stream);
-  return a.head_dim == 64 ? launch_variant<prefill_kernel<F16, 64>>(p, a, grid, stream)
-                          : launch_variant<prefill_kernel<F16, 128>>(p, a, grid, stream);
+    return a.head_dim == 64 ? launch_variant<prefill_kernel<BF16, 64, false>>(p, a, grid, stream)
+                            : launch_variant<prefill_kernel<BF16, 128, false>>(p, a, grid, stream);
+  return a.head_dim == 64 ? launch_variant<prefill_kernel<F16, 64, false>>(p, a, grid, stream)
+                          : launch_variant<prefill_kernel<F16, 128, false>>(p, a, grid, stream);
 }
 
 }  // namespace pa

@@ -154,3 +154,69 @@ def test_bad_block_id_flagged_not_faults():
     kp, vp = u16(xd.k_pool), u16(xd.v_pool)
     want = oracle_prefill(x, kp, vp, rows=np.arange(100))
     assert_close(out, want, x.dtype, rows=np.arange(100), what="unaffected sequence")
+
+
+def _prefill_with_hint(x, max_seqlen_q):
+    out = torch.empty_like(x.q)
+    pa.pa_prefill_varlen(out, x.q, x.k_pool, x.v_pool, x.block_table, x.cu_seqlens_q,
+                         x.context_lens, scale=x.scale, max_seqlen_q=max_seqlen_q,
+                         max_context_len=x.max_context_len, causal=x.causal)
+    return out
+
+
+def test_chunked_prefill_workload_full_size_every_row():
+    # The chunked-prefill workload (16 sequences, contexts of 2K-8K tokens, 1,
+    # 4 or 64 new queries each, GQA 4): every output row against the oracle.
+    # Its queries fit one 128-row tile per sequence, the launch shape whose
+    # softmax starts each row's exponentials from its running max.
+    x = W.make_inputs("chunked-prefill")
+    assert x.max_seqlen_q <= 128
+    _run(x, what="chunked-prefill")
+
+
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("causal", [True, False])
+def test_short_queries_grid(d, dtype, causal):
+    # Every sequence's queries fit one tile: q in 1..128 against longer
+    # contexts, ragged across block and tile edges, GQA 4.
+    lengths = [1, 128, 129, 300, 517, 1000, 64]
+    qlens = [1, 128, 7, 100, 128, 3, 64]
+    c = cfg(kind="prefill", hq=8, hkv=2, d=d, bs=16 if d == 64 else 128,
+            nb=sum(-(-n // 16) for n in lengths) + 8, dtype=dtype, lengths=lengths,
+            causal=causal)
+    x = W.make_inputs(c, seed=71 + d, q_lens=qlens, new_lens=qlens)
+    _run(x, what=f"short q d{d} {dtype} causal={causal}")
+
+
+@pytest.mark.parametrize("boost,dtype", [(20.0, "bf16"), (4.0, "f16")])
+def test_short_queries_equal_long_query_launch_bitwise(boost, dtype):
+    # max_seqlen_q is an upper bound: a hint above 128 runs the launch shape
+    # built for longer queries on the same inputs, and the two give the same
+    # bits -- including rows whose running max jumps by more than the rescale
+    # threshold in a later key tile (keys 256..299 scaled up), which makes the
+    # early-start softmax redo those rows' exponentials (in some rows of a
+    # warp and not others).  With the milder boost the scores stay spread
+    # enough for the stated fp16 bound against the oracle; with the strong one
+    # a few keys carry each row, and the rounding of P to bf16 alone can
+    # exceed that bound, so only the two launches are compared.
+    require_gpu()
+    lengths = [700, 400, 1000]
+    qlens = [64, 128, 5]
+    c = cfg(kind="prefill", hq=8, hkv=2, d=128, bs=32, nb=80, dtype=dtype, lengths=lengths)
+    x = W.make_inputs(c, seed=73, q_lens=qlens, new_lens=qlens)
+    kp = x.k_pool.clone()
+    for b in range(len(lengths)):
+        for j in range(256, 300):
+            blk = int(x.block_table[b, j // 32])
+            kp[blk, j % 32] = kp[blk, j % 32] * boost
+    x.k_pool = kp
+    xd = x.to("cuda")
+    gpu_write(xd)
+    short = _prefill_with_hint(xd, 128)
+    long = _prefill_with_hint(xd, 129)
+    torch.cuda.synchronize()
+    assert torch.equal(short.view(torch.int16), long.view(torch.int16))
+    if dtype == "f16":
+        kpo, vpo = u16(xd.k_pool), u16(xd.v_pool)
+        assert_close(short, oracle_prefill(x, kpo, vpo), x.dtype, what="max jumps")
