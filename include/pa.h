@@ -286,6 +286,21 @@ pa_status pa_decode_write(void *out, int64_t out_row_stride,
                           pa_dtype dtype, int32_t *d_error, void *stream);
 
 /*
+ * pa_debug_set_wait_limit_ns -- a testing aid; the pages have no
+ * counterpart.
+ *
+ * Sets the bound, in nanoseconds, of every pipeline wait (one warp waiting
+ * for another's data or buffer) in the kernels launched after the call,
+ * from any thread; 0 restores the default of 2 s.  A wait that runs out
+ * sets PA_DEVERR_TIMEOUT and its block returns, after waiting (with the full
+ * 2 s bound) for the copies it has in flight and freeing its tensor memory.
+ * A short bound lets a test run that recovery path without any fault: the
+ * outputs of launches whose waits ran out are unspecified, and the launches
+ * after them must be unaffected.
+ */
+void pa_debug_set_wait_limit_ns(uint64_t ns);
+
+/*
  * pa_decode_static_ws -- pa_decode for callers that cannot allocate.
  *
  * The pages have no counterpart to this entry point; it is a convenience of
@@ -307,6 +322,10 @@ pa_status pa_decode_write(void *out, int64_t out_row_stride,
  *  - partition_size == 0 uses pa_decode's automatic plan, lengthened (fewer
  *    partitions) until its workspace fits the array; an explicit
  *    partition_size whose workspace does not fit returns PA_ERR_WORKSPACE.
+ *    So does a shape that would fit only with partitions too long for the
+ *    decode kernel's shared memory (their block ids; many sequences of
+ *    long contexts at block_size 8 or 16): use pa_decode with a workspace.
+ *  - A failed lookup is recorded for pa_last_cuda_error().
  *  - All calls on a device share the array and leave their partial results
  *    in it (nothing in it has to start at zero).  Calls that may overlap on
  *    the GPU race on it: order them on one stream.

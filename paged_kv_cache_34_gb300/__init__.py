@@ -69,6 +69,8 @@ def library(path: str | None = None):
         lib.pa_abi_version.argtypes, lib.pa_abi_version.restype = [], I32
         lib.pa_status_string.argtypes, lib.pa_status_string.restype = [c.c_int], c.c_char_p
         lib.pa_last_cuda_error.argtypes, lib.pa_last_cuda_error.restype = [], I32
+        lib.pa_debug_set_wait_limit_ns.argtypes = [c.c_uint64]
+        lib.pa_debug_set_wait_limit_ns.restype = None
         lib.pa_reshape_and_cache.argtypes = [V, V, I64, V, V, V, I32, I32, I32, I32, I64,
                                              c.c_int, V, V]
         lib.pa_reshape_and_cache.restype = c.c_int
@@ -228,6 +230,12 @@ def pa_copy_blocks(key_cache, value_cache, block_mapping, *, d_error=None, strea
                             _ptr(block_mapping), block_mapping.numel() // 2, _ptr(d_error),
                             _stream(stream))
     _check(lib, st, "pa_copy_blocks")
+
+
+def pa_debug_set_wait_limit_ns(ns: int, *, lib=None):
+    """Bound (ns) of the kernels' pipeline waits for later launches; 0 = the
+    default 2 s.  A testing aid: lets a test make waits run out."""
+    (lib or library()).pa_debug_set_wait_limit_ns(int(ns))
 
 
 def pa_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,

@@ -60,6 +60,7 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
   p.k_scale = a.k_scale;
   p.v_scale = a.v_scale;
   p.err = a.d_error;
+  p.wait_ns = a.wait_ns;
   if (a.head_dim != 64 && a.head_dim != 128) return cudaErrorInvalidValue;
   const bool bf = a.dtype == PA_BF16;
   if (a.kv_int8 && a.kv_fp8)

@@ -137,6 +137,7 @@ struct DecodeParams {
   void *k_pool, *v_pool;
   int64_t num_slots;
   int32_t *err;
+  uint64_t wait_ns;  // bound of a pipeline wait
 };
 
 // One piece of work: tokens [start, end) of unit (sequence b, slice g) whose
@@ -627,7 +628,7 @@ __global__ void __launch_bounds__(threads_for(WR), kDecodeCtasPerSm)
         nbox += __shfl_xor_sync(0xffffffffu, nbox, o);
       bool ok = true;
       if (lane == 0 && c >= NS)
-        ok = mbar_wait_bounded(smem_u32(empty + s), ((c / NS) - 1) & 1);
+        ok = mbar_wait_bounded(smem_u32(empty + s), ((c / NS) - 1) & 1, p.wait_ns);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok || *s_abort) {
         if (lane == 0) {
@@ -644,6 +645,12 @@ __global__ void __launch_bounds__(threads_for(WR), kDecodeCtasPerSm)
         if (lane == 0) {
           s_hdr[s] = kTerminate;
           mbar_arrive(smem_u32(full + s));
+          // Leave only once the copies issued are in: a worker that gave up
+          // waiting (a timed-out wait) no longer holds the block open.  Stage
+          // c - NS was released by its consumers (the wait above), so its
+          // data had landed; its slot now holds the terminate phase.
+          for (int k = c - 1; k >= 0 && k > c - NS; --k)
+            mbar_wait_bounded(smem_u32(full + (k % NS)), (k / NS) & 1);
         }
         cp_async_wait_all();
         return;
@@ -993,7 +1000,7 @@ __global__ void __launch_bounds__(threads_for(WR), kDecodeCtasPerSm)
       active = begin();
       need_piece = false;
     }
-    if (!mbar_wait_bounded(smem_u32(full + s), (c / NS) & 1)) {
+    if (!mbar_wait_bounded(smem_u32(full + s), (c / NS) & 1, p.wait_ns)) {
       raise_error(p.err, PA_DEVERR_TIMEOUT);
       *s_abort = 1;
       break;

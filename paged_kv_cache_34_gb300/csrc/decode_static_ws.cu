@@ -28,6 +28,7 @@
 #include <mutex>
 
 #include "pa.h"
+#include "pa_internal.h"
 
 namespace {
 
@@ -75,8 +76,10 @@ pa_status pa_decode_static_ws(void *out, int64_t out_row_stride, const void *que
   // Pick a plan whose workspace fits the array.  An explicit partition size
   // that does not fit is an error.  When the automatic plan does not fit,
   // fixed partitions are used instead, grown (fewer partial results) until
-  // they fit; a partition at least as long as max_context_len needs no
-  // workspace at all, so the search always ends.
+  // they fit.  A partition at least as long as max_context_len needs no
+  // workspace at all, but a long partition needs more shared memory for its
+  // block ids: a shape that fits the array only with partitions the decode
+  // kernel cannot hold is refused with PA_ERR_WORKSPACE.
   int32_t part = 0;
   size_t need = 0;
   pa_status st = pa_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
@@ -84,22 +87,28 @@ pa_status pa_decode_static_ws(void *out, int64_t out_row_stride, const void *que
   if (st != PA_OK) return st;
   if (need > kStaticWorkspaceBytes) {
     if (partition_size != 0) return PA_ERR_WORKSPACE;
-    part = 64;
-    st = pa_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, part,
-                        &part, &need);
-    if (st != PA_OK) return st;
-    while (need > kStaticWorkspaceBytes) {
-      if (part >= max_context_len) return PA_ERR_WORKSPACE;  // unreachable: need is 0 there
-      part *= 2;
-      st = pa_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, part,
-                          &part, &need);
+    int64_t p64 = 64;
+    while (true) {
+      if (block_size > 0 &&
+          pa::decode_smem_bytes(head_dim, num_seqs, static_cast<int>(p64), block_size) >
+              227 * 1024)
+        return PA_ERR_WORKSPACE;
+      st = pa_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
+                          static_cast<int32_t>(p64), &part, &need);
       if (st != PA_OK) return st;
+      if (need <= kStaticWorkspaceBytes) break;
+      if (p64 >= max_context_len) return PA_ERR_WORKSPACE;  // need is 0 there: unreachable
+      p64 *= 2;
+      if (p64 > max_context_len) p64 = (static_cast<int64_t>(max_context_len) + 15) / 16 * 16;
     }
   }
   void *ws = nullptr;
   if (need > 0) {
     const cudaError_t e = static_workspace(&ws);
-    if (e != cudaSuccess) return PA_ERR_CUDA;
+    if (e != cudaSuccess) {
+      pa::record_cuda_error(e);
+      return PA_ERR_CUDA;
+    }
   }
   return pa_decode(out, out_row_stride, query, q_row_stride, key_cache, value_cache, block_table,
                    block_table_stride, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,

@@ -9,6 +9,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "pa.h"
@@ -133,11 +134,23 @@ int plan_partition(int num_seqs, int num_q_heads, int num_kv_heads, int max_ctx,
 
 }  // namespace
 
+namespace pa {
+void record_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int32_t>(e); }
+
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+uint64_t pipeline_wait_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+}  // namespace pa
+
 extern "C" {
 
 int32_t pa_abi_version(void) { return PA_ABI_VERSION; }
 
 int32_t pa_last_cuda_error(void) { return g_last_cuda_error; }
+
+void pa_debug_set_wait_limit_ns(uint64_t ns) {
+  pa::g_wait_ns.store(ns ? ns : pa::kDefaultWaitNs, std::memory_order_relaxed);
+}
 
 const char *pa_status_string(pa_status s) {
   switch (s) {
@@ -445,6 +458,7 @@ pa_status decode_call(void *out, int64_t out_row_stride, const void *query, int6
   }
   a.d_error = d_error;
   a.dtype = dtype;
+  a.wait_ns = pa::pipeline_wait_ns();
   a.box_rows = block_size < pa::kDecodeSub ? block_size : pa::kDecodeSub;
   // The item schedule keeps per-sequence prefix sums in shared memory.
   if (pa::decode_smem_bytes(head_dim, num_seqs, P, block_size, int8) > 227 * 1024)
@@ -683,6 +697,7 @@ pa_status pa_prefill_varlen(void *out, int64_t out_row_stride, const void *query
   a.causal = causal ? 1 : 0;
   a.d_error = d_error;
   a.dtype = dtype;
+  a.wait_ns = pa::pipeline_wait_ns();
   cudaError_t e = current_num_sms(&a.num_sms);
   if (e != cudaSuccess) return cuda_fail(e);
   const int64_t kv_rows = num_blocks * block_size;

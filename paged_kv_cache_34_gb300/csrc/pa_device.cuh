@@ -260,13 +260,16 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 // Waits for the phase of `bar` with the given parity to complete.  Returns
-// false if the bound was reached.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// false if the bound was reached.  Pipeline waits take the launch's bound
+// (kWaitLimitNs unless a test shortened it); waits for a block's own copies
+// in flight before it leaves keep kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t start = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - start > kWaitLimitNs) return false;
+    if (global_timer_ns() - start > limit_ns) return false;
   }
 }
 

@@ -134,8 +134,14 @@ struct DecodeArgs {
   bool kv_int8 = false;  // one-byte pools with per-KV-head scales
   bool kv_fp8 = false;   // ... holding E4M3 codes rather than INT8
   const float *k_scale = nullptr, *v_scale = nullptr;
+  uint64_t wait_ns = 0;  // bound of a pipeline wait (see pipeline_wait_ns)
 };
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+// Records a failed CUDA call for pa_last_cuda_error() (this thread).
+void record_cuda_error(cudaError_t e);
+// Bound of the kernels' pipeline waits for the next launches: 2 s, unless a
+// test shortened it through pa_debug_set_wait_limit_ns.
+uint64_t pipeline_wait_ns();
 size_t decode_smem_bytes(int head_dim, int num_seqs, int partition_size, int block_size,
                          bool kv_int8 = false);
 
@@ -158,6 +164,7 @@ struct PrefillArgs {
   pa_dtype dtype;
   CUtensorMap tm_q, tm_k, tm_v;
   int num_sms;
+  uint64_t wait_ns = 0;  // bound of a pipeline wait (see pipeline_wait_ns)
 };
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
 

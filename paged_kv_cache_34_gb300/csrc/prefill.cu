@@ -115,6 +115,7 @@ struct PrefillParams {
   int32_t num_items;
   int32_t sched_slot;
   int32_t *err;
+  uint64_t wait_ns;  // bound of a pipeline wait
 };
 
 // Work counters for the dynamic item schedule.  A launch uses one slot
@@ -292,7 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto take_item = [&](int j, int *x, PairItem *it) {
     const int slot = j % kItemRing;
     bool ok = true;
-    if (lane == 0) ok = mbar_wait_bounded(bar(kItemFull + slot), (j / kItemRing) & 1);
+    if (lane == 0)
+      ok = mbar_wait_bounded(bar(kItemFull + slot), (j / kItemRing) & 1, p.wait_ns);
     __syncwarp();
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     int v = -1;
@@ -308,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Lane 0 waits, the warp learns the outcome.
   auto warp_wait = [&](uint32_t b, uint32_t parity) {
     bool ok = true;
-    if (lane == 0) ok = mbar_wait_bounded(b, parity);
+    if (lane == 0) ok = mbar_wait_bounded(b, parity, p.wait_ns);
     return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
   };
 
@@ -362,7 +364,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Publish the item (or the end of the list) to the other roles.
         if (lane == 0) {
           if (j >= kItemRing)
-            ok = mbar_wait_bounded(bar(kItemEmpty + j % kItemRing), ((j / kItemRing) - 1) & 1);
+            ok = mbar_wait_bounded(bar(kItemEmpty + j % kItemRing), ((j / kItemRing) - 1) & 1,
+                                   p.wait_ns);
           if (it.seq >= 0 && ok) store_item(s_items + (j % kItemRing) * kItemWords, it);
           misc[8 + j % kItemRing] = it.seq >= 0 && ok ? x : -1;
           mbar_arrive(bar(kItemFull + j % kItemRing));
@@ -444,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int vn = kbase + it.nkv - 1;
           if (nfix > 0) ok = warp_wait(bar(kVFixFree), (nfix - 1) & 1);
           // every lane waits: each then writes into the landed tile
-          if (ok) ok = mbar_wait_bounded(bar(kKVFull + v_slot(vn)), v_par(vn));
+          if (ok) ok = mbar_wait_bounded(bar(kKVFull + v_slot(vn)), v_par(vn), p.wait_ns);
           ok = __all_sync(0xffffffffu, ok);
           if (ok) {
             uint8_t *vt = smem + kKVOff + v_slot(vn) * kTile;
@@ -467,7 +470,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok && lane == 0) {
         if (!misc[3]) raise_error(p.err, PA_DEVERR_TIMEOUT);
         misc[3] = 1;
-        // Do not leave while copies this CTA issued may still land.
+      }
+      // Do not leave while copies this CTA issued may still land (consumers
+      // that gave up waiting no longer hold the block open).
+      if (lane == 0) {
         if (nq > 0) mbar_wait_bounded(bar(kQFull), (nq - 1) & 1);
         for (int n = nk - 1; n >= 0 && n >= nk - kKBufs; --n)
           mbar_wait_bounded(bar(kKVFull + k_slot(n)), k_par(n));
@@ -625,9 +631,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         raise_error(p.err, PA_DEVERR_TIMEOUT);
         misc[3] = 1;
       }
-      // Every MMA issued above has completed once this barrier fires.
+      // Every MMA issued above has completed once this barrier fires (the
+      // full bound: TMEM is freed after it).
       commit(kFin);
-      warp_wait(bar(kFin), 0);
+      if (lane == 0) mbar_wait_bounded(bar(kFin), 0);
+      __syncwarp();
     }
   } else if (warp >= kEpiWarp0) {
     // ----------------------------------------------------- epilogue --
@@ -647,10 +655,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int t = 0; t < 2; ++t) {
         const int nkv_t = it.nkv_t[t];
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kOFull + t), j & 1));
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kOFull + t), j & 1, p.wait_ns));
         tc_fence_after();
         // every thread waits: each reads row sums another warp wrote
-        if (ok) ok = mbar_wait_bounded(bar(kLFull + t), j & 1);
+        if (ok) ok = mbar_wait_bounded(bar(kLFull + t), j & 1, p.wait_ns);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         const float l = l_buf[t * 128 + r];
@@ -709,14 +717,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok || x < 0) break;
       const int my_nkv = it.nkv_t[t];
       if (my_nkv == 0) {  // the MMA thread's empty S commit for this tile
-        ok = mbar_wait_bounded(bar(kSFull + t), n & 1);
+        ok = mbar_wait_bounded(bar(kSFull + t), n & 1, p.wait_ns);
         ++n;
         if (!ok) break;
       }
       const int lim = min(it.lim_base + it.row0[t] + r, it.L - 1);  // last visible key
       float m_ref = -INFINITY, l = 0.f;
       for (int kt = 0; kt < my_nkv; ++kt, ++n) {
-        ok = mbar_wait_bounded(bar(kSFull + t), n & 1);
+        ok = mbar_wait_bounded(bar(kSFull + t), n & 1, p.wait_ns);
         if (!ok) break;
         tc_fence_after();
         const int bound = lim - kt * 128;  // columns 0..bound are visible
@@ -921,6 +929,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
   p.scale_log2 = a.scale_log2;
   p.causal = a.causal;
   p.err = a.d_error;
+  p.wait_ns = a.wait_ns;
   // Pairs of query tiles: sum_b ceil(q_b / 256) is at most both bounds below;
   // items are (pair, head).  One persistent CTA per SM walks them.
   const int64_t max_pairs = (static_cast<int64_t>(a.max_seqlen_q) + 255) / 256;

@@ -6,7 +6,9 @@ owns every allocation, a plain C caller).  It must give the same results as
 pa_decode with an allocated workspace.  These tests call both through the C
 ABI on the same inputs, twice in a row with different inputs (the shared
 device array keeps the previous call's contents), and once where the
-automatic plan has to be lengthened to fit the array.
+automatic plan has to be lengthened to fit the array.  Each output is also
+checked against the fp64 oracle of the same step (its own write, then its
+decode) within the dtype's bound.
 
 This file is collected last on purpose: it also passes when run alone."""
 import ctypes
@@ -16,6 +18,7 @@ import pytest
 import torch
 
 import paged_kv_cache_34_gb300 as pa
+from gpu_util import assert_close, oracle_decode, oracle_pools_after_write
 from paged_kv_cache_34_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -51,12 +54,18 @@ def static_decode(lib, x, out, partition_size, err):
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
-def inputs(name, **kw):
+def inputs(name, with_oracle=True, **kw):
     """Seeded inputs with the step's new tokens already in the cache (decode
-    reads the cache after the write, so context_lens count them)."""
-    x = W.make_inputs(name, device="cuda", **kw)
+    reads the cache after the write, so context_lens count them), and the
+    oracle's output for them (from the host copies: the oracle's own write,
+    then its decode)."""
+    x_host = W.make_inputs(name, **kw)
+    x = x_host.to("cuda")
     if x.slot_mapping.numel():
         pa.pa_reshape_and_cache(x.k_new, x.v_new, x.k_pool, x.v_pool, x.slot_mapping)
+    if with_oracle:
+        kp, vp = oracle_pools_after_write(x_host)
+        x.want = oracle_decode(x_host, kp, vp)
     return x
 
 
@@ -77,6 +86,7 @@ def check(lib, x, partition_size=0):
     assert torch.isfinite(out).all()
     diff = (out.double() - want.double()).abs().max().item()
     assert diff <= TOL[x.dtype], f"max-abs difference {diff}"
+    assert_close(out, x.want, x.dtype, what="static workspace vs oracle")
     return out
 
 
@@ -112,7 +122,8 @@ def test_automatic_plan_falls_back_to_fixed_partitions_that_fit():
     assert need > STATIC_BYTES  # the automatic plan would not fit
     check(lib, x, partition_size=0)
     # an explicit partition size that does not fit is refused, not run
-    y = inputs("long-context-decode", lengths=[131072, 120000, 90000, 131000])
+    y = inputs("long-context-decode", with_oracle=False,
+               lengths=[131072, 120000, 90000, 131000])
     _, need64 = pa.pa_decode_plan(y.num_seqs, y.num_q_heads, y.num_kv_heads, y.head_dim,
                                   y.max_context_len, 64)
     assert need64 > STATIC_BYTES
