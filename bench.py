@@ -43,7 +43,7 @@ import torch  # noqa: E402
 HEADLINE = "llama7b-decode"
 METRIC = "paged-decode KV-read GB/s (% of HBM peak); varlen prefill TFLOP/s"
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
-HOST_LEAD_CYCLES = 200_000  # ~0.1 ms of device spin ahead of each timed step
+HOST_LEAD_CYCLES = 1_000_000  # ~0.5 ms of device spin ahead of each timed step
 
 
 # ---------------------------------------------------------------------------
@@ -157,12 +157,21 @@ def settle(step, seconds: float = 0.25):
         torch.cuda.synchronize()
 
 
+# seconds of untimed steps before each timed loop (0 in the --only profiling
+# mode, whose launch counts must be fixed)
+SETTLE_S = 0.25
+
+
 def time_steps(step, k, flush_buf, stream):
     """Per-step device time (ms) with CUDA events on the launching stream, L2
     flushed (untimed) before each step."""
-    settle(step)
+    if SETTLE_S > 0:
+        settle(step, SETTLE_S)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
+    for e in starts + ends:  # create the events now, not inside the timed loop
+        e.record(stream)
+    torch.cuda.synchronize()
     for i in range(k):
         flush_l2(flush_buf)
         # a short device-side spin before the start event, so the host has
@@ -596,11 +605,19 @@ def run_reference(args):
 
 
 def run_only(pa, W, args, flush_buf, stream):
-    """One kernel's workload alone, without the e2e, secondary and CPU legs."""
-    if args.only in ("decode", "long-context"):
-        name = HEADLINE if args.only == "decode" else "long-context-decode"
+    """One kernel's workload alone, without the e2e, secondary and CPU legs,
+    and with a fixed number of launches (a profiling target): W warm-up steps,
+    K timed steps, then K calls of the kernel alone."""
+    global SETTLE_S
+    SETTLE_S = 0.0
+    decode_only = {"decode": (HEADLINE, None), "long-context": ("long-context-decode", None),
+                   "continuous-batching": ("continuous-batching", None),
+                   "continuous-batching-g16": ("continuous-batching", {"num_q_heads": 128}),
+                   "tiny-decode": ("tiny-decode", None)}
+    if args.only in decode_only:
+        name, over = decode_only[args.only]
         x, _, _, part, nparts, _, t = bench_decode(pa, W, name, args.steps, args.warmup,
-                                                   flush_buf, stream)
+                                                   flush_buf, stream, overrides=over)
         ms = statistics.fmean(t)
         print(json.dumps({"only": args.only, "workload": name, "ms": round(ms, 5),
                           "GBps": round(decode_bytes(x) / (ms * 1e-3) / 1e9, 1),
@@ -620,10 +637,12 @@ def run_only(pa, W, args, flush_buf, stream):
         print(json.dumps({"only": "copy-blocks", "pairs": COPY_PAIRS, "ms": round(ms, 5),
                           "GBps": round(moved / (ms * 1e-3) / 1e9, 1)}))
     else:
-        x, _, t = bench_prefill(pa, W, args.steps, args.warmup, flush_buf, stream)
+        name = "chunked-prefill" if args.only == "chunked-prefill" else "packed-prefill"
+        x, _, t = bench_prefill(pa, W, args.steps, args.warmup, flush_buf, stream, name)
         ms = statistics.fmean(t)
-        print(json.dumps({"only": "prefill", "workload": "packed-prefill", "ms": round(ms, 5),
-                          "TFLOPs": round(prefill_flops(x) / (ms * 1e-3) / 1e12, 1)}))
+        print(json.dumps({"only": args.only, "workload": name, "ms": round(ms, 5),
+                          "TFLOPs": round(prefill_flops(x) / (ms * 1e-3) / 1e12, 1),
+                          "KV_GBps": round(kv_read_bytes(x) / (ms * 1e-3) / 1e9, 1)}))
 
 
 def main():
@@ -638,8 +657,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--only",
-                    choices=["decode", "long-context", "decode-int8", "decode-fp8", "copy-blocks",
-                             "prefill"],
+                    choices=["decode", "long-context", "continuous-batching",
+                             "continuous-batching-g16", "tiny-decode", "decode-int8",
+                             "decode-fp8", "copy-blocks", "prefill", "chunked-prefill"],
                     help="time one kernel's workload alone (a small profiling target)")
     args = ap.parse_args()
     if args.impl == "reference":

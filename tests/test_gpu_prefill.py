@@ -220,3 +220,19 @@ def test_short_queries_equal_long_query_launch_bitwise(boost, dtype):
     if dtype == "f16":
         kpo, vpo = u16(xd.k_pool), u16(xd.v_pool)
         assert_close(short, oracle_prefill(x, kpo, vpo), x.dtype, what="max jumps")
+
+
+def test_packed_prefill_gqa_full_size_sampled_rows():
+    # The packed-prefill workload's lengths and launch shape with 32 query
+    # heads over 8 KV heads (GQA 4), on the sampled rows.
+    x = W.make_inputs("packed-prefill", num_kv_heads=8)
+    _run(x, rows=sampled_rows(x.cu_seqlens_q.tolist()), what="packed-prefill GQA 4")
+
+
+def test_mid_size_packed_batch_every_row():
+    # Eight sequences of about 1000 tokens packed together, every row of
+    # every head against the oracle.
+    lengths = [1000, 873, 1111, 960, 1024, 777, 1200, 1050]
+    c = cfg(kind="prefill", hq=16, hkv=4, d=128, bs=64,
+            nb=sum(-(-n // 64) for n in lengths) + 4, dtype="bf16", lengths=lengths)
+    _run(W.make_inputs(c, seed=91), what="mid-size packed")
