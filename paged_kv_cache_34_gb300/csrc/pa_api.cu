@@ -77,7 +77,7 @@ EncodeTiledFn encode_fn() {
 // 64-byte swizzle at head_dim 64.
 bool encode_rows_map(CUtensorMap *map, const void *base, pa_dtype dtype, int head_dim,
                      int heads, int64_t rows, int64_t row_stride, int box_rows,
-                     bool int8 = false) {
+                     bool int8 = false, int box_heads = 1) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t eb = int8 ? 1 : 2;  // element bytes
@@ -85,7 +85,8 @@ bool encode_rows_map(CUtensorMap *map, const void *base, pa_dtype dtype, int hea
                               static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * eb,
                                  static_cast<cuuint64_t>(row_stride) * eb};
-  const cuuint32_t box[3] = {int8 ? static_cast<cuuint32_t>(head_dim) : 64u, 1,
+  const cuuint32_t box[3] = {int8 ? static_cast<cuuint32_t>(head_dim) : 64u,
+                             static_cast<cuuint32_t>(box_heads),
                              static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType dt = int8               ? CU_TENSOR_MAP_DATA_TYPE_UINT8
@@ -702,8 +703,12 @@ pa_status pa_prefill_varlen(void *out, int64_t out_row_stride, const void *query
   if (e != cudaSuccess) return cuda_fail(e);
   const int64_t kv_rows = num_blocks * block_size;
   const int64_t kv_stride = static_cast<int64_t>(num_kv_heads) * head_dim;
-  const int box = block_size;  // one box per block; the query tile is 128 rows
-  if (!encode_rows_map(&a.tm_q, query, dtype, head_dim, num_q_heads, total_q, q_row_stride, 128) ||
+  const int box = block_size;  // one box per block
+  // The query tile is 128 rows: 128 / pg tokens x the pg query heads of one
+  // KV head, the heads of a token adjacent.
+  a.packed_heads = pa::prefill_packed_heads(num_q_heads / num_kv_heads, max_seqlen_q);
+  if (!encode_rows_map(&a.tm_q, query, dtype, head_dim, num_q_heads, total_q, q_row_stride,
+                       128 / a.packed_heads, false, a.packed_heads) ||
       !encode_rows_map(&a.tm_k, key_cache, dtype, head_dim, num_kv_heads, kv_rows, kv_stride,
                        box) ||
       !encode_rows_map(&a.tm_v, value_cache, dtype, head_dim, num_kv_heads, kv_rows, kv_stride,

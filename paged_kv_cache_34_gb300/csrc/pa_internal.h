@@ -162,10 +162,21 @@ struct PrefillArgs {
   int32_t causal;
   int32_t *d_error;
   pa_dtype dtype;
+  // Query heads packed into a tile's rows (a power of two dividing 128 and
+  // the GQA group, or 1); tm_q's box is 64 x packed_heads x 128 / packed_heads.
+  int packed_heads = 1;
   CUtensorMap tm_q, tm_k, tm_v;
   int num_sms;
   uint64_t wait_ns = 0;  // bound of a pipeline wait (see pipeline_wait_ns)
 };
+// The query heads a prefill tile packs: the whole GQA group when it is a
+// power of two up to 128 (and the packed rows of the longest sequence fit in
+// int32), else 1.
+inline int prefill_packed_heads(int group, int max_seqlen_q) {
+  if (group < 1 || group > 128 || (group & (group - 1)) != 0) return 1;
+  if (static_cast<int64_t>(max_seqlen_q) * group > 0x3fffffff) return 1;
+  return group;
+}
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
 
 }  // namespace pa

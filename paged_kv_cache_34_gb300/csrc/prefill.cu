@@ -109,6 +109,10 @@ struct PrefillParams {
   int32_t capacity, max_ctx;
   int32_t num_seqs, total_q, max_seqlen_q;
   int32_t hq, group, block_size;
+  // Query heads packed into one tile's rows: a tile row is (token, head) =
+  // (row >> pg_log2, first head + (row & (pg - 1))), so the pg heads of one
+  // KV head share every K/V tile an item loads; hu = hq / pg head units.
+  int32_t pg, pg_log2, hu;
   int64_t num_blocks;
   float scale_log2;
   int32_t causal;
@@ -132,9 +136,10 @@ constexpr int kSchedSlots = 256;
 __device__ SchedSlot g_prefill_sched[kSchedSlots];
 
 // Item x of the work list: items are ordered by sequence, then pair of query
-// tiles (latest, i.e. heaviest, pair first), then query head.  The items of
-// one sequence are neighbours, so they run at about the same time and share
-// that sequence's K/V tiles in L2; heads of one KV group are neighbours too.
+// tiles (latest, i.e. heaviest, pair first), then head unit (pg query heads
+// of one KV head, packed into the tiles' rows).  The items of one sequence
+// are neighbours, so they run at about the same time and share that
+// sequence's K/V tiles in L2; head units of one KV group are neighbours too.
 // Warp-collective.
 __device__ void find_item(const PrefillParams &p, int x, int lane, int *seq_out, int *pair_out,
                           int *head_out) {
@@ -144,7 +149,7 @@ __device__ void find_item(const PrefillParams &p, int x, int lane, int *seq_out,
     int cnt = 0;
     if (s < p.num_seqs) {
       const int q = __ldg(p.cu + s + 1) - __ldg(p.cu + s);
-      if (q > 0 && q <= p.max_seqlen_q) cnt = ((q + 255) / 256) * p.hq;
+      if (q > 0 && q <= p.max_seqlen_q) cnt = (((q << p.pg_log2) + 255) / 256) * p.hu;
     }
     int incl = cnt;
 #pragma unroll
@@ -157,11 +162,11 @@ __device__ void find_item(const PrefillParams &p, int x, int lane, int *seq_out,
       const int src = __ffs(hit) - 1;
       const int cs = __shfl_sync(0xffffffffu, cnt, src);
       const int first = base + __shfl_sync(0xffffffffu, incl, src) - cs;
-      const int npairs = cs / p.hq;
+      const int npairs = cs / p.hu;
       const int rem = x - first;
       *seq_out = c0 + src;
-      *pair_out = npairs - 1 - rem / p.hq;
-      *head_out = rem % p.hq;
+      *pair_out = npairs - 1 - rem / p.hu;
+      *head_out = rem % p.hu;
       return;
     }
     base += __shfl_sync(0xffffffffu, incl, 31);
@@ -190,8 +195,9 @@ __device__ __forceinline__ uint32_t k_par(int kt) { return (kt / kKBufs) & 1; }
 __device__ __forceinline__ int v_slot(int kt) { return kKBufs + kt % kVBufs; }
 __device__ __forceinline__ uint32_t v_par(int kt) { return (kt / kVBufs) & 1; }
 
-// One work item: a (sequence, pair of query tiles, query head), with the
-// geometry every role derives from it.
+// One work item: a (sequence, pair of query tiles, head unit), with the
+// geometry every role derives from it.  Rows are packed (token, head) rows:
+// row0[t] is tile t's first, the sequence has q_len << pg_log2 of them.
 struct PairItem {
   int seq, h, q_start, q_len, L, lim_base;
   int row0[2], nkv_t[2], nkv;
@@ -249,16 +255,18 @@ __device__ PairItem item_at(const PrefillParams &p, int x, int lane, bool report
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       it.row0[t] = pair * 256 + t * 128;
-      if (it.row0[t] < it.q_len) {
+      if (it.row0[t] < (it.q_len << p.pg_log2)) {
+        // keys up to those of the tile's last token
         int kv_end = it.L;
-        if (p.causal) kv_end = min(it.L, it.L - it.q_len + it.row0[t] + 128);
+        if (p.causal)
+          kv_end = min(it.L, it.L - it.q_len + ((it.row0[t] + 127) >> p.pg_log2) + 1);
         if (kv_end < 0) kv_end = 0;
         it.nkv_t[t] = (kv_end + 127) / 128;
       }
     }
   }
   it.nkv = max(it.nkv_t[0], it.nkv_t[1]);
-  it.has_b = seq >= 0 && it.row0[1] < it.q_len;
+  it.has_b = seq >= 0 && it.row0[1] < (it.q_len << p.pg_log2);
   return it;
 }
 
@@ -375,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Claim the next item now; the answer is first needed next iteration.
         int x_next = 0;
         if (lane == 0) x_next = static_cast<int>(atomicAdd(&sched->next, 1u)) + gridDim.x;
-        const int g = it.h / p.group;
+        const int g = (it.h << p.pg_log2) / p.group;
         // Q of item j once the previous item's last QK has read Q.
         if (j > 0) ok = warp_wait(bar(kQEmpty), (j - 1) & 1);
         if (!ok || misc[3]) {
@@ -387,10 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int qtiles = it.nkv > 0 ? (it.has_b ? 2 : 1) : 0;
           mbar_arrive_expect_tx(bar(kQFull), qtiles * kHalves * kHalf);
           for (int t = 0; t < qtiles; ++t) {
-            tma_load_3d(qs + t * kTile, &tmq, bar(kQFull), 0, it.h, it.q_start + it.row0[t]);
-            if (kHalves == 2)
-              tma_load_3d(qs + t * kTile + kHalf, &tmq, bar(kQFull), 64, it.h,
-                          it.q_start + it.row0[t]);
+            // a box of 128 / pg tokens x pg heads: rows in (token, head) order
+            const int h0 = it.h << p.pg_log2, tok = it.q_start + (it.row0[t] >> p.pg_log2);
+            tma_load_3d(qs + t * kTile, &tmq, bar(kQFull), 0, h0, tok);
+            if (kHalves == 2) tma_load_3d(qs + t * kTile + kHalf, &tmq, bar(kQFull), 64, h0, tok);
           }
         }
         ++nq;
@@ -663,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         const float l = l_buf[t * 128 + r];
         const float inv_l = (nkv_t > 0 && l > 0.f) ? 1.f / l : 0.f;
-        const bool rows = it.row0[t] < it.q_len;
+        const bool rows = it.row0[t] < (it.q_len << p.pg_log2);
         uint32_t w[D / 2];  // the row of O / l, packed to the output type
         if (nkv_t > 0 && rows) {
 #pragma unroll
@@ -683,10 +691,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kOFree + t));  // O of this tile is free
-        const int64_t grow = static_cast<int64_t>(it.q_start) + it.row0[t] + r;
-        if (rows && it.row0[t] + r < it.q_len && grow >= 0 && grow < p.total_q) {
+        // tile row -> (token, query head)
+        const int prow = it.row0[t] + r;
+        const int tok = prow >> p.pg_log2;
+        const int head = (it.h << p.pg_log2) + (prow & (p.pg - 1));
+        const int64_t grow = static_cast<int64_t>(it.q_start) + tok;
+        if (rows && tok < it.q_len && grow >= 0 && grow < p.total_q) {
           typename E::T *orow =
-              static_cast<typename E::T *>(p.out) + grow * p.out_row_stride + it.h * D;
+              static_cast<typename E::T *>(p.out) + grow * p.out_row_stride + head * D;
 #pragma unroll
           for (int c = 0; c < D / 8; ++c)
             *reinterpret_cast<uint4 *>(orow + c * 8) =
@@ -721,7 +733,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++n;
         if (!ok) break;
       }
-      const int lim = min(it.lim_base + it.row0[t] + r, it.L - 1);  // last visible key
+      // last visible key of this row's token
+      const int lim = min(it.lim_base + ((it.row0[t] + r) >> p.pg_log2), it.L - 1);
       float m_ref = -INFINITY, l = 0.f;
       for (int kt = 0; kt < my_nkv; ++kt, ++n) {
         ok = mbar_wait_bounded(bar(kSFull + t), n & 1, p.wait_ns);
@@ -924,26 +937,30 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
   p.max_seqlen_q = a.max_seqlen_q;
   p.hq = a.num_q_heads;
   p.group = a.num_q_heads / a.num_kv_heads;
+  p.pg = a.packed_heads;
+  p.pg_log2 = 0;
+  while ((1 << p.pg_log2) < p.pg) ++p.pg_log2;
+  p.hu = p.hq / p.pg;
   p.block_size = a.block_size;
   p.num_blocks = a.num_blocks;
   p.scale_log2 = a.scale_log2;
   p.causal = a.causal;
   p.err = a.d_error;
   p.wait_ns = a.wait_ns;
-  // Pairs of query tiles: sum_b ceil(q_b / 256) is at most both bounds below;
-  // items are (pair, head).  One persistent CTA per SM walks them.
-  const int64_t max_pairs = (static_cast<int64_t>(a.max_seqlen_q) + 255) / 256;
-  int64_t slots = (static_cast<int64_t>(a.total_q) + 255LL * a.num_seqs) / 256;
+  // Pairs of query tiles: sum_b ceil(pg q_b / 256) is at most both bounds
+  // below; items are (pair, head unit).  One persistent CTA per SM walks them.
+  const int64_t max_pairs = ((static_cast<int64_t>(a.max_seqlen_q) << p.pg_log2) + 255) / 256;
+  int64_t slots = ((static_cast<int64_t>(a.total_q) << p.pg_log2) + 255LL * a.num_seqs) / 256;
   if (slots > a.num_seqs * max_pairs) slots = a.num_seqs * max_pairs;
   if (slots <= 0) return cudaSuccess;
-  const int64_t items = slots * a.num_q_heads;
+  const int64_t items = slots * p.hu;
   if (items > 0x7fffffff) return cudaErrorInvalidValue;
   p.num_items = static_cast<int32_t>(items);
   p.sched_slot = static_cast<int32_t>(g_prefill_launches.fetch_add(1) % kSchedSlots);
   const int64_t grid = items < a.num_sms ? items : a.num_sms;
   // No sequence has more than one 128-row query tile (chunked prefill, a few
   // new tokens per sequence): every item is a single tile.
-  if (a.max_seqlen_q <= 128) {
+  if ((static_cast<int64_t>(a.max_seqlen_q) << p.pg_log2) <= 128) {
     if (a.dtype == PA_BF16)
       return a.head_dim == 64
                  ? launch_variant<prefill_kernel<BF16, 64, true>>(p, a, grid, stream)

@@ -167,43 +167,49 @@ def _prefill_with_hint(x, max_seqlen_q):
 def test_chunked_prefill_workload_full_size_every_row():
     # The chunked-prefill workload (16 sequences, contexts of 2K-8K tokens, 1,
     # 4 or 64 new queries each, GQA 4): every output row against the oracle.
-    # Its queries fit one 128-row tile per sequence, the launch shape whose
-    # softmax starts each row's exponentials from its running max.
+    # The four query heads of a KV head share a tile (rows = token x head),
+    # so a sequence's 64 queries fill two tiles.
     x = W.make_inputs("chunked-prefill")
-    assert x.max_seqlen_q <= 128
+    assert x.max_seqlen_q * (x.num_q_heads // x.num_kv_heads) == 256
     _run(x, what="chunked-prefill")
 
 
 @pytest.mark.parametrize("d", [128, 64])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("causal", [True, False])
-def test_short_queries_grid(d, dtype, causal):
-    # Every sequence's queries fit one tile: q in 1..128 against longer
-    # contexts, ragged across block and tile edges, GQA 4.
+@pytest.mark.parametrize("hq,hkv,qmax", [(8, 8, 128), (8, 2, 32), (16, 2, 16), (8, 2, 128)])
+def test_short_queries_grid(d, dtype, causal, hq, hkv, qmax):
+    # Short queries against longer contexts, ragged across block and tile
+    # edges.  With qmax x (heads packed per KV head) <= 128 every sequence's
+    # rows fit one tile (the launch shape whose softmax starts each row's
+    # exponentials from its running max); the last case needs two.
     lengths = [1, 128, 129, 300, 517, 1000, 64]
-    qlens = [1, 128, 7, 100, 128, 3, 64]
-    c = cfg(kind="prefill", hq=8, hkv=2, d=d, bs=16 if d == 64 else 128,
+    qlens = [min(q, qmax) for q in (1, 128, 7, 100, 128, 3, 64)]
+    c = cfg(kind="prefill", hq=hq, hkv=hkv, d=d, bs=16 if d == 64 else 128,
             nb=sum(-(-n // 16) for n in lengths) + 8, dtype=dtype, lengths=lengths,
             causal=causal)
-    x = W.make_inputs(c, seed=71 + d, q_lens=qlens, new_lens=qlens)
-    _run(x, what=f"short q d{d} {dtype} causal={causal}")
+    x = W.make_inputs(c, seed=71 + d + hq + hkv, q_lens=qlens, new_lens=qlens)
+    _run(x, what=f"short q d{d} {dtype} causal={causal} {hq}/{hkv}")
 
 
-@pytest.mark.parametrize("boost,dtype", [(20.0, "bf16"), (4.0, "f16")])
-def test_short_queries_equal_long_query_launch_bitwise(boost, dtype):
-    # max_seqlen_q is an upper bound: a hint above 128 runs the launch shape
-    # built for longer queries on the same inputs, and the two give the same
-    # bits -- including rows whose running max jumps by more than the rescale
-    # threshold in a later key tile (keys 256..299 scaled up), which makes the
-    # early-start softmax redo those rows' exponentials (in some rows of a
-    # warp and not others).  With the milder boost the scores stay spread
-    # enough for the stated fp16 bound against the oracle; with the strong one
-    # a few keys carry each row, and the rounding of P to bf16 alone can
-    # exceed that bound, so only the two launches are compared.
+@pytest.mark.parametrize("boost,dtype,hkv", [(20.0, "bf16", 8), (4.0, "f16", 8),
+                                             (20.0, "bf16", 2), (4.0, "f16", 2)])
+def test_short_queries_equal_long_query_launch_bitwise(boost, dtype, hkv):
+    # max_seqlen_q is an upper bound: a hint above 128 / (heads packed per
+    # tile) runs the launch shape built for longer queries on the same
+    # inputs, and the two give the same bits -- including rows whose running
+    # max jumps by more than the rescale threshold in a later key tile (keys
+    # 256..299 scaled up), which makes the early-start softmax redo those
+    # rows' exponentials (in some rows of a warp and not others).  With the
+    # milder boost the scores stay spread enough for the stated fp16 bound
+    # against the oracle; with the strong one a few keys carry each row, and
+    # the rounding of P to bf16 alone can exceed that bound, so only the two
+    # launches are compared.
     require_gpu()
     lengths = [700, 400, 1000]
-    qlens = [64, 128, 5]
-    c = cfg(kind="prefill", hq=8, hkv=2, d=128, bs=32, nb=80, dtype=dtype, lengths=lengths)
+    pg = 8 // hkv
+    qlens = [min(q, 128 // pg) for q in (64, 128, 5)]
+    c = cfg(kind="prefill", hq=8, hkv=hkv, d=128, bs=32, nb=80, dtype=dtype, lengths=lengths)
     x = W.make_inputs(c, seed=73, q_lens=qlens, new_lens=qlens)
     kp = x.k_pool.clone()
     for b in range(len(lengths)):
@@ -213,8 +219,8 @@ def test_short_queries_equal_long_query_launch_bitwise(boost, dtype):
     x.k_pool = kp
     xd = x.to("cuda")
     gpu_write(xd)
-    short = _prefill_with_hint(xd, 128)
-    long = _prefill_with_hint(xd, 129)
+    short = _prefill_with_hint(xd, 128 // pg)
+    long = _prefill_with_hint(xd, 128 // pg + 1)
     torch.cuda.synchronize()
     assert torch.equal(short.view(torch.int16), long.view(torch.int16))
     if dtype == "f16":
@@ -236,3 +242,41 @@ def test_mid_size_packed_batch_every_row():
     c = cfg(kind="prefill", hq=16, hkv=4, d=128, bs=64,
             nb=sum(-(-n // 64) for n in lengths) + 4, dtype="bf16", lengths=lengths)
     _run(W.make_inputs(c, seed=91), what="mid-size packed")
+
+
+def _expanded_heads(x, g):
+    """The same batch with every KV head repeated for each of its g query
+    heads (num_kv_heads = num_q_heads): plain multi-head attention."""
+    y = x.to("cuda")
+    y.k_pool = x.k_pool.repeat_interleave(g, dim=2).contiguous()
+    y.v_pool = x.v_pool.repeat_interleave(g, dim=2).contiguous()
+    y.num_kv_heads = x.num_q_heads
+    return y
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 4), (8, 2), (16, 2), (32, 2), (128, 1), (12, 4)])
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("chunked", [False, True])
+def test_gqa_packed_rows_equal_expanded_heads_bitwise(hq, hkv, d, chunked):
+    # The query heads of a KV head share a tile's rows (token x head) when
+    # the group is a power of two; each row still sees exactly its own
+    # token's keys, in the same tiles and order, so the output equals that
+    # of the same batch with the KV heads repeated (one head per tile row
+    # block) bit for bit.  A group of 3 runs unpacked.  Lengths cross the
+    # packed tiles' 128- and 256-row edges.
+    require_gpu()
+    g = hq // hkv
+    lengths = [300, 129, 517, 64, 33] if chunked else [1, 5, 31, 33, 64, 100, 300]
+    qlens = [44, 129, 200, 1, 33] if chunked else lengths
+    c = cfg(kind="prefill", hq=hq, hkv=hkv, d=d, bs=32,
+            nb=sum(-(-n // 32) for n in lengths) + 3, dtype="bf16", lengths=lengths)
+    x = W.make_inputs(c, seed=300 + hq + hkv + d + chunked, q_lens=qlens, new_lens=qlens)
+    xd = x.to("cuda")
+    gpu_write(xd)
+    packed = gpu_prefill(xd)
+    expanded = gpu_prefill(_expanded_heads(xd, g))
+    torch.cuda.synchronize()
+    assert torch.equal(packed.view(torch.int16), expanded.view(torch.int16))
+    if hq == 16 and d == 128:
+        kp, vp = u16(xd.k_pool), u16(xd.v_pool)
+        assert_close(packed, oracle_prefill(x, kp, vp), x.dtype, what=f"GQA {g} packed")
