@@ -332,10 +332,11 @@ def bench_copy_blocks(pa, steps, warmup, flush_buf, stream):
     return moved, t
 
 
-def bench_prefill(pa, W, steps, warmup, flush_buf, stream, name="packed-prefill"):
+def bench_prefill(pa, W, steps, warmup, flush_buf, stream, name="packed-prefill",
+                  overrides=None):
     """A prefill step (this step's K/V rows written, then causal attention of
     the packed queries against the paged cache), and the prefill call alone."""
-    x = W.make_inputs(name, device="cuda")
+    x = W.make_inputs(name, device="cuda", **(overrides or {}))
     out = torch.empty_like(x.q)
 
     def pre():
@@ -638,7 +639,8 @@ def run_only(pa, W, args, flush_buf, stream):
                           "GBps": round(moved / (ms * 1e-3) / 1e9, 1)}))
     else:
         name = "chunked-prefill" if args.only == "chunked-prefill" else "packed-prefill"
-        x, _, t = bench_prefill(pa, W, args.steps, args.warmup, flush_buf, stream, name)
+        over = {"num_kv_heads": 8} if args.only == "prefill-gqa4" else None
+        x, _, t = bench_prefill(pa, W, args.steps, args.warmup, flush_buf, stream, name, over)
         ms = statistics.fmean(t)
         print(json.dumps({"only": args.only, "workload": name, "ms": round(ms, 5),
                           "TFLOPs": round(prefill_flops(x) / (ms * 1e-3) / 1e12, 1),
@@ -659,7 +661,8 @@ def main():
     ap.add_argument("--only",
                     choices=["decode", "long-context", "continuous-batching",
                              "continuous-batching-g16", "tiny-decode", "decode-int8",
-                             "decode-fp8", "copy-blocks", "prefill", "chunked-prefill"],
+                             "decode-fp8", "copy-blocks", "prefill", "chunked-prefill",
+                             "prefill-gqa4"],
                     help="time one kernel's workload alone (a small profiling target)")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -744,10 +747,13 @@ def main():
         if not args.no_secondary:
             sec = {}
             pre_hash = source_hash("prefill.cu", "pa_tcgen05.cuh", "pa_device.cuh")
-            # ---- prefill: packed (q = L) and chunked / multi-token (q < L)
-            for pname in ("packed-prefill", "chunked-prefill"):
+            # ---- prefill: packed (q = L; also with 32 query heads over 8 KV
+            # heads, packed four to a tile) and chunked / multi-token (q < L)
+            for pname, over in (("packed-prefill", None), ("chunked-prefill", None),
+                                ("packed-prefill", {"num_kv_heads": 8})):
+                key = pname + ("-gqa4" if over else "")
                 xp, t_pstep, t_pre = bench_prefill(pa, W, max(10, args.steps // 10), args.warmup,
-                                                   flush_buf, stream, pname)
+                                                   flush_buf, stream, pname, over)
                 fl = prefill_flops(xp)
                 ms_pre = statistics.fmean(t_pre)
                 tf = fl / (ms_pre * 1e-3) / 1e12
@@ -756,7 +762,8 @@ def main():
                     "value": round(tf, 2), "unit": "TFLOP/s", "flops": fl,
                     "kv_bytes": kvb, "ms_prefill": round(ms_pre, 5),
                     "ms_write_plus_prefill": round(statistics.fmean(t_pstep), 5),
-                    "q_lens": "q = L" if pname == "packed-prefill" else "1, 4, 64 cycling"}
+                    "q_lens": "q = L" if pname == "packed-prefill" else "1, 4, 64 cycling",
+                    "heads": f"{xp.num_q_heads}/{xp.num_kv_heads}"}
                 if pname == "packed-prefill":
                     entry["write_GBps"] = round(write_bytes(xp) / ((statistics.fmean(t_pstep)
                                                                     - ms_pre) * 1e-3) / 1e9, 1)
@@ -764,7 +771,7 @@ def main():
                         "bound": "tensor", "achieved": round(tf, 1), "peak": tf_peak,
                         "peak_kind": f"{peak_kind} bf16 burst", "unit": "TFLOP/s",
                         "frac": round(tf / tf_peak, 4),
-                        "traffic": recorded_traffic("pa_prefill_varlen", pname, pre_hash)}
+                        "traffic": recorded_traffic("pa_prefill_varlen", key, pre_hash)}
                 else:
                     # a few queries per sequence against long contexts: the
                     # K/V bytes, not the flops, set the bound
@@ -772,13 +779,13 @@ def main():
                     entry["roofline"] = {
                         "bound": "hbm", "achieved": round(gbp, 1), "peak": hbm_peak,
                         "unit": "GB/s", "frac": round(gbp / hbm_peak, 4),
-                        "traffic": recorded_traffic("pa_prefill_varlen", pname, pre_hash)}
+                        "traffic": recorded_traffic("pa_prefill_varlen", key, pre_hash)}
                 r, calls, th, el = oracle_prefill_rate(xp, ob)
                 entry["cpu_baseline"] = {"value": round(r, 6), "unit": "TFLOP/s", "cores": th,
                                          "kind": "oracle",
                                          "sample": f"{calls} oracle prefill calls on the last "
                                                    f"8 query rows of each sequence ({el:.1f} s)"}
-                sec[pname] = entry
+                sec[key] = entry
                 del xp
             # ---- 16-bit decodes: the other decode workloads (and a 16-query-
             # head group over the continuous-batching batch)
