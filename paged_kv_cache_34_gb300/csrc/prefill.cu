@@ -11,8 +11,11 @@
 // Design (the pages build a per-sequence mask from cu_seqlens on Ascend;
 // here nothing is masked outside the diagonal tiles and nothing is padded):
 //  * Work item = (two consecutive 128-row query tiles A and B of one
-//    sequence, query head).  Both tiles share every K/V tile loaded, halving
-//    the K/V traffic per flop.  One persistent CTA per SM claims items one
+//    sequence, head unit).  Both tiles share every K/V tile loaded, halving
+//    the K/V traffic per flop.  A head unit is one query head, or, when the
+//    GQA group is a power of two, all the query heads of one KV head: a tile
+//    row is then a (token, head) pair, so the group shares every K/V tile
+//    too.  One persistent CTA per SM claims items one
 //    at a time from a global counter, in an order that keeps one or two
 //    sequences in flight across the GPU (so each sequence's K/V comes from
 //    HBM once and is then reused from L2) and runs the heaviest items of a
