@@ -45,7 +45,7 @@ def _what(c, extra=""):
             f"L={c['lengths']} {extra}")
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(24))
 def test_random_decode(seed):
     require_gpu()
     r, c = _draw(1000 + seed, "decode")
@@ -62,7 +62,7 @@ def test_random_decode(seed):
     assert_close(out, want, x.dtype, what=_what(c, f"P{part}"))
 
 
-@pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("seed", range(12))
 def test_random_decode_step(seed):
     # the one-call step: this step's rows written, then the decode that reads
     # them; pools bit-exact, output against the oracle
@@ -85,7 +85,7 @@ def test_random_decode_step(seed):
 
 
 @pytest.mark.parametrize("fmt", ["int8", "fp8"])
-@pytest.mark.parametrize("seed", range(5))
+@pytest.mark.parametrize("seed", range(8))
 def test_random_decode_one_byte_pools(fmt, seed):
     r, c = _draw(5000 + seed, "decode")
     part = int(r.choice([0, 64]))
@@ -93,7 +93,7 @@ def test_random_decode_one_byte_pools(fmt, seed):
     check_decode8(fmt, x, part, _what(c, f"P{part}"))
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(24))
 def test_random_prefill(seed):
     require_gpu()
     r, c = _draw(7000 + seed, "prefill")
